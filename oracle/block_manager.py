@@ -1,0 +1,190 @@
+"""Model of the pages' host block manager, used to check the product's manager.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+What it follows, by page title and section:
+  [PidokuInfra 10]  "10 PagedAttention", section 4 "Tiny example": a stack of
+                    free block ids; Allocate(n) takes the top n entries in
+                    slice order and sets their refcount to 1, or fails with no
+                    state change when fewer than n are free; Free decrements
+                    each refcount and pushes a block back only when it reaches
+                    0; Fork increments every refcount and copies the table;
+                    BlocksNeeded = ceil(tokens / B); a sequence grows by one
+                    block when a token crosses a block boundary;
+                    PhysicalIndex = table[pos / B] * B + pos % B.
+  [nano-vLLM ch.04] "04 · PagedAttention", section 6 "Copy-on-write block
+                    sharing" and section 7 "The BlockManager in code": before a
+                    write into a block whose refcount is above 1, copy it,
+                    decrement the old block's refcount and give the copy to
+                    the writer; with refcount 1, write in place.
+  [tokentrails]     "PagedAttention", step 4: only a partly filled shared block
+                    is ever written, so only such a block is copied.
+
+Readings where the pages are silent or differ:
+  * The free order is a parameter (the stack's bottom first).  The default is
+    the Go constructor's: ids pushed from num_blocks-1 down to 0.
+  * A failed append (no free block for a new block or for a copy) changes no
+    state.  (The Go AppendToken bumps the length before allocating; the
+    nano-vLLM allocate() and the Go Allocate() change nothing on failure, and
+    that convention is taken for every call.)
+  * Copy-on-write: with refcount n on the written block, each of the first
+    n-1 writers copies, and the last one writes in place.
+"""
+
+
+class OracleBlockManager:
+    """Free list, refcounts, block tables and copy-on-write, in plain Python."""
+
+    def __init__(self, num_blocks, block_size, free_order=None):
+        if num_blocks < 0 or block_size <= 0:
+            raise ValueError("bad pool shape")
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+        if free_order is None:
+            self.free = list(range(num_blocks - 1, -1, -1))
+        else:
+            self.free = [int(b) for b in free_order]
+            if sorted(self.free) != list(range(num_blocks)):
+                raise ValueError("free_order must be a permutation of the pool's block ids")
+        self.ref = {}
+        self.tables = {}
+        self.lens = {}
+        self._next_seq = 0
+
+    # ---- block-level calls (PidokuInfra section 4) ----
+    def blocks_needed(self, tokens):
+        return (tokens + self.block_size - 1) // self.block_size
+
+    def allocate(self, n):
+        """Top n free ids in slice order, refcount 1; None (no change) when short."""
+        if len(self.free) < n:
+            return None
+        if n == 0:
+            return []
+        blocks = self.free[len(self.free) - n:]
+        del self.free[len(self.free) - n:]
+        for b in blocks:
+            self.ref[b] = 1
+        return list(blocks)
+
+    def free_blocks(self, blocks):
+        for b in blocks:
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                del self.ref[b]
+                self.free.append(b)
+
+    def fork_blocks(self, blocks):
+        for b in blocks:
+            self.ref[b] += 1
+        return list(blocks)
+
+    # ---- sequence-level calls ----
+    def new_sequence(self, prompt_len):
+        blocks = self.allocate(self.blocks_needed(prompt_len))
+        if blocks is None:
+            return None
+        seq = self._next_seq
+        self._next_seq += 1
+        self.tables[seq] = blocks
+        self.lens[seq] = int(prompt_len)
+        return seq
+
+    def append_token(self, seq):
+        """Make room for the next token of ``seq``.
+
+        Returns (slot, cow_pair) where cow_pair is (src, dst) or None, or None
+        when the pool has no block to give (no state change)."""
+        table = self.tables[seq]
+        pos = self.lens[seq]
+        logical = pos // self.block_size
+        pair = None
+        if pos % self.block_size == 0:
+            got = self.allocate(1)
+            if got is None:
+                return None
+            table.append(got[0])
+        else:
+            old = table[logical]
+            if self.ref[old] > 1:
+                got = self.allocate(1)
+                if got is None:
+                    return None
+                self.ref[old] -= 1
+                table[logical] = got[0]
+                pair = (old, got[0])
+        self.lens[seq] = pos + 1
+        return self.physical_index(seq, pos), pair
+
+    def fork(self, parent):
+        child = self._next_seq
+        self._next_seq += 1
+        self.tables[child] = self.fork_blocks(self.tables[parent])
+        self.lens[child] = self.lens[parent]
+        return child
+
+    def free_seq(self, seq):
+        if seq not in self.tables:
+            raise KeyError("unknown or already freed sequence %r" % (seq,))
+        self.free_blocks(self.tables.pop(seq))
+        del self.lens[seq]
+
+    def physical_index(self, seq, pos):
+        table = self.tables[seq]
+        return table[pos // self.block_size] * self.block_size + pos % self.block_size
+
+    def stats(self):
+        """(free, used, shared) block counts."""
+        shared = sum(1 for r in self.ref.values() if r > 1)
+        return len(self.free), self.num_blocks - len(self.free), shared
+
+
+def run_script(num_blocks, block_size, free_order, script):
+    """Run a workload's block-manager script: ("new", tokens), ("fork", parent),
+    ("append", seq, count).  Sequences are numbered in creation order.
+
+    Returns a dict with the manager, the final ``tables`` (list per sequence),
+    ``lens``, the ``slots`` of every appended token in script order, the
+    copy-on-write ``pairs`` in the order they were made, and
+    ``written_refcounts``: the refcount of each written block at write time."""
+    import numpy as np
+
+    m = OracleBlockManager(num_blocks, block_size, free_order)
+    slots, pairs, written_refs = [], [], []
+    for op in script:
+        if op[0] == "new":
+            if m.new_sequence(op[1]) is None:
+                raise RuntimeError("pool exhausted creating a sequence")
+        elif op[0] == "fork":
+            m.fork(op[1])
+        elif op[0] == "append":
+            for _ in range(op[2]):
+                got = m.append_token(op[1])
+                if got is None:
+                    raise RuntimeError("pool exhausted appending a token")
+                slot, pair = got
+                slots.append(slot)
+                written_refs.append(m.ref[slot // block_size])
+                if pair is not None:
+                    pairs.append(pair)
+        else:
+            raise ValueError("unknown op %r" % (op,))
+    order = sorted(m.tables)
+    return {
+        "manager": m,
+        "tables": [list(m.tables[s]) for s in order],
+        "lens": np.asarray([m.lens[s] for s in order], dtype=np.int32),
+        "slots": np.asarray(slots, dtype=np.int64),
+        "pairs": np.asarray(pairs, dtype=np.int32).reshape(-1, 2),
+        "written_refcounts": written_refs,
+    }
+
+
+def pad_tables(tables, max_blocks):
+    """Tables as an int32 [num_seqs, max_blocks] array, unused entries -1."""
+    import numpy as np
+
+    out = np.full((len(tables), max(1, max_blocks)), -1, dtype=np.int32)
+    for i, t in enumerate(tables):
+        out[i, :len(t)] = t
+    return out

@@ -1,0 +1,270 @@
+"""Seeded synthetic workloads for the paged-KV decode path.
+
+This module is shared by the tests, the benchmark and the smoke check, and by
+both sides of every parity check (the CUDA library and the CPU oracle).  It
+holds no arithmetic of the method itself: it draws sequence lengths, the order
+of the free list, a script of block-manager operations and random K/V/q
+values.  Block tables, slots and copy-on-write pairs are NOT computed here;
+each side derives them from the script with its own block manager.
+
+Workload shapes follow the pages' examples and the five benchmark workloads:
+  cfg0  fp32 tiny decode: lengths {5,16,23,40}, 4 q heads = 4 KV heads,
+        head_dim 64, block_size 4, pool of 32 blocks.
+  cfg1  bf16 MHA decode: 32 sequences, lengths uniform in [128, 2048],
+        32 = 32 heads, head_dim 128, block_size 16, pool 1.25x the need.
+  cfg2  bf16 GQA mixed lengths: 256 sequences, lognormal lengths (median 512,
+        sigma 1.0, clipped to [16, 8192]), 32 q / 8 KV heads, head_dim 128,
+        block_size 16, pool 1.1x the need.
+  cfg3  bf16 parallel sampling: 64 prompts of 2000 tokens (2008 in the
+        copy-on-write variant), each forked into 4 samples, each sample
+        appends 1..256 tokens; 32 q / 8 KV heads, head_dim 128, block_size 16.
+        The reduced twin uses 4 prompts of 192 tokens (200 for copy-on-write)
+        and appends of 1..40 tokens.
+  cfg4  bf16 long context: 16 sequences of 32768 tokens, 64 q / 8 KV heads,
+        head_dim 128, block_size 16 or 32, pool 1.05x the need.
+
+Conventions (readings of the workload text):
+  * Workload k is seeded with 1500 + k (numpy PCG64 for structure, a torch
+    generator on the target device for values).  Reduced-size variants used by
+    parity tests are seeded with 2500 + k.
+  * For decode workloads a sequence's stated length L counts the token written
+    in this step: the script creates it with L - 1 tokens, then appends one.
+  * Every pool element is N(0, 1), cast to the workload's element type
+    (round-to-nearest-even for bf16).  Blocks are placed by popping a
+    seed-shuffled free list (pop from the end).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import List, Optional, Tuple
+
+import numpy as np
+
+NEW = "new"        # ("new", prompt_len): create a sequence holding prompt_len tokens
+FORK = "fork"      # ("fork", parent): create a sequence sharing the parent's blocks
+APPEND = "append"  # ("append", seq, count): append count new tokens to seq
+
+
+@dataclass
+class Workload:
+    name: str
+    dtype: str                    # "f32" or "bf16"
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    seed: int
+    free_order: np.ndarray        # int32 [num_blocks]; the top of the stack is the last entry
+    script: List[Tuple]           # block-manager operations, in order
+    seq_lens: np.ndarray          # int32 [num_seqs]: final length of every sequence (decode order)
+    num_new_tokens: int           # rows of k/v written by this step (in script order)
+    note: str = ""
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def elem_bytes(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return max(1, -(-int(self.seq_lens.max(initial=0)) // self.block_size))
+
+    def kv_bytes_read(self) -> int:
+        """Bytes of K and V that one decode pass reads: sum_i L_i * Hk * D * 2 * elem."""
+        return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_dim * 2 * self.elem_bytes
+
+    def pool_bytes(self) -> int:
+        return 2 * self.num_blocks * self.block_size * self.num_kv_heads * self.head_dim * self.elem_bytes
+
+
+def _shuffled_free_order(rng: np.random.Generator, num_blocks: int) -> np.ndarray:
+    return rng.permutation(num_blocks).astype(np.int32)
+
+
+def decode_workload(name: str, lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                    block_size: int, dtype: str, seed: int, pool_factor: float = 1.0,
+                    num_blocks: Optional[int] = None, rng: Optional[np.random.Generator] = None,
+                    note: str = "") -> Workload:
+    """One decode step over independent sequences of the given final lengths.
+
+    Each sequence is created with L-1 tokens and then receives one new token
+    (the token this step writes); a length of 0 creates an empty sequence and
+    writes nothing."""
+    lens = np.asarray(lens, dtype=np.int32)
+    if rng is None:
+        rng = np.random.default_rng(seed)
+    need = int(sum(-(-int(L) // block_size) for L in lens))
+    if num_blocks is None:
+        num_blocks = max(1, int(math.ceil(pool_factor * need)))
+    free_order = _shuffled_free_order(rng, num_blocks)
+    script: List[Tuple] = []
+    for L in lens:
+        script.append((NEW, max(int(L) - 1, 0)))
+    ntok = 0
+    for i, L in enumerate(lens):
+        if L > 0:
+            script.append((APPEND, i, 1))
+            ntok += 1
+    return Workload(name, dtype, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                    seed, free_order, script, lens, ntok, note=note)
+
+
+def sampling_workload(name: str, num_prompts: int, prompt_len: int, samples: int,
+                      max_append: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                      block_size: int, dtype: str, seed: int, spare_blocks: int = 64) -> Workload:
+    """Parallel sampling: each prompt is forked into ``samples`` sequences that
+    share its blocks, then every sample appends U[1, max_append] tokens, in
+    sample order.  Decode runs over every sample."""
+    rng = np.random.default_rng(seed)
+    appends = rng.integers(1, max_append + 1, size=num_prompts * samples).astype(np.int32)
+    script: List[Tuple] = []
+    lens = []
+    seq = 0
+    sample_ids = []
+    for p in range(num_prompts):
+        parent = seq
+        script.append((NEW, prompt_len))
+        seq += 1
+        ids = [parent]
+        for _ in range(samples - 1):
+            script.append((FORK, parent))
+            ids.append(seq)
+            seq += 1
+        sample_ids.extend(ids)
+    for j, s in enumerate(sample_ids):
+        script.append((APPEND, s, int(appends[j])))
+        lens.append(prompt_len + int(appends[j]))
+    # Pool sizing: the prompt's blocks once, every sample's own growth, one
+    # private copy of a partly filled shared last block per sample, plus spare.
+    bs = block_size
+    prompt_blocks = -(-prompt_len // bs)
+    growth = sum(-(-(prompt_len + int(a)) // bs) - prompt_blocks for a in appends)
+    partial_copies = num_prompts * samples if prompt_len % bs else 0
+    num_blocks = num_prompts * prompt_blocks + growth + partial_copies + spare_blocks
+    free_order = _shuffled_free_order(rng, num_blocks)
+    return Workload(name, dtype, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                    seed, free_order, script, np.asarray(lens, dtype=np.int32),
+                    int(appends.sum()),
+                    note="%d prompts x %d samples, prompt %d, append U[1,%d]"
+                         % (num_prompts, samples, prompt_len, max_append),
+                    extra={"prompt_len": prompt_len, "samples": samples,
+                           "num_prompts": num_prompts})
+
+
+def workload(cfg: str, small: bool = False, block_size: Optional[int] = None,
+             prompt_len: Optional[int] = None) -> Workload:
+    """The named benchmark workload ("cfg0".."cfg4"), or its reduced-size twin.
+
+    ``block_size`` selects 16 or 32 for cfg4; ``prompt_len`` overrides cfg3's
+    prompt (2000 as written, 2008 for the copy-on-write variant)."""
+    k = int(cfg[-1])
+    seed = (2500 if small else 1500) + k
+    rng = np.random.default_rng(seed)
+    if k == 0:
+        return decode_workload("cfg0", [5, 16, 23, 40], 4, 4, 64, 4, "f32", seed,
+                               num_blocks=32, rng=rng, note="tiny fp32 decode")
+    if k == 1:
+        if small:
+            lens = rng.integers(128, 700, size=6)
+        else:
+            lens = rng.integers(128, 2049, size=32)
+        return decode_workload("cfg1" + ("-small" if small else ""), lens, 32, 32, 128, 16,
+                               "bf16", seed, pool_factor=1.25, rng=rng,
+                               note="MHA decode, lengths U[128,2048]")
+    if k == 2:
+        if small:
+            body = np.clip(np.rint(np.exp(rng.normal(math.log(160.0), 1.0, size=20))), 16, 1500)
+            lens = np.concatenate([[1, 15, 16, 17, 33], body]).astype(np.int32)
+        else:
+            lens = np.clip(np.rint(np.exp(rng.normal(math.log(512.0), 1.0, size=256))), 16, 8192)
+        return decode_workload("cfg2" + ("-small" if small else ""), lens.astype(np.int32), 32, 8,
+                               128, 16, "bf16", seed, pool_factor=1.1, rng=rng,
+                               note="GQA mixed lengths, lognormal(median 512, sigma 1)")
+    if k == 3:
+        if prompt_len is None:
+            prompt_len = 192 if small else 2000
+        if small:
+            return sampling_workload("cfg3-small-p%d" % prompt_len, 4, prompt_len, 4, 40, 32, 8,
+                                     128, 16, "bf16", seed, spare_blocks=8)
+        return sampling_workload("cfg3-p%d" % prompt_len, 64, prompt_len, 4, 256, 32, 8, 128, 16,
+                                 "bf16", seed)
+    if k == 4:
+        bs = block_size or 16
+        if small:
+            lens = [4096 + 5, 2 * bs + 3]
+        else:
+            lens = [32768] * 16
+        return decode_workload("cfg4-b%d" % bs + ("-small" if small else ""), lens, 64, 8, 128, bs,
+                               "bf16", seed, pool_factor=1.05, rng=rng,
+                               note="long-context decode, block_size %d" % bs)
+    raise ValueError("unknown workload %r" % cfg)
+
+
+# ---------------------------------------------------------------- values
+def torch_dtype(dtype: str):
+    import torch
+    return torch.float32 if dtype == "f32" else torch.bfloat16
+
+
+def _randn(shape, dtype: str, gen, device, chunk_elems: int = 1 << 27):
+    """N(0,1) fp32 draws cast to the element type, produced in chunks."""
+    import torch
+    out = torch.empty(shape, dtype=torch_dtype(dtype), device=device)
+    flat = out.view(-1)
+    total = flat.numel()
+    start = 0
+    while start < total:
+        n = min(chunk_elems, total - start)
+        flat[start:start + n].copy_(torch.randn(n, generator=gen, device=device, dtype=torch.float32))
+        start += n
+    return out
+
+
+def make_values(wl: Workload, device="cpu"):
+    """Random tensors for one step: q [N,H,D], k/v new rows [T,Hk,D] and the
+    pool caches [NB,B,Hk,D], all N(0,1) in the workload's element type."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(wl.seed)
+    cache_shape = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+    k_cache = _randn(cache_shape, wl.dtype, gen, device)
+    v_cache = _randn(cache_shape, wl.dtype, gen, device)
+    q = _randn((wl.num_seqs, wl.num_q_heads, wl.head_dim), wl.dtype, gen, device)
+    k_new = _randn((wl.num_new_tokens, wl.num_kv_heads, wl.head_dim), wl.dtype, gen, device)
+    v_new = _randn((wl.num_new_tokens, wl.num_kv_heads, wl.head_dim), wl.dtype, gen, device)
+    return {"q": q, "k": k_new, "v": v_new, "k_cache": k_cache, "v_cache": v_cache}
+
+
+def to_numpy_elems(t):
+    """Host numpy view of a tensor's elements: float32, or uint16 bits for bf16."""
+    import torch
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def shard_sequences(seq_bytes, world_size: int):
+    """Greedy longest-first split of sequences over ranks by their KV bytes.
+
+    Returns a list (one per rank) of sequence index arrays.  Ranks share no
+    sequence, and every sequence goes to exactly one rank."""
+    seq_bytes = np.asarray(seq_bytes, dtype=np.int64)
+    order = np.argsort(-seq_bytes, kind="stable")
+    loads = np.zeros(world_size, dtype=np.int64)
+    parts: List[list] = [[] for _ in range(world_size)]
+    for i in order:
+        r = int(np.argmin(loads))
+        parts[r].append(int(i))
+        loads[r] += seq_bytes[i]
+    return [np.asarray(sorted(p), dtype=np.int64) for p in parts]

@@ -1,0 +1,151 @@
+"""Pins for the oracle's block-manager model: the pages' worked examples,
+sharing counts, copy-on-write invariants and failure semantics."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_cache_150_gb300 import inputs
+
+
+def test_go_worked_example(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "go_worked_example.json")))
+    m = oracle.OracleBlockManager(g["num_blocks"], g["block_size"])
+    seqs = {}
+    for st in g["steps"]:
+        if st["op"] == "new":
+            s = m.new_sequence(st["tokens"])
+            assert s is not None
+            seqs[st["name"]] = s
+            if "expect_blocks" in st:
+                assert len(m.tables[s]) == st["expect_blocks"]
+        else:
+            m.free_seq(seqs[st["name"]])
+        free, used, _ = m.stats()
+        if "expect_free" in st:
+            assert free == st["expect_free"]
+        if "expect_used" in st:
+            assert used == st["expect_used"]
+    d = g["derived"]
+    assert m.tables[seqs["e"]] == d["table_e"]
+    assert m.tables[seqs["a"]] == d["table_a"] and m.tables[seqs["c"]] == d["table_c"]
+    assert m.physical_index(seqs["e"], 40) == d["physical_index_e_40"]
+
+
+def test_nano_vllm_free_list_pops_highest_first(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "slot_mapping_examples.json")))["free_list"]
+    m = oracle.OracleBlockManager(g["num_blocks"], 256, list(range(g["num_blocks"])))
+    s = m.new_sequence(1)
+    assert m.tables[s] == [g["first_pop"]]
+    m.free_seq(s)
+    assert m.free[-1] == g["first_pop"]
+
+
+def test_parallel_sampling_shares_prompt_blocks(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "sharing_examples.json")))["parallel_sampling"]
+    B = g["block_size"]
+    m = oracle.OracleBlockManager(len(g["free_order"]), B, g["free_order"])
+    parent = m.new_sequence(len(g["prompt_blocks"]) * B)
+    seqs = [parent] + [m.fork(parent) for _ in range(g["samples"] - 1)]
+    assert m.tables[parent] == g["prompt_blocks"]
+    assert all(m.ref[b] == g["prompt_refcount"] for b in g["prompt_blocks"])
+    pairs = []
+    for s in seqs:
+        slot, pair = m.append_token(s)
+        pairs.append(pair)
+    assert pairs == [None] * g["samples"]  # block-aligned prompt: no copy
+    assert [m.tables[s][-1] for s in seqs] == g["extra_blocks"]
+    free, used, shared = m.stats()
+    assert used == g["physical_blocks"]
+    unshared = sum(len(m.tables[s]) for s in seqs)
+    assert unshared == g["unshared_blocks"]
+    assert 1 - used / unshared == pytest.approx(g["saved_fraction"])
+    assert shared == len(g["prompt_blocks"])
+
+
+def test_three_requests_share_two_blocks(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "sharing_examples.json")))["three_requests"]
+    B = g["block_size"]
+    tail = list(reversed(g["new_blocks"])) + g["shared_blocks"]
+    top = max(tail) + 1
+    order = [b for b in range(top) if b not in tail] + tail
+    m = oracle.OracleBlockManager(top, B, order)
+    first = m.new_sequence(len(g["shared_blocks"]) * B)
+    seqs = [first] + [m.fork(first) for _ in range(g["requests"] - 1)]
+    assert m.stats()[1] == len(g["shared_blocks"])
+    assert all(m.ref[b] == g["shared_refcount"] for b in g["shared_blocks"])
+    for s in seqs:
+        m.append_token(s)
+    assert [m.tables[s][-1] for s in seqs] == g["new_blocks"]
+    assert all(m.tables[s][:2] == g["shared_blocks"] for s in seqs)
+    assert m.stats()[1] == g["distinct_blocks"]
+
+
+def _check_invariants(m):
+    free, used, _ = m.stats()
+    assert free + used == m.num_blocks
+    assert sum(m.ref.values()) == sum(len(t) for t in m.tables.values())
+    assert len(set(m.free)) == len(m.free) and not (set(m.free) & set(m.ref))
+
+
+@pytest.mark.parametrize("prompt_len,expect_pairs", [(192, 0), (200, 3)])
+def test_copy_on_write_in_parallel_sampling(prompt_len, expect_pairs):
+    wl = inputs.workload("cfg3", small=True, prompt_len=prompt_len)
+    r = oracle.run_script(wl.num_blocks, wl.block_size, wl.free_order, wl.script)
+    m = r["manager"]
+    prompts = wl.extra["num_prompts"]
+    assert len(r["pairs"]) == expect_pairs * prompts
+    assert all(ref == 1 for ref in r["written_refcounts"])  # no shared block written in place
+    dst = r["pairs"][:, 1].tolist()
+    assert len(set(dst)) == len(dst) and not (set(dst) & set(r["pairs"][:, 0].tolist()))
+    np.testing.assert_array_equal(r["lens"], wl.seq_lens)
+    _check_invariants(m)
+    if expect_pairs:
+        # the last writer of each shared partial block writes it in place
+        srcs = r["pairs"][:, 0]
+        for s in set(srcs.tolist()):
+            assert (srcs == s).sum() == wl.extra["samples"] - 1 and m.ref[s] == 1
+
+
+def _state(m):
+    return (list(m.free), dict(m.ref), {k: list(v) for k, v in m.tables.items()}, dict(m.lens))
+
+
+def test_allocation_failure_changes_nothing():
+    m = oracle.OracleBlockManager(3, 4)
+    m.new_sequence(8)  # 2 blocks used, 1 free
+    before = _state(m)
+    assert m.new_sequence(9) is None  # needs 3 blocks
+    assert _state(m) == before
+    m2 = oracle.OracleBlockManager(2, 4)
+    s = m2.new_sequence(6)  # partly filled last block, pool now empty
+    m2.fork(s)
+    before = _state(m2)
+    assert m2.append_token(s) is None  # a copy is needed and no block is free
+    assert _state(m2) == before
+    m3 = oracle.OracleBlockManager(1, 4)
+    s3 = m3.new_sequence(4)
+    before = _state(m3)
+    assert m3.append_token(s3) is None  # a new block is needed and none is free
+    assert _state(m3) == before
+
+
+def test_free_of_unknown_sequence_raises():
+    m = oracle.OracleBlockManager(4, 4)
+    s = m.new_sequence(4)
+    m.free_seq(s)
+    with pytest.raises(KeyError):
+        m.free_seq(s)
+
+
+def test_decode_workload_tables_cover_lengths():
+    for cfg in ("cfg0", "cfg1", "cfg2"):
+        wl = inputs.workload(cfg, small=True)
+        r = oracle.run_script(wl.num_blocks, wl.block_size, wl.free_order, wl.script)
+        np.testing.assert_array_equal(r["lens"], wl.seq_lens)
+        for L, t in zip(wl.seq_lens, r["tables"]):
+            assert len(t) == -(-int(L) // wl.block_size)
+        assert len(r["slots"]) == wl.num_new_tokens
+        _check_invariants(r["manager"])
