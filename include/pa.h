@@ -1,0 +1,249 @@
+/*
+ * pa.h - C ABI of libpa.so: paged-KV decode attention for NVIDIA GB300 (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *   [nano-vLLM ch.04]  "04 · PagedAttention", nano-vLLM Deep Dive
+ *   [PidokuInfra 10]   "10 PagedAttention", PidokuInfra inference engineering
+ *   [tokentrails]      "PagedAttention", tokentrails.org serving notes
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - KV cache layout (both K and V): [num_blocks, block_size, num_kv_heads,
+ *   head_dim], row-major, head_dim contiguous ([PidokuInfra 10] section 5
+ *   "The kernel side", comment on k_cache).  Token slot s of the pool is the
+ *   row k_cache[s / block_size, s % block_size, :, :].
+ * - Element types: PA_F32 (IEEE fp32) or PA_BF16 (bfloat16).  q, k, v, out
+ *   and both caches share the cache's element type.  Arithmetic is fp32.
+ * - Pointers named "device" must be CUDA device memory (or managed memory)
+ *   of the current device; "host" pointers are ordinary host memory.  The
+ *   caller owns every buffer.  The library never allocates device memory and
+ *   keeps no pointer after a call returns.
+ * - Work is enqueued on the caller's stream (NULL = legacy default stream).
+ *   No call synchronises, except pa_get_device_error.
+ * - Every call checks what the host can see (null pointers, shapes, sizes,
+ *   alignment, supported combinations) and returns a status without
+ *   launching anything when a check fails.  Nothing aborts the process.
+ *   Index errors that only the device can see (a slot or table entry outside
+ *   the pool, a length beyond the table) are skipped by the kernels and
+ *   recorded in a per-device error word read by pa_get_device_error.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* same type as cudaStream_t / CUstream */
+struct CUevent_st;  /* same type as cudaEvent_t / CUevent */
+typedef struct CUstream_st *pa_stream_t;
+typedef struct CUevent_st *pa_event_t;
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = -1,    /* null pointer, bad shape or size */
+    PA_ERR_UNSUPPORTED = -2,    /* valid request with no compiled kernel variant */
+    PA_ERR_CUDA = -3,           /* a CUDA runtime/driver call failed */
+    PA_ERR_NO_BLOCKS = -4,      /* block manager: the free list cannot satisfy the request */
+    PA_ERR_DEVICE_BOUNDS = -5,  /* a kernel met an index outside the pool or the table */
+    PA_ERR_DEVICE_TIMEOUT = -6, /* a kernel's bounded wait on an mbarrier ran out */
+    PA_ERR_WORKSPACE = -7       /* the decode workspace is smaller than required */
+} pa_status_t;
+
+typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1 } pa_dtype_t;
+
+/* Shape of the paged KV pool (host struct, read during the call only). */
+typedef struct pa_cache_desc {
+    int32_t num_blocks;   /* NB: physical blocks in the pool */
+    int32_t block_size;   /* B: tokens per block */
+    int32_t num_kv_heads; /* Hk */
+    int32_t head_dim;     /* D */
+    int32_t dtype;        /* pa_dtype_t */
+} pa_cache_desc_t;
+
+/* Human-readable name of a status code (static string). */
+const char *pa_status_string(pa_status_t status);
+
+/* Library version string (static). */
+const char *pa_version(void);
+
+/* ------------------------------------------------------------------------
+ * pa_reshape_and_cache - paged KV write.
+ *
+ * For every new token t with slot s = slot_mapping[t]:
+ *     k_cache[s / B, s % B, h, :] = k[t, h, :]   and the same for v,
+ * for every KV head h, as bit copies.  The slot is the one the block manager
+ * gives (physical_block * B + offset; [nano-vLLM ch.04] section 4,
+ * Mechanism 3 "The slot mapping"; [tokentrails] Code).
+ *
+ * k, v          device, [num_tokens, Hk, D], cache element type, contiguous.
+ * slot_mapping  device int32 [num_tokens].  A negative slot is padding and is
+ *               skipped.  A slot >= NB * B is skipped and recorded as
+ *               PA_ERR_DEVICE_BOUNDS.
+ * k_cache, v_cache  device, [NB, B, Hk, D]; written in place.
+ * Slots must be distinct (two tokens with one slot race).
+ * num_tokens == 0 is a no-op.  Pointers must be 16-byte aligned when a
+ * token row (Hk * D elements) is a multiple of 16 bytes.
+ * ---------------------------------------------------------------------- */
+pa_status_t pa_reshape_and_cache(const void *k, const void *v, const int32_t *slot_mapping,
+                                 int32_t num_tokens, void *k_cache, void *v_cache,
+                                 const pa_cache_desc_t *cache, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_copy_blocks - copy-on-write block copy.
+ *
+ * For every pair p: block dst = src_dst_pairs[2p + 1] of both caches becomes a
+ * bit copy of block src = src_dst_pairs[2p] (all B * Hk * D elements).  This is
+ * the copy made before a write into a block whose refcount is above one
+ * ([nano-vLLM ch.04] section 6 "Copy-on-write block sharing";
+ * [tokentrails] step 4 and Code; [PidokuInfra 10] section 5 "Copy-on-write
+ * sharing").
+ *
+ * src_dst_pairs  device int32 [num_pairs, 2].  Destinations must be distinct
+ *                and no destination may also be a source in the same call;
+ *                the result then does not depend on pair order.  The host
+ *                block manager only emits such pairs.  An id outside [0, NB)
+ *                skips the pair and is recorded as PA_ERR_DEVICE_BOUNDS.
+ * num_pairs == 0 is a no-op.
+ * ---------------------------------------------------------------------- */
+pa_status_t pa_copy_blocks(void *k_cache, void *v_cache, const pa_cache_desc_t *cache,
+                           const int32_t *src_dst_pairs, int32_t num_pairs, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_decode - single-query decode attention through block tables.
+ *
+ * For every sequence i and query head h (kv head kh = h / (H / Hk)):
+ *     out[i, h, :] = sum_j softmax_j(scale * q[i, h, :] . K_j) V_j,
+ * over positions j < seq_lens[i], where K_j, V_j are the cache rows of slot
+ * block_tables[i, j / B] * B + j % B ([PidokuInfra 10] section 4
+ * PhysicalIndex and section 5 "The kernel side"; [tokentrails] step 3: the
+ * same attention as over contiguous memory).  A sequence of length 0 gives
+ * an all-zero output.
+ *
+ * The work is split over a grid of persistent CTAs that share the flattened
+ * list of (KV-head group, sequence, block) evenly; a sequence cut between
+ * CTAs is merged by a rescaling reduce (running max and sum).
+ *
+ * out           device [num_seqs, H, D] (written).
+ * q             device [num_seqs, H, D].
+ * block_tables  device int32 [num_seqs, max_blocks_per_seq]; entries past
+ *               ceil(seq_lens[i] / B) are never read.  An entry outside
+ *               [0, NB) reads zeros and is recorded as PA_ERR_DEVICE_BOUNDS.
+ * seq_lens      device int32 [num_seqs], each in [0, max_blocks_per_seq * B];
+ *               an out-of-range length counts as 0 and is recorded.
+ * scale         multiplies q . k before the softmax (commonly 1/sqrt(D)).
+ * workspace     device scratch of at least pa_decode_workspace_bytes(...)
+ *               bytes with the same options, 256-byte aligned; its contents
+ *               need no initialisation and are garbage afterwards.  Calls that
+ *               share a workspace must be ordered on one stream.
+ * opts          optional (NULL = defaults), see pa_decode_opts_t.
+ * Requirements: H % Hk == 0, H / Hk <= 8, D in {64, 128, 256} (f32: {64, 128}),
+ *               num_seqs * max_blocks_per_seq < 2^31.
+ * ---------------------------------------------------------------------- */
+typedef enum pa_kernel {
+    PA_KERNEL_AUTO = 0, /* tensor-core kernel when it applies, else the CUDA-core one */
+    PA_KERNEL_SIMT = 1, /* CUDA-core kernel (fp32 and bf16) */
+    PA_KERNEL_MMA = 2   /* TMA + tensor-core kernel (bf16, D % 64 == 0, B % 16 == 0) */
+} pa_kernel_t;
+
+typedef struct pa_decode_opts {
+    int32_t num_splits; /* persistent CTAs sharing the work; 0 = one wave on this device */
+    int32_t kernel;     /* pa_kernel_t */
+    pa_event_t ev_partial_begin; /* optional: recorded just before the attention kernel */
+    pa_event_t ev_partial_end;   /* optional: recorded just after the attention kernel */
+} pa_decode_opts_t;
+
+size_t pa_decode_workspace_bytes(const pa_cache_desc_t *cache, int32_t num_seqs, int32_t num_heads,
+                                 const pa_decode_opts_t *opts);
+
+pa_status_t pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const pa_cache_desc_t *cache, const int32_t *block_tables,
+                      int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
+                      int32_t num_heads, float scale, void *workspace, size_t workspace_bytes,
+                      const pa_decode_opts_t *opts, pa_stream_t stream);
+
+/* Number of CTAs a default (num_splits = 0) decode launch uses on the current
+ * device for this shape, or a negative pa_status_t. */
+int32_t pa_decode_default_splits(const pa_cache_desc_t *cache, int32_t num_heads,
+                                 const pa_decode_opts_t *opts);
+
+/* Host mirror of the decode work split (the kernels use the same integer
+ * formulas): CTA c of num_splits owns flattened blocks [begin, end) of
+ * total_blocks; pa_split_owner gives the CTA that owns block x. */
+void pa_split_range(int64_t total_blocks, int32_t num_splits, int32_t c, int64_t *begin,
+                    int64_t *end);
+int32_t pa_split_owner(int64_t total_blocks, int32_t num_splits, int64_t x);
+
+/* ------------------------------------------------------------------------
+ * pa_get_device_error - synchronise `stream`, then read and clear the error
+ * word of the current device.  Returns PA_OK, PA_ERR_DEVICE_BOUNDS,
+ * PA_ERR_DEVICE_TIMEOUT or PA_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+pa_status_t pa_get_device_error(pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Host block manager (all host memory; not thread-safe per handle).
+ *
+ * A stack of free block ids, a refcount per block and a block table per
+ * sequence ([PidokuInfra 10] section 4 "Tiny example"; [nano-vLLM ch.04]
+ * sections 4 and 7):
+ * - allocation takes the top n ids of the stack in stack order and sets
+ *   their refcount to 1; a request the stack cannot meet returns
+ *   PA_ERR_NO_BLOCKS and changes nothing;
+ * - freeing decrements refcounts and pushes a block back only at 0;
+ * - fork copies a table and increments every refcount;
+ * - appending a token at position pos allocates a block when pos % B == 0;
+ *   otherwise, if the block holding pos has refcount > 1, it is copied first
+ *   (copy-on-write: a fresh block replaces it in this table, the old block's
+ *   refcount drops by one, and the (src, dst) pair is returned for
+ *   pa_copy_blocks), so a shared block is never written in place;
+ * - the slot of a token is table[pos / B] * B + pos % B (PhysicalIndex).
+ * Sequence ids are assigned 0, 1, 2, ... in creation order.
+ * ---------------------------------------------------------------------- */
+typedef struct pa_bm pa_bm_t;
+
+/* free_order (host, nullable): the initial stack, bottom first, a permutation
+ * of [0, num_blocks); the last entry is popped first.  NULL gives the stack
+ * num_blocks-1, ..., 1, 0 (block 0 on top).  Returns NULL on bad arguments or
+ * when num_blocks * block_size >= 2^31. */
+pa_bm_t *pa_bm_create(int32_t num_blocks, int32_t block_size, const int32_t *free_order);
+void pa_bm_destroy(pa_bm_t *bm);
+
+pa_status_t pa_bm_new_seq(pa_bm_t *bm, int32_t num_tokens, int32_t *seq_out);
+pa_status_t pa_bm_fork(pa_bm_t *bm, int32_t parent, int32_t *child_out);
+pa_status_t pa_bm_free_seq(pa_bm_t *bm, int32_t seq);
+
+/* Make room for the next token of seq.  slot_out receives its slot; cow_src /
+ * cow_dst receive the copy-on-write pair or -1 when no copy is needed. */
+pa_status_t pa_bm_append_token(pa_bm_t *bm, int32_t seq, int32_t *slot_out, int32_t *cow_src,
+                               int32_t *cow_dst);
+
+/* Append `count` tokens at once: all or nothing (PA_ERR_NO_BLOCKS leaves the
+ * state unchanged).  slots_out [count]; cow_pairs_out [2] receives at most one
+ * pair (only the first written block can be shared); *num_pairs_out is 0 or 1. */
+pa_status_t pa_bm_append_tokens(pa_bm_t *bm, int32_t seq, int32_t count, int32_t *slots_out,
+                                int32_t *cow_pairs_out, int32_t *num_pairs_out);
+
+pa_status_t pa_bm_seq_len(const pa_bm_t *bm, int32_t seq, int32_t *len_out,
+                          int32_t *num_blocks_out);
+pa_status_t pa_bm_block_table(const pa_bm_t *bm, int32_t seq, int32_t *out, int32_t capacity,
+                              int32_t *len_out);
+pa_status_t pa_bm_physical_index(const pa_bm_t *bm, int32_t seq, int32_t pos, int32_t *slot_out);
+pa_status_t pa_bm_refcount(const pa_bm_t *bm, int32_t block, int32_t *ref_out);
+pa_status_t pa_bm_stats(const pa_bm_t *bm, int32_t *free_out, int32_t *used_out,
+                        int32_t *shared_out);
+
+/* Export tables for a decode batch: tables_out [n, max_blocks] (host) padded
+ * with -1, lens_out [n]; PA_ERR_INVALID_ARG if a table is longer than
+ * max_blocks. */
+pa_status_t pa_bm_export(const pa_bm_t *bm, const int32_t *seqs, int32_t n, int32_t max_blocks,
+                         int32_t *tables_out, int32_t *lens_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

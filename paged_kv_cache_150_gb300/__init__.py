@@ -1,6 +1,300 @@
 """Paged-KV decode attention for NVIDIA GB300 (sm_103a).
 
-The compute path is the C-ABI library ``libpa.so`` (hand-written CUDA); this
-package only marshals arguments to it.  The library is loaded on first use, and
-every call fails loudly when it is missing.
+The compute path is the C-ABI library ``libpa.so`` (hand-written CUDA, see
+include/pa.h).  This package only marshals arguments to it: tensors must
+already live on the GPU, and every call runs on torch's current stream.  The
+library is loaded on first use; a missing library raises, there is no
+fallback.
+
+Calls (same names as the C ABI):
+  pa_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache)
+  pa_copy_blocks(k_cache, v_cache, src_dst_pairs)
+  pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, ...)
+  pa_get_device_error()
+  BlockManager: the host block manager (free list, refcounts, fork,
+  copy-on-write, slot mapping).
 """
+import ctypes
+
+import numpy as np
+
+from . import _lib
+from ._lib import (PA_BF16, PA_F32, PA_KERNEL_AUTO, PA_KERNEL_MMA, PA_KERNEL_SIMT, PA_OK,
+                   PagedAttentionError)
+
+_KERNELS = {"auto": PA_KERNEL_AUTO, "simt": PA_KERNEL_SIMT, "mma": PA_KERNEL_MMA}
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return PA_F32
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    raise TypeError("element type must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _cache_desc(k_cache, v_cache):
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("caches must both be [num_blocks, block_size, num_kv_heads, head_dim]")
+    if k_cache.dtype != v_cache.dtype:
+        raise TypeError("k_cache and v_cache element types differ")
+    nb, bs, hk, d = k_cache.shape
+    return _lib.CacheDesc(nb, bs, hk, d, _dtype_code(k_cache))
+
+
+def _dev(t, name, dtype=None):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(_torch().cuda.current_stream().cuda_stream)
+
+
+def pa_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache):
+    """Write new tokens' K/V rows into the paged caches at their slots."""
+    torch = _torch()
+    desc = _cache_desc(k_cache, v_cache)
+    T = k.shape[0]
+    if k.shape != v.shape or k.shape[1:] != k_cache.shape[2:]:
+        raise ValueError("k, v must be [num_tokens, num_kv_heads, head_dim] matching the cache")
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must be [num_tokens]")
+    for name, t in (("k", k), ("v", v)):
+        if t.dtype != k_cache.dtype:
+            raise TypeError("%s element type differs from the cache" % name)
+    st = _lib.load().pa_reshape_and_cache(
+        _dev(k, "k"), _dev(v, "v"), _dev(slot_mapping, "slot_mapping", torch.int32), T,
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(desc), _stream())
+    _lib.check("pa_reshape_and_cache", st)
+
+
+def pa_copy_blocks(k_cache, v_cache, src_dst_pairs):
+    """Copy whole blocks: for each (src, dst) row of the int32 [P, 2] tensor."""
+    torch = _torch()
+    desc = _cache_desc(k_cache, v_cache)
+    pairs = src_dst_pairs.reshape(-1, 2) if src_dst_pairs.numel() else src_dst_pairs
+    P = pairs.shape[0] if pairs.numel() else 0
+    if P == 0:
+        return
+    st = _lib.load().pa_copy_blocks(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                                    ctypes.byref(desc), _dev(pairs, "src_dst_pairs", torch.int32), P,
+                                    _stream())
+    _lib.check("pa_copy_blocks", st)
+
+
+def _opts(num_splits, kernel, events):
+    o = _lib.DecodeOpts(int(num_splits), _KERNELS[kernel], None, None)
+    if events is not None:
+        o.ev_partial_begin = ctypes.c_void_p(events[0].cuda_event)
+        o.ev_partial_end = ctypes.c_void_p(events[1].cuda_event)
+    return o
+
+
+def pa_decode_workspace_bytes(k_cache, num_seqs, num_heads, num_splits=0, kernel="auto"):
+    desc = _cache_desc(k_cache, k_cache)
+    o = _opts(num_splits, kernel, None)
+    n = _lib.load().pa_decode_workspace_bytes(ctypes.byref(desc), int(num_seqs), int(num_heads),
+                                              ctypes.byref(o))
+    if n == 0:
+        raise PagedAttentionError("pa_decode_workspace_bytes", _lib.PA_ERR_UNSUPPORTED)
+    return int(n)
+
+
+def pa_decode_default_splits(k_cache, num_heads, kernel="auto"):
+    desc = _cache_desc(k_cache, k_cache)
+    o = _opts(0, kernel, None)
+    n = _lib.load().pa_decode_default_splits(ctypes.byref(desc), int(num_heads), ctypes.byref(o))
+    if n < 0:
+        raise PagedAttentionError("pa_decode_default_splits", n)
+    return int(n)
+
+
+def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None, workspace=None,
+              num_splits=0, kernel="auto", events=None):
+    """Decode attention through block tables; returns ``out`` [N, H, D].
+
+    ``events``: optional (begin, end) torch.cuda.Event pair recorded around the
+    attention kernel on the current stream."""
+    torch = _torch()
+    desc = _cache_desc(k_cache, v_cache)
+    N, H, D = q.shape
+    if D != k_cache.shape[3] or q.dtype != k_cache.dtype:
+        raise ValueError("q must be [num_seqs, num_heads, head_dim] in the cache's element type")
+    if block_tables.dim() != 2 or block_tables.shape[0] != N or seq_lens.shape != (N,):
+        raise ValueError("block_tables must be [num_seqs, max_blocks] and seq_lens [num_seqs]")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must match q")
+    o = _opts(num_splits, kernel, events)
+    lib = _lib.load()
+    need = lib.pa_decode_workspace_bytes(ctypes.byref(desc), N, H, ctypes.byref(o))
+    if need == 0:
+        raise PagedAttentionError("pa_decode_workspace_bytes", _lib.PA_ERR_UNSUPPORTED)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = lib.pa_decode(_dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                       ctypes.byref(desc), _dev(block_tables, "block_tables", torch.int32),
+                       block_tables.shape[1], _dev(seq_lens, "seq_lens", torch.int32), N, H,
+                       float(scale), _dev(workspace, "workspace"), workspace.numel(),
+                       ctypes.byref(o), _stream())
+    _lib.check("pa_decode", st)
+    return out
+
+
+def pa_get_device_error(raise_on_error=True):
+    """Synchronise the current stream and read/clear the device error word."""
+    st = _lib.load().pa_get_device_error(_stream())
+    if raise_on_error:
+        _lib.check("kernel", st)
+    return st
+
+
+def pa_split_range(total_blocks, num_splits, c):
+    b, e = ctypes.c_int64(), ctypes.c_int64()
+    _lib.load().pa_split_range(int(total_blocks), int(num_splits), int(c), ctypes.byref(b), ctypes.byref(e))
+    return b.value, e.value
+
+
+def pa_split_owner(total_blocks, num_splits, x):
+    return int(_lib.load().pa_split_owner(int(total_blocks), int(num_splits), int(x)))
+
+
+def _i32p(arr):
+    return arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+class BlockManager:
+    """Host block manager (C++ in libpa.so)."""
+
+    def __init__(self, num_blocks, block_size, free_order=None):
+        lib = _lib.load()
+        self._lib = lib
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+        if free_order is None:
+            h = lib.pa_bm_create(self.num_blocks, self.block_size, None)
+        else:
+            fo = np.ascontiguousarray(np.asarray(free_order, dtype=np.int32))
+            if fo.shape != (self.num_blocks,):
+                raise ValueError("free_order must hold num_blocks ids")
+            h = lib.pa_bm_create(self.num_blocks, self.block_size, _i32p(fo))
+        if not h:
+            raise ValueError("pa_bm_create rejected its arguments")
+        self._h = ctypes.c_void_p(h)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            self._lib.pa_bm_destroy(h)
+            self._h = None
+
+    def _call(self, name, *args):
+        st = getattr(self._lib, name)(self._h, *args)
+        _lib.check(name, st)
+
+    def new_seq(self, num_tokens):
+        s = ctypes.c_int32()
+        self._call("pa_bm_new_seq", int(num_tokens), ctypes.byref(s))
+        return s.value
+
+    def fork(self, parent):
+        s = ctypes.c_int32()
+        self._call("pa_bm_fork", int(parent), ctypes.byref(s))
+        return s.value
+
+    def free_seq(self, seq):
+        self._call("pa_bm_free_seq", int(seq))
+
+    def append_token(self, seq):
+        slot, src, dst = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        self._call("pa_bm_append_token", int(seq), ctypes.byref(slot), ctypes.byref(src), ctypes.byref(dst))
+        return slot.value, (None if src.value < 0 else (src.value, dst.value))
+
+    def append_tokens(self, seq, count):
+        slots = np.empty(max(int(count), 1), dtype=np.int32)
+        pair = np.full(2, -1, dtype=np.int32)
+        npairs = ctypes.c_int32()
+        self._call("pa_bm_append_tokens", int(seq), int(count), _i32p(slots), _i32p(pair), ctypes.byref(npairs))
+        return slots[:int(count)], (tuple(int(x) for x in pair) if npairs.value else None)
+
+    def seq_len(self, seq):
+        n, nb = ctypes.c_int32(), ctypes.c_int32()
+        self._call("pa_bm_seq_len", int(seq), ctypes.byref(n), ctypes.byref(nb))
+        return n.value
+
+    def block_table(self, seq):
+        n, nb = ctypes.c_int32(), ctypes.c_int32()
+        self._call("pa_bm_seq_len", int(seq), ctypes.byref(n), ctypes.byref(nb))
+        out = np.empty(max(nb.value, 1), dtype=np.int32)
+        ln = ctypes.c_int32()
+        self._call("pa_bm_block_table", int(seq), _i32p(out), out.shape[0], ctypes.byref(ln))
+        return out[:ln.value].tolist()
+
+    def physical_index(self, seq, pos):
+        s = ctypes.c_int32()
+        self._call("pa_bm_physical_index", int(seq), int(pos), ctypes.byref(s))
+        return s.value
+
+    def refcount(self, block):
+        r = ctypes.c_int32()
+        self._call("pa_bm_refcount", int(block), ctypes.byref(r))
+        return r.value
+
+    def stats(self):
+        """(free, used, shared) block counts."""
+        f, u, s = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        self._call("pa_bm_stats", ctypes.byref(f), ctypes.byref(u), ctypes.byref(s))
+        return f.value, u.value, s.value
+
+    def export(self, seqs, max_blocks):
+        """(tables int32 [n, max_blocks] padded with -1, lens int32 [n])."""
+        seqs = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+        n = seqs.shape[0]
+        tables = np.empty((max(n, 1), max(int(max_blocks), 1)), dtype=np.int32)
+        lens = np.empty(max(n, 1), dtype=np.int32)
+        self._call("pa_bm_export", _i32p(seqs), n, int(max_blocks), _i32p(tables), _i32p(lens))
+        return tables[:n], lens[:n]
+
+    def apply_script(self, script):
+        """Run a workload script ("new", tokens) / ("fork", parent) /
+        ("append", seq, count).  Returns (slots int32 [T], pairs int32 [P, 2]),
+        slots in script order and pairs in the order they were made."""
+        slots, pairs = [], []
+        for op in script:
+            if op[0] == "new":
+                self.new_seq(op[1])
+            elif op[0] == "fork":
+                self.fork(op[1])
+            elif op[0] == "append":
+                s, pair = self.append_tokens(op[1], op[2])
+                slots.append(s)
+                if pair is not None:
+                    pairs.append(pair)
+            else:
+                raise ValueError("unknown op %r" % (op,))
+        slots = np.concatenate(slots).astype(np.int32) if slots else np.zeros(0, np.int32)
+        return slots, np.asarray(pairs, dtype=np.int32).reshape(-1, 2)
+
+
+def version():
+    return _lib.load().pa_version().decode()
+
+
+__all__ = [
+    "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_workspace_bytes",
+    "pa_decode_default_splits", "pa_get_device_error", "pa_split_range", "pa_split_owner",
+    "BlockManager", "PagedAttentionError", "version",
+]

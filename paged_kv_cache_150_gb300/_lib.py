@@ -1,0 +1,104 @@
+"""ctypes declarations of the C ABI in include/pa.h (libpa.so, built in-tree).
+
+Loading fails loudly: there is no Python or CPU fallback for any call.
+"""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(HERE, "libpa.so")
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = -1
+PA_ERR_UNSUPPORTED = -2
+PA_ERR_CUDA = -3
+PA_ERR_NO_BLOCKS = -4
+PA_ERR_DEVICE_BOUNDS = -5
+PA_ERR_DEVICE_TIMEOUT = -6
+PA_ERR_WORKSPACE = -7
+
+PA_F32 = 0
+PA_BF16 = 1
+
+PA_KERNEL_AUTO = 0
+PA_KERNEL_SIMT = 1
+PA_KERNEL_MMA = 2
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+class DecodeOpts(ctypes.Structure):
+    _fields_ = [("num_splits", ctypes.c_int32), ("kernel", ctypes.c_int32),
+                ("ev_partial_begin", ctypes.c_void_p), ("ev_partial_end", ctypes.c_void_p)]
+
+
+# symbol -> (restype, argtypes)
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_PI32 = ctypes.POINTER(ctypes.c_int32)
+_PI64 = ctypes.POINTER(ctypes.c_int64)
+_DESC = ctypes.POINTER(CacheDesc)
+_OPTS = ctypes.POINTER(DecodeOpts)
+
+SIGNATURES = {
+    "pa_status_string": (ctypes.c_char_p, [_I32]),
+    "pa_version": (ctypes.c_char_p, []),
+    "pa_reshape_and_cache": (_I32, [_P, _P, _P, _I32, _P, _P, _DESC, _P]),
+    "pa_copy_blocks": (_I32, [_P, _P, _DESC, _P, _I32, _P]),
+    "pa_decode_workspace_bytes": (ctypes.c_size_t, [_DESC, _I32, _I32, _OPTS]),
+    "pa_decode": (_I32, [_P, _P, _P, _P, _DESC, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P,
+                         ctypes.c_size_t, _OPTS, _P]),
+    "pa_decode_default_splits": (_I32, [_DESC, _I32, _OPTS]),
+    "pa_split_range": (None, [_I64, _I32, _I32, _PI64, _PI64]),
+    "pa_split_owner": (_I32, [_I64, _I32, _I64]),
+    "pa_get_device_error": (_I32, [_P]),
+    "pa_bm_create": (_P, [_I32, _I32, _PI32]),
+    "pa_bm_destroy": (None, [_P]),
+    "pa_bm_new_seq": (_I32, [_P, _I32, _PI32]),
+    "pa_bm_fork": (_I32, [_P, _I32, _PI32]),
+    "pa_bm_free_seq": (_I32, [_P, _I32]),
+    "pa_bm_append_token": (_I32, [_P, _I32, _PI32, _PI32, _PI32]),
+    "pa_bm_append_tokens": (_I32, [_P, _I32, _I32, _PI32, _PI32, _PI32]),
+    "pa_bm_seq_len": (_I32, [_P, _I32, _PI32, _PI32]),
+    "pa_bm_block_table": (_I32, [_P, _I32, _PI32, _I32, _PI32]),
+    "pa_bm_physical_index": (_I32, [_P, _I32, _I32, _PI32]),
+    "pa_bm_refcount": (_I32, [_P, _I32, _PI32]),
+    "pa_bm_stats": (_I32, [_P, _PI32, _PI32, _PI32]),
+    "pa_bm_export": (_I32, [_P, _PI32, _I32, _I32, _PI32, _PI32]),
+}
+
+_lib = None
+
+
+def load():
+    """The loaded libpa.so with argument types set.  Raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIBRARY):
+            raise RuntimeError(
+                "libpa.so is not built (%s). Run `python -c \"import __graft_entry__ as g; g.build()\"` "
+                "or `python paged_kv_cache_150_gb300/build.py`; there is no fallback path." % LIBRARY)
+        lib = ctypes.CDLL(LIBRARY)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, call, status):
+        self.status = int(status)
+        msg = load().pa_status_string(int(status))
+        super().__init__("%s failed: %s (%d)" % (call, msg.decode() if msg else "?", status))
+
+
+def check(call, status):
+    if status != PA_OK:
+        raise PagedAttentionError(call, status)

@@ -1,0 +1,237 @@
+// Host block manager: free list, refcounts, block tables, fork and
+// copy-on-write.  Pure host code; it feeds block tables and slot mappings to
+// the kernels.
+//
+// Follows "10 PagedAttention" (PidokuInfra), section 4 "Tiny example"
+// (stack of free ids, Allocate/Free/Fork/BlocksNeeded/AppendToken/
+// PhysicalIndex) and "04 · PagedAttention" (nano-vLLM Deep Dive), section 6
+// "Copy-on-write block sharing" and section 7 "The BlockManager in code"
+// (refcount > 1 means copy before writing; allocation failure is reported,
+// not raised).  Every failing call leaves the state unchanged.
+#include <cstdint>
+#include <new>
+#include <vector>
+
+#include "../../include/pa.h"
+
+struct pa_bm {
+    int32_t num_blocks = 0;
+    int32_t block_size = 0;
+    std::vector<int32_t> free;     // stack; back() is the top
+    std::vector<int32_t> ref;      // refcount per block, 0 when free
+    struct Seq {
+        bool live = false;
+        int32_t len = 0;
+        std::vector<int32_t> table;
+    };
+    std::vector<Seq> seqs;          // indexed by sequence id
+
+    int32_t blocks_needed(int64_t tokens) const {
+        return (int32_t)((tokens + block_size - 1) / block_size);
+    }
+    Seq *get(int32_t s) {
+        return (s >= 0 && s < (int32_t)seqs.size() && seqs[s].live) ? &seqs[s] : nullptr;
+    }
+    const Seq *get(int32_t s) const {
+        return (s >= 0 && s < (int32_t)seqs.size() && seqs[s].live) ? &seqs[s] : nullptr;
+    }
+    // Top n ids in stack order; the caller has checked free.size() >= n.
+    void take(int32_t n, std::vector<int32_t> &out) {
+        const size_t first = free.size() - (size_t)n;
+        for (size_t i = first; i < free.size(); ++i) {
+            out.push_back(free[i]);
+            ref[free[i]] = 1;
+        }
+        free.resize(first);
+    }
+    int32_t pop_one() {
+        const int32_t b = free.back();
+        free.pop_back();
+        ref[b] = 1;
+        return b;
+    }
+    int32_t slot(const Seq &s, int32_t pos) const {
+        return s.table[pos / block_size] * block_size + pos % block_size;
+    }
+};
+
+extern "C" pa_bm_t *pa_bm_create(int32_t num_blocks, int32_t block_size, const int32_t *free_order) {
+    if (num_blocks < 0 || block_size <= 0) return nullptr;
+    if ((int64_t)num_blocks * block_size >= ((int64_t)1 << 31)) return nullptr;
+    pa_bm *bm = new (std::nothrow) pa_bm();
+    if (!bm) return nullptr;
+    bm->num_blocks = num_blocks;
+    bm->block_size = block_size;
+    bm->ref.assign((size_t)num_blocks, 0);
+    bm->free.reserve((size_t)num_blocks);
+    if (free_order) {
+        std::vector<char> seen((size_t)num_blocks, 0);
+        for (int32_t i = 0; i < num_blocks; ++i) {
+            const int32_t b = free_order[i];
+            if (b < 0 || b >= num_blocks || seen[b]) {
+                delete bm;
+                return nullptr;
+            }
+            seen[b] = 1;
+            bm->free.push_back(b);
+        }
+    } else {
+        for (int32_t b = num_blocks - 1; b >= 0; --b) bm->free.push_back(b);
+    }
+    return bm;
+}
+
+extern "C" void pa_bm_destroy(pa_bm_t *bm) { delete bm; }
+
+extern "C" pa_status_t pa_bm_new_seq(pa_bm_t *bm, int32_t num_tokens, int32_t *seq_out) {
+    if (!bm || num_tokens < 0 || !seq_out) return PA_ERR_INVALID_ARG;
+    const int32_t n = bm->blocks_needed(num_tokens);
+    if ((int64_t)n > (int64_t)bm->free.size()) return PA_ERR_NO_BLOCKS;
+    pa_bm::Seq s;
+    s.live = true;
+    s.len = num_tokens;
+    s.table.reserve((size_t)n);
+    bm->take(n, s.table);
+    bm->seqs.push_back(std::move(s));
+    *seq_out = (int32_t)bm->seqs.size() - 1;
+    return PA_OK;
+}
+
+extern "C" pa_status_t pa_bm_fork(pa_bm_t *bm, int32_t parent, int32_t *child_out) {
+    if (!bm || !child_out) return PA_ERR_INVALID_ARG;
+    const pa_bm::Seq *p = bm->get(parent);
+    if (!p) return PA_ERR_INVALID_ARG;
+    pa_bm::Seq c;
+    c.live = true;
+    c.len = p->len;
+    c.table = p->table;
+    for (int32_t b : c.table) bm->ref[b] += 1;
+    bm->seqs.push_back(std::move(c));
+    *child_out = (int32_t)bm->seqs.size() - 1;
+    return PA_OK;
+}
+
+extern "C" pa_status_t pa_bm_free_seq(pa_bm_t *bm, int32_t seq) {
+    if (!bm) return PA_ERR_INVALID_ARG;
+    pa_bm::Seq *s = bm->get(seq);
+    if (!s) return PA_ERR_INVALID_ARG;
+    for (int32_t b : s->table) {
+        if (--bm->ref[b] == 0) bm->free.push_back(b);
+    }
+    s->table.clear();
+    s->table.shrink_to_fit();
+    s->live = false;
+    s->len = 0;
+    return PA_OK;
+}
+
+extern "C" pa_status_t pa_bm_append_tokens(pa_bm_t *bm, int32_t seq, int32_t count, int32_t *slots_out,
+                                           int32_t *cow_pairs_out, int32_t *num_pairs_out) {
+    if (!bm || count < 0 || (count > 0 && !slots_out)) return PA_ERR_INVALID_ARG;
+    pa_bm::Seq *s = bm->get(seq);
+    if (!s) return PA_ERR_INVALID_ARG;
+    if ((int64_t)s->len + count > INT32_MAX) return PA_ERR_INVALID_ARG;
+    if (num_pairs_out) *num_pairs_out = 0;
+    if (count == 0) return PA_OK;
+    const int32_t pos0 = s->len;
+    const int32_t B = bm->block_size;
+    // Blocks this append needs: new blocks past the table, plus one private
+    // copy when the first token lands in a partly filled shared block.
+    const bool cow = (pos0 % B != 0) && bm->ref[s->table[pos0 / B]] > 1;
+    const int64_t grow = (int64_t)bm->blocks_needed((int64_t)pos0 + count) - (int64_t)s->table.size();
+    if (cow && !cow_pairs_out) return PA_ERR_INVALID_ARG;
+    if ((int64_t)cow + grow > (int64_t)bm->free.size()) return PA_ERR_NO_BLOCKS;
+    if (cow) {
+        const int32_t old = s->table[pos0 / B];
+        const int32_t fresh = bm->pop_one();
+        bm->ref[old] -= 1;
+        s->table[pos0 / B] = fresh;
+        cow_pairs_out[0] = old;
+        cow_pairs_out[1] = fresh;
+        if (num_pairs_out) *num_pairs_out = 1;
+    }
+    for (int32_t i = 0; i < count; ++i) {
+        const int32_t pos = pos0 + i;
+        if (pos % B == 0) s->table.push_back(bm->pop_one());
+        slots_out[i] = bm->slot(*s, pos);
+    }
+    s->len = pos0 + count;
+    return PA_OK;
+}
+
+extern "C" pa_status_t pa_bm_append_token(pa_bm_t *bm, int32_t seq, int32_t *slot_out, int32_t *cow_src,
+                                          int32_t *cow_dst) {
+    if (!slot_out) return PA_ERR_INVALID_ARG;
+    int32_t pair[2] = {-1, -1};
+    int32_t np = 0;
+    const pa_status_t st = pa_bm_append_tokens(bm, seq, 1, slot_out, pair, &np);
+    if (st != PA_OK) return st;
+    if (cow_src) *cow_src = np ? pair[0] : -1;
+    if (cow_dst) *cow_dst = np ? pair[1] : -1;
+    return PA_OK;
+}
+
+extern "C" pa_status_t pa_bm_seq_len(const pa_bm_t *bm, int32_t seq, int32_t *len_out,
+                                     int32_t *num_blocks_out) {
+    if (!bm) return PA_ERR_INVALID_ARG;
+    const pa_bm::Seq *s = bm->get(seq);
+    if (!s) return PA_ERR_INVALID_ARG;
+    if (len_out) *len_out = s->len;
+    if (num_blocks_out) *num_blocks_out = (int32_t)s->table.size();
+    return PA_OK;
+}
+
+extern "C" pa_status_t pa_bm_block_table(const pa_bm_t *bm, int32_t seq, int32_t *out, int32_t capacity,
+                                         int32_t *len_out) {
+    if (!bm || capacity < 0 || (capacity > 0 && !out)) return PA_ERR_INVALID_ARG;
+    const pa_bm::Seq *s = bm->get(seq);
+    if (!s) return PA_ERR_INVALID_ARG;
+    const int32_t n = (int32_t)s->table.size();
+    if (len_out) *len_out = n;
+    if (n > capacity) return PA_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n; ++i) out[i] = s->table[i];
+    return PA_OK;
+}
+
+extern "C" pa_status_t pa_bm_physical_index(const pa_bm_t *bm, int32_t seq, int32_t pos, int32_t *slot_out) {
+    if (!bm || !slot_out) return PA_ERR_INVALID_ARG;
+    const pa_bm::Seq *s = bm->get(seq);
+    if (!s || pos < 0 || pos / bm->block_size >= (int32_t)s->table.size()) return PA_ERR_INVALID_ARG;
+    *slot_out = bm->slot(*s, pos);
+    return PA_OK;
+}
+
+extern "C" pa_status_t pa_bm_refcount(const pa_bm_t *bm, int32_t block, int32_t *ref_out) {
+    if (!bm || !ref_out || block < 0 || block >= bm->num_blocks) return PA_ERR_INVALID_ARG;
+    *ref_out = bm->ref[block];
+    return PA_OK;
+}
+
+extern "C" pa_status_t pa_bm_stats(const pa_bm_t *bm, int32_t *free_out, int32_t *used_out,
+                                   int32_t *shared_out) {
+    if (!bm) return PA_ERR_INVALID_ARG;
+    int32_t shared = 0;
+    for (int32_t r : bm->ref) shared += r > 1;
+    if (free_out) *free_out = (int32_t)bm->free.size();
+    if (used_out) *used_out = bm->num_blocks - (int32_t)bm->free.size();
+    if (shared_out) *shared_out = shared;
+    return PA_OK;
+}
+
+extern "C" pa_status_t pa_bm_export(const pa_bm_t *bm, const int32_t *seqs, int32_t n, int32_t max_blocks,
+                                    int32_t *tables_out, int32_t *lens_out) {
+    if (!bm || n < 0 || max_blocks <= 0 || (n > 0 && (!seqs || !tables_out || !lens_out)))
+        return PA_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n; ++i) {
+        const pa_bm::Seq *s = bm->get(seqs[i]);
+        if (!s || (int32_t)s->table.size() > max_blocks) return PA_ERR_INVALID_ARG;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        const pa_bm::Seq *s = bm->get(seqs[i]);
+        int32_t *row = tables_out + (int64_t)i * max_blocks;
+        const int32_t nb = (int32_t)s->table.size();
+        for (int32_t j = 0; j < max_blocks; ++j) row[j] = j < nb ? s->table[j] : -1;
+        lens_out[i] = s->len;
+    }
+    return PA_OK;
+}

@@ -1,0 +1,166 @@
+// Paged KV write (pa_reshape_and_cache) and copy-on-write block copy
+// (pa_copy_blocks).  Both are bit copies bound by HBM bandwidth: every byte is
+// read once and written once, in 16-byte vectors where the row allows it.
+//
+// Cache write: "04 · PagedAttention" (nano-vLLM Deep Dive), section 4,
+// Mechanism 3 "The slot mapping" - a token's K and V go to the cache row of
+// its slot.  In the [NB, B, Hk, D] layout all Hk * D elements of one token are
+// contiguous at element offset slot * Hk * D, so one token is one contiguous
+// row copy.
+// Block copy: "PagedAttention" (tokentrails), step 4 and Code (copy_block); a
+// whole block is B * Hk * D contiguous elements.
+#include "pa_internal.h"
+
+namespace pa {
+
+template <typename V>
+__global__ void __launch_bounds__(256) reshape_and_cache_kernel(
+    const V *__restrict__ k, const V *__restrict__ v, const int32_t *__restrict__ slots,
+    int32_t num_tokens, V *__restrict__ k_cache, V *__restrict__ v_cache, int64_t num_slots,
+    int32_t row_vecs, unsigned int *__restrict__ err) {
+    const int64_t total = (int64_t)num_tokens * row_vecs;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int32_t t = (int32_t)(i / row_vecs);
+        const int32_t j = (int32_t)(i - (int64_t)t * row_vecs);
+        const int32_t s = __ldg(slots + t);
+        if (s < 0) continue;  // padding token
+        if ((int64_t)s >= num_slots) {
+            if (j == 0) atomicOr(err, kErrBounds);
+            continue;
+        }
+        const int64_t dst = (int64_t)s * row_vecs + j;
+        const int64_t src = (int64_t)t * row_vecs + j;
+        k_cache[dst] = __ldcs(k + src);
+        v_cache[dst] = __ldcs(v + src);
+    }
+}
+
+template <typename V>
+__global__ void __launch_bounds__(256) copy_blocks_kernel(V *__restrict__ k_cache, V *__restrict__ v_cache,
+                                                          const int32_t *__restrict__ pairs,
+                                                          int32_t num_pairs, int32_t num_blocks,
+                                                          int64_t block_vecs, int32_t chunks_per_pair,
+                                                          unsigned int *__restrict__ err) {
+    const int32_t p = blockIdx.x / chunks_per_pair;
+    const int32_t chunk = blockIdx.x - p * chunks_per_pair;
+    if (p >= num_pairs) return;
+    const int32_t src = __ldg(pairs + 2 * p);
+    const int32_t dst = __ldg(pairs + 2 * p + 1);
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (chunk == 0 && threadIdx.x == 0) atomicOr(err, kErrBounds);
+        return;
+    }
+    const int64_t per_chunk = (block_vecs + chunks_per_pair - 1) / chunks_per_pair;
+    const int64_t lo = chunk * per_chunk;
+    const int64_t hi = min(block_vecs, lo + per_chunk);
+    const V *ks = k_cache + (int64_t)src * block_vecs;
+    const V *vs = v_cache + (int64_t)src * block_vecs;
+    V *kd = k_cache + (int64_t)dst * block_vecs;
+    V *vd = v_cache + (int64_t)dst * block_vecs;
+    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+        kd[i] = ks[i];
+        vd[i] = vs[i];
+    }
+}
+
+static int vec_bytes_for(int64_t row_bytes, const void *a, const void *b, const void *c, const void *d) {
+    const uintptr_t any = (uintptr_t)a | (uintptr_t)b | (uintptr_t)c | (uintptr_t)d;
+    if (row_bytes % 16 == 0 && any % 16 == 0) return 16;
+    if (row_bytes % 8 == 0 && any % 8 == 0) return 8;
+    if (row_bytes % 4 == 0 && any % 4 == 0) return 4;
+    return 2;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" pa_status_t pa_reshape_and_cache(const void *k, const void *v, const int32_t *slot_mapping,
+                                            int32_t num_tokens, void *k_cache, void *v_cache,
+                                            const pa_cache_desc_t *cache, pa_stream_t stream) {
+    pa_status_t st = validate_cache_desc(cache);
+    if (st != PA_OK) return st;
+    if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+    unsigned int *err = device_error_word();
+    if (!err) return PA_ERR_CUDA;
+    const int64_t row_bytes = (int64_t)cache->num_kv_heads * cache->head_dim * dtype_bytes(cache->dtype);
+    const int vb = vec_bytes_for(row_bytes, k, v, k_cache, v_cache);
+    const int32_t row_vecs = (int32_t)(row_bytes / vb);
+    const int64_t num_slots = (int64_t)cache->num_blocks * cache->block_size;
+    const int64_t total = (int64_t)num_tokens * row_vecs;
+    const int threads = 256;
+    const int64_t want = (total + threads - 1) / threads;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)std::max(num_sms(), 1) * 16));
+    cudaStream_t s = (cudaStream_t)stream;
+    switch (vb) {
+        case 16:
+            reshape_and_cache_kernel<uint4><<<grid, threads, 0, s>>>(
+                (const uint4 *)k, (const uint4 *)v, slot_mapping, num_tokens, (uint4 *)k_cache,
+                (uint4 *)v_cache, num_slots, row_vecs, err);
+            break;
+        case 8:
+            reshape_and_cache_kernel<uint2><<<grid, threads, 0, s>>>(
+                (const uint2 *)k, (const uint2 *)v, slot_mapping, num_tokens, (uint2 *)k_cache,
+                (uint2 *)v_cache, num_slots, row_vecs, err);
+            break;
+        case 4:
+            reshape_and_cache_kernel<uint32_t><<<grid, threads, 0, s>>>(
+                (const uint32_t *)k, (const uint32_t *)v, slot_mapping, num_tokens,
+                (uint32_t *)k_cache, (uint32_t *)v_cache, num_slots, row_vecs, err);
+            break;
+        default:
+            reshape_and_cache_kernel<uint16_t><<<grid, threads, 0, s>>>(
+                (const uint16_t *)k, (const uint16_t *)v, slot_mapping, num_tokens,
+                (uint16_t *)k_cache, (uint16_t *)v_cache, num_slots, row_vecs, err);
+            break;
+    }
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" pa_status_t pa_copy_blocks(void *k_cache, void *v_cache, const pa_cache_desc_t *cache,
+                                      const int32_t *src_dst_pairs, int32_t num_pairs,
+                                      pa_stream_t stream) {
+    pa_status_t st = validate_cache_desc(cache);
+    if (st != PA_OK) return st;
+    if (num_pairs < 0) return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PA_OK;
+    if (!k_cache || !v_cache || !src_dst_pairs) return PA_ERR_INVALID_ARG;
+    unsigned int *err = device_error_word();
+    if (!err) return PA_ERR_CUDA;
+    const int64_t block_bytes = (int64_t)cache->block_size * cache->num_kv_heads * cache->head_dim *
+                                dtype_bytes(cache->dtype);
+    const int vb = vec_bytes_for(block_bytes, k_cache, v_cache, k_cache, v_cache);
+    const int64_t block_vecs = block_bytes / vb;
+    const int threads = 256;
+    // ~8 KiB of each tensor per CTA, at least one CTA per pair
+    int32_t chunks = (int32_t)std::max<int64_t>(1, (block_vecs * vb + 8191) / 8192);
+    if ((int64_t)num_pairs * chunks > INT32_MAX) chunks = INT32_MAX / num_pairs;
+    const int grid = num_pairs * chunks;
+    cudaStream_t s = (cudaStream_t)stream;
+    switch (vb) {
+        case 16:
+            copy_blocks_kernel<uint4><<<grid, threads, 0, s>>>((uint4 *)k_cache, (uint4 *)v_cache,
+                                                               src_dst_pairs, num_pairs,
+                                                               cache->num_blocks, block_vecs, chunks, err);
+            break;
+        case 8:
+            copy_blocks_kernel<uint2><<<grid, threads, 0, s>>>((uint2 *)k_cache, (uint2 *)v_cache,
+                                                               src_dst_pairs, num_pairs,
+                                                               cache->num_blocks, block_vecs, chunks, err);
+            break;
+        case 4:
+            copy_blocks_kernel<uint32_t><<<grid, threads, 0, s>>>(
+                (uint32_t *)k_cache, (uint32_t *)v_cache, src_dst_pairs, num_pairs, cache->num_blocks,
+                block_vecs, chunks, err);
+            break;
+        default:
+            copy_blocks_kernel<uint16_t><<<grid, threads, 0, s>>>(
+                (uint16_t *)k_cache, (uint16_t *)v_cache, src_dst_pairs, num_pairs, cache->num_blocks,
+                block_vecs, chunks, err);
+            break;
+    }
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}

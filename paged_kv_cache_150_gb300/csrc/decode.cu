@@ -1,0 +1,790 @@
+// Paged decode attention (pa_decode).
+//
+// What is computed: for every sequence i and query head h,
+//   out[i, h] = softmax_j(scale * q[i, h] . K_j) V_j   over j < seq_lens[i],
+// with K_j, V_j the cache rows of slot table[i][j / B] * B + j % B
+// ("10 PagedAttention" (PidokuInfra), section 4 PhysicalIndex and section 5
+// "The kernel side"; "PagedAttention" (tokentrails), step 3: the same
+// attention as over contiguous memory).  Query head h reads KV head
+// h / (H / Hk).
+//
+// How (GB300 design; the pages give only a one-CTA-per-(seq, head) sketch):
+// 1. decode_plan_kernel: one CTA turns seq_lens into block counts and their
+//    exclusive prefix sums cu[] (and clamps bad lengths, recording them).
+// 2. A persistent grid of C CTAs splits the flattened list of
+//    (KV-head group, sequence, block) into C equal contiguous ranges
+//    (split_begin).  A CTA walks its range; each of its consumer warps owns
+//    one KV head and all G query heads that share it, so each KV byte is read
+//    from HBM once.  A range piece covering a whole sequence writes `out`
+//    directly; a piece of a longer sequence writes an unnormalised partial
+//    (running max m in log2 units, sum l, accumulator) to the workspace.
+// 3. decode_reduce_kernel merges the partials of each cut sequence:
+//    out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p, M = max_p m_p.
+//
+// Two attention kernels share this plan:
+//  - decode_mma_kernel (bf16): a producer warp streams whole (block, head
+//    group) tiles of K and V into a multi-stage shared-memory ring with TMA
+//    (cp.async.bulk.tensor, 128-byte swizzle, mbarrier completion); consumer
+//    warps compute S^T = K Q^T and O^T += V^T P^T with mma.sync m16n8k16
+//    (tokens on M, the G heads on N) and an online softmax in registers.
+//  - decode_simt_kernel (fp32, or bf16 shapes the MMA kernel does not cover):
+//    plain coalesced loads, warp-shuffle dot products.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "pa_internal.h"
+
+namespace pa {
+
+// ------------------------------------------------------------ output stores
+__device__ __forceinline__ void store_out(float *p, float v) { *p = v; }
+__device__ __forceinline__ void store_out(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+
+// ---------------------------------------------------------------- plan kernel
+__global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__restrict__ seq_lens, int32_t N,
+                                                           int32_t B, int32_t max_len,
+                                                           int32_t *__restrict__ lens_ws,
+                                                           int32_t *__restrict__ cu,
+                                                           unsigned int *__restrict__ err) {
+    __shared__ int32_t warp_incl[32];
+    __shared__ int32_t carry;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int32_t base = 0; base < N; base += blockDim.x) {
+        const int32_t i = base + threadIdx.x;
+        int32_t nb = 0;
+        if (i < N) {
+            int32_t L = seq_lens[i];
+            if (L < 0 || L > max_len) {
+                atomicOr(err, kErrLength);
+                L = 0;
+            }
+            lens_ws[i] = L;
+            nb = (L + B - 1) / B;
+        }
+        int32_t x = nb;  // inclusive scan within the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_incl[w] = x;
+        __syncthreads();
+        if (w == 0) {
+            int32_t s = lane < nwarps ? warp_incl[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += y;
+            }
+            warp_incl[lane] = s;
+        }
+        __syncthreads();
+        const int32_t incl = x + (w > 0 ? warp_incl[w - 1] : 0) + carry;
+        if (i < N) cu[i] = incl - nb;
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry = incl;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) cu[N] = carry;
+}
+
+// -------------------------------------------------------------- reduce kernel
+// One CTA per (group, sequence); one warp per query head of the group.
+template <typename T>
+__global__ void __launch_bounds__(128) decode_reduce_kernel(T *__restrict__ out,
+                                                            const float2 *__restrict__ ml_ws,
+                                                            const float *__restrict__ acc_ws,
+                                                            const int32_t *__restrict__ cu, int32_t N,
+                                                            int32_t H, int32_t D, int32_t NG,
+                                                            int32_t HPG, int32_t C) {
+    const int32_t sp = blockIdx.x;
+    const int32_t g = sp / N, i = sp - g * N;
+    const int32_t Wg = cu[N];
+    const int64_t W = (int64_t)NG * Wg;
+    const int32_t nb = cu[i + 1] - cu[i];
+    T *o = out + ((int64_t)i * H + (int64_t)g * HPG) * D;
+    if (nb == 0) {  // empty sequence: output zero
+        for (int e = threadIdx.x; e < HPG * D; e += blockDim.x) store_out(o + e, 0.f);
+        return;
+    }
+    const int64_t x0 = (int64_t)g * Wg + cu[i];
+    const int32_t c0 = split_owner(x0, W, C);
+    const int32_t c1 = split_owner(x0 + nb - 1, W, C);
+    if (c0 == c1) return;  // written directly by the attention kernel
+    const int lane = threadIdx.x & 31;
+    for (int hh = threadIdx.x >> 5; hh < HPG; hh += blockDim.x >> 5) {
+        float M = -INFINITY;
+        for (int32_t c = c0; c <= c1; ++c) M = fmaxf(M, ml_ws[partial_slot(c, sp) * HPG + hh].x);
+        float Lsum = 0.f;
+        for (int32_t c = c0; c <= c1; ++c) {
+            const float2 v = ml_ws[partial_slot(c, sp) * HPG + hh];
+            Lsum += ex2_approx(v.x - M) * v.y;
+        }
+        const float inv = 1.f / Lsum;
+        for (int d = lane; d < D; d += 32) {
+            float a = 0.f;
+            for (int32_t c = c0; c <= c1; ++c) {
+                const int64_t slot = partial_slot(c, sp);
+                a += ex2_approx(ml_ws[slot * HPG + hh].x - M) * acc_ws[(slot * HPG + hh) * D + d];
+            }
+            store_out(o + (int64_t)hh * D + d, a * inv);
+        }
+    }
+}
+
+// ------------------------------------------------------- CUDA-core kernel
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T, int VPL>
+__device__ __forceinline__ void load_row_slice(const T *__restrict__ p, float (&x)[VPL]) {
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) x[j] = to_f32<T>(p[j]);
+}
+
+// Block tile: NH warps, warp w handles KV head g*NH + w and its G (<= GMAX)
+// query heads, one token at a time (lane holds D/32 consecutive elements).
+template <typename T, int D, int GMAX>
+__global__ void __launch_bounds__(256) decode_simt_kernel(
+    const T *__restrict__ q, T *__restrict__ out, const T *__restrict__ k_cache,
+    const T *__restrict__ v_cache, const int32_t *__restrict__ tables, int32_t max_blocks,
+    const int32_t *__restrict__ lens, const int32_t *__restrict__ cu, int32_t N, int32_t H,
+    int32_t Hk, int32_t G, int32_t B, int32_t NB, int32_t NH, float scale_log2, int32_t C,
+    float2 *__restrict__ ml_ws, float *__restrict__ acc_ws, unsigned int *__restrict__ err) {
+    constexpr int VPL = D / 32;
+    const int32_t NG = Hk / NH;
+    const int32_t HPG = NH * G;
+    const int64_t W = (int64_t)NG * cu[N];
+    const int32_t c = blockIdx.x;
+    const int64_t lo = split_begin(c, W, C), hi = split_begin(c + 1, W, C);
+    if (lo >= hi) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    BlockCursor cur;
+    cur.init(lo, cu, N);
+    float qv[GMAX][VPL], acc[GMAX][VPL], m[GMAX], l[GMAX];
+    bool seg_start = true, seg_from_first = false;
+    for (int64_t x = lo; x < hi; ++x) {
+        const int32_t kvh = cur.g * NH + warp;
+        const int32_t L = lens[cur.seq];
+        if (seg_start) {
+            const T *qp = q + ((int64_t)cur.seq * H + (int64_t)kvh * G) * D + lane * VPL;
+#pragma unroll
+            for (int h = 0; h < GMAX; ++h) {
+                if (h < G) {
+                    load_row_slice<T, VPL>(qp + (int64_t)h * D, qv[h]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < VPL; ++j) qv[h][j] = 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < VPL; ++j) acc[h][j] = 0.f;
+                m[h] = -INFINITY;
+                l[h] = 0.f;
+            }
+            seg_from_first = (cur.blk == 0);
+            seg_start = false;
+        }
+        int32_t phys = tables[(int64_t)cur.seq * max_blocks + cur.blk];
+        const bool valid = phys >= 0 && phys < NB;
+        if (!valid && lane == 0) atomicOr(err, kErrBounds);
+        const int32_t tok0 = cur.blk * B;
+        const int32_t ntok = min(B, L - tok0);
+        for (int32_t t = 0; t < ntok; ++t) {
+            float kx[VPL], vx[VPL];
+            if (valid) {
+                const int64_t row = (((int64_t)phys * B + t) * Hk + kvh) * D + lane * VPL;
+                load_row_slice<T, VPL>(k_cache + row, kx);
+                load_row_slice<T, VPL>(v_cache + row, vx);
+            } else {  // an invalid block id reads zeros (as the TMA kernel does)
+#pragma unroll
+                for (int j = 0; j < VPL; ++j) kx[j] = vx[j] = 0.f;
+            }
+#pragma unroll
+            for (int h = 0; h < GMAX; ++h) {
+                if (h >= G) break;
+                float s = 0.f;
+#pragma unroll
+                for (int j = 0; j < VPL; ++j) s = fmaf(qv[h][j], kx[j], s);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                const float xs = s * scale_log2;
+                const float mn = fmaxf(m[h], xs);
+                const float alpha = ex2_approx(m[h] - mn);
+                const float p = ex2_approx(xs - mn);
+                l[h] = l[h] * alpha + p;
+#pragma unroll
+                for (int j = 0; j < VPL; ++j) acc[h][j] = fmaf(acc[h][j], alpha, p * vx[j]);
+                m[h] = mn;
+            }
+        }
+        const bool last_blk = (cur.blk == cur.nb - 1);
+        if (last_blk || x + 1 == hi) {
+            const int32_t sp = cur.g * N + cur.seq;
+            if (seg_from_first && last_blk) {
+                T *op = out + ((int64_t)cur.seq * H + (int64_t)kvh * G) * D + lane * VPL;
+#pragma unroll
+                for (int h = 0; h < GMAX; ++h) {
+                    if (h >= G) break;
+                    const float inv = 1.f / l[h];
+#pragma unroll
+                    for (int j = 0; j < VPL; ++j) store_out(op + (int64_t)h * D + j, acc[h][j] * inv);
+                }
+            } else {
+                const int64_t slot = partial_slot(c, sp);
+#pragma unroll
+                for (int h = 0; h < GMAX; ++h) {
+                    if (h >= G) break;
+                    const int64_t hh = slot * HPG + warp * G + h;
+                    float *ap = acc_ws + hh * D + lane * VPL;
+#pragma unroll
+                    for (int j = 0; j < VPL; ++j) ap[j] = acc[h][j];
+                    if (lane == 0) ml_ws[hh] = make_float2(m[h], l[h]);
+                }
+            }
+            seg_start = true;
+        }
+        cur.advance(cu, N);
+    }
+}
+
+// ------------------------------------------------- TMA + tensor-core kernel
+// Shared-memory tile of one stage and one tensor (K or V): the TMA box
+// {64 elements, B tokens, D/64 halves, NH heads}, i.e. [head][half][token][64]
+// with 128-byte lines swizzled (16-byte chunk index XOR line % 8).
+template <int D, int B>
+struct MmaTile {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kSlabBytes = kHalves * B * 128;  // one head
+    static constexpr int kStages = 3;
+};
+
+__device__ __forceinline__ uint32_t swz_addr(uint32_t slab, int line, int chunk) {
+    return slab + (uint32_t)line * 128u + ((uint32_t)(chunk ^ (line & 7)) << 4);
+}
+
+template <int D, int B>
+__global__ void __launch_bounds__(288, 1) decode_mma_kernel(
+    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+    const __nv_bfloat16 *__restrict__ q, __nv_bfloat16 *__restrict__ out,
+    const int32_t *__restrict__ tables, int32_t max_blocks, const int32_t *__restrict__ lens,
+    const int32_t *__restrict__ cu, int32_t N, int32_t H, int32_t Hk, int32_t G, int32_t NB,
+    int32_t NH, float scale_log2, int32_t C, float2 *__restrict__ ml_ws, float *__restrict__ acc_ws,
+    unsigned int *__restrict__ err) {
+    using Tile = MmaTile<D, B>;
+    constexpr int S = Tile::kStages;
+    constexpr int KT = D / 16;  // k-steps of q.k and m-tiles of O^T
+    const uint32_t tile_bytes = (uint32_t)NH * Tile::kSlabBytes;
+    const uint32_t stage_bytes = 2u * tile_bytes;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *full = (uint64_t *)(smem + S * stage_bytes);
+    uint64_t *empty = full + S;
+
+    const int32_t NG = Hk / NH;
+    const int64_t W = (int64_t)NG * cu[N];
+    const int32_t c = blockIdx.x;
+    const int64_t lo = split_begin(c, W, C), hi = split_begin(c + 1, W, C);
+    if (lo >= hi) return;
+    const int64_t n = hi - lo;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), (uint32_t)NH);
+        }
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+
+    if (warp == NH) {
+        // ------------------------------------------------------- producer
+        if (lane == 0) {
+            prefetch_tmap(&tmk);
+            prefetch_tmap(&tmv);
+            BlockCursor cur;
+            cur.init(lo, cu, N);
+            int64_t issued = 0;
+            for (; issued < n; ++issued) {
+                const int s = (int)(issued % S);
+                const uint32_t ph = (uint32_t)((issued / S) & 1);
+                if (issued >= S && !mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u)) {
+                    atomicOr(err, kErrTimeout);
+                    break;
+                }
+                int32_t phys = tables[(int64_t)cur.seq * max_blocks + cur.blk];
+                if (phys < 0 || phys >= NB) {  // read zeros: the box lies past the pool
+                    atomicOr(err, kErrBounds);
+                    phys = NB;
+                }
+                const uint32_t fb = smem_u32(&full[s]);
+                const uint32_t dst = smem_u32(smem + (size_t)s * stage_bytes);
+                mbar_arrive_expect_tx(fb, stage_bytes);
+                tma_load_4d(dst, &tmk, fb, 0, phys * B, 0, cur.g * NH);
+                tma_load_4d(dst + tile_bytes, &tmv, fb, 0, phys * B, 0, cur.g * NH);
+                cur.advance(cu, N);
+            }
+            // Let every copy still in flight land before the CTA may exit.
+            for (int64_t j = issued > S ? issued - S : 0; j < issued; ++j)
+                mbar_wait_bounded(smem_u32(&full[j % S]), (uint32_t)((j / S) & 1));
+        }
+        return;
+    }
+
+    // ----------------------------------------------------------- consumers
+    const int r = lane >> 2, cq = lane & 3;  // mma groupID / thread-in-group
+    const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: matrix id / row id
+    uint32_t qf[KT][2];
+    float o[KT][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    BlockCursor cur;
+    cur.init(lo, cu, N);
+    bool seg_start = true, seg_from_first = false;
+
+    for (int64_t it = 0; it < n; ++it) {
+        const int s = (int)(it % S);
+        const uint32_t ph = (uint32_t)((it / S) & 1);
+        const int32_t kvh = cur.g * NH + warp;
+        const int32_t L = lens[cur.seq];
+        if (seg_start) {
+            // B operand of S^T = K Q^T: column n = query head r of this KV head.
+            const bool hv = r < G;
+            const __nv_bfloat16 *qp = q + ((int64_t)cur.seq * H + (int64_t)kvh * G + (hv ? r : 0)) * D;
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk) {
+                qf[kk][0] = hv ? *reinterpret_cast<const uint32_t *>(qp + kk * 16 + 2 * cq) : 0u;
+                qf[kk][1] = hv ? *reinterpret_cast<const uint32_t *>(qp + kk * 16 + 8 + 2 * cq) : 0u;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[kk][e] = 0.f;
+            }
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+            seg_from_first = (cur.blk == 0);
+            seg_start = false;
+        }
+
+        const bool ok = mbar_wait_bounded(smem_u32(&full[s]), ph);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) atomicOr(err, kErrTimeout);
+            return;
+        }
+        const uint32_t kslab = smem_u32(smem + (size_t)s * stage_bytes) + (uint32_t)warp * Tile::kSlabBytes;
+        const uint32_t vslab = kslab + tile_bytes;
+        const int32_t tok0 = cur.blk * B;
+        const int32_t ntok = min(B, L - tok0);
+        if (ntok < B) {
+            // Rows past the sequence end hold stale data (maybe NaN): zero
+            // them in V so that p = 0 rows contribute exactly 0.
+            const int rows = B - ntok;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            for (int e = lane; e < Tile::kHalves * rows * 8; e += 32) {
+                const int chunk = e & 7;
+                const int ri = e >> 3;
+                const int half = ri / rows;
+                const int t = ntok + (ri - half * rows);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 vslab + (uint32_t)((half * B + t) * 128 + chunk * 16)),
+                             "r"(z.x), "r"(z.y), "r"(z.z), "r"(z.w)
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+
+#pragma unroll
+        for (int mt = 0; mt < B / 16; ++mt) {
+            if (tok0 + mt * 16 >= L) break;
+            // S^T (16 tokens x 8 heads) = K (16 x D) Q^T (D x 8)
+            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk) {
+                const int t = mt * 16 + rr + (mi & 1) * 8;
+                const int d = kk * 16 + (mi >> 1) * 8;
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4(swz_addr(kslab, (d >> 6) * B + t, (d & 63) >> 3), a0, a1, a2, a3);
+                mma_bf16_16816(sacc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+            }
+            // online softmax in log2 units; rows = tokens, columns = heads
+            const int ta = tok0 + mt * 16 + r, tb = ta + 8;
+            const float x0 = ta < L ? sacc[0] * scale_log2 : -INFINITY;
+            const float x1 = ta < L ? sacc[1] * scale_log2 : -INFINITY;
+            const float x2 = tb < L ? sacc[2] * scale_log2 : -INFINITY;
+            const float x3 = tb < L ? sacc[3] * scale_log2 : -INFINITY;
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float al0 = ex2_approx(m0 - mn0), al1 = ex2_approx(m1 - mn1);
+            const float p0 = ex2_approx(x0 - mn0), p1 = ex2_approx(x1 - mn1);
+            const float p2 = ex2_approx(x2 - mn0), p3 = ex2_approx(x3 - mn1);
+            l0 = l0 * al0 + (p0 + p2);
+            l1 = l1 * al1 + (p1 + p3);
+            m0 = mn0;
+            m1 = mn1;
+#pragma unroll
+            for (int dm = 0; dm < KT; ++dm) {
+                o[dm][0] *= al0;
+                o[dm][1] *= al1;
+                o[dm][2] *= al0;
+                o[dm][3] *= al1;
+            }
+            // P^T as the B operand: transpose the two 8x8 bf16 quadrants.
+            const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+            const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+            // O^T (D x 8 heads) += V^T (D x 16 tokens) P^T (16 tokens x 8 heads)
+#pragma unroll
+            for (int dm = 0; dm < KT; ++dm) {
+                const int t = mt * 16 + rr + (mi >> 1) * 8;
+                const int d = dm * 16 + (mi & 1) * 8;
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4_trans(swz_addr(vslab, (d >> 6) * B + t, (d & 63) >> 3), a0, a1, a2, a3);
+                mma_bf16_16816(o[dm], a0, a1, a2, a3, pb0, pb1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+
+        const bool last_blk = (cur.blk == cur.nb - 1);
+        if (last_blk || it + 1 == n) {
+            float lt0 = l0, lt1 = l1;
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                lt0 += __shfl_xor_sync(0xffffffffu, lt0, off);
+                lt1 += __shfl_xor_sync(0xffffffffu, lt1, off);
+            }
+            const int h0 = 2 * cq, h1 = 2 * cq + 1;
+            if (seg_from_first && last_blk) {
+                const float i0 = 1.f / lt0, i1 = 1.f / lt1;
+                __nv_bfloat16 *ob = out + ((int64_t)cur.seq * H + (int64_t)kvh * G) * D;
+#pragma unroll
+                for (int dm = 0; dm < KT; ++dm) {
+                    const int d = dm * 16 + r;
+                    if (h0 < G) {
+                        ob[h0 * D + d] = __float2bfloat16_rn(o[dm][0] * i0);
+                        ob[h0 * D + d + 8] = __float2bfloat16_rn(o[dm][2] * i0);
+                    }
+                    if (h1 < G) {
+                        ob[h1 * D + d] = __float2bfloat16_rn(o[dm][1] * i1);
+                        ob[h1 * D + d + 8] = __float2bfloat16_rn(o[dm][3] * i1);
+                    }
+                }
+            } else {
+                const int32_t HPG = NH * G;
+                const int64_t slot = partial_slot(c, cur.g * N + cur.seq);
+                float *ab = acc_ws + (slot * HPG + (int64_t)warp * G) * D;
+#pragma unroll
+                for (int dm = 0; dm < KT; ++dm) {
+                    const int d = dm * 16 + r;
+                    if (h0 < G) {
+                        ab[h0 * D + d] = o[dm][0];
+                        ab[h0 * D + d + 8] = o[dm][2];
+                    }
+                    if (h1 < G) {
+                        ab[h1 * D + d] = o[dm][1];
+                        ab[h1 * D + d + 8] = o[dm][3];
+                    }
+                }
+                if (r == 0) {
+                    if (h0 < G) ml_ws[slot * HPG + warp * G + h0] = make_float2(m0, lt0);
+                    if (h1 < G) ml_ws[slot * HPG + warp * G + h1] = make_float2(m1, lt1);
+                }
+            }
+            seg_start = true;
+        }
+        cur.advance(cu, N);
+    }
+}
+
+// ====================================================================== host
+namespace {
+
+struct DecodePlan {
+    int kernel;    // PA_KERNEL_SIMT or PA_KERNEL_MMA
+    int NH;        // KV heads per CTA (consumer warps)
+    int NG;        // head groups = Hk / NH
+    int HPG;       // query heads per group = NH * G
+    int C;         // persistent CTAs
+    size_t smem;   // dynamic shared memory of the attention kernel
+    // workspace layout (byte offsets)
+    size_t off_lens, off_cu, off_ml, off_acc, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int largest_divisor_at_most(int n, int cap) {
+    for (int d = std::min(n, cap); d >= 1; --d)
+        if (n % d == 0) return d;
+    return 1;
+}
+
+bool mma_supported(const pa_cache_desc_t *c, int G) {
+    return c->dtype == PA_BF16 && (c->head_dim == 64 || c->head_dim == 128) &&
+           (c->block_size == 16 || c->block_size == 32) && G >= 1 && G <= 8;
+}
+
+bool simt_supported(const pa_cache_desc_t *c, int G) {
+    const bool d_ok = c->dtype == PA_F32 ? (c->head_dim == 64 || c->head_dim == 128)
+                                         : (c->head_dim == 64 || c->head_dim == 128 || c->head_dim == 256);
+    return d_ok && G >= 1 && G <= 8;
+}
+
+int simt_gmax(int G) { return G <= 1 ? 1 : (G <= 4 ? 4 : 8); }
+
+size_t mma_smem_bytes(int D, int B, int NH) {
+    const size_t tile = (size_t)NH * (D / 64) * B * 128;
+    return 3 * 2 * tile + 2 * 3 * sizeof(uint64_t) + 1024;
+}
+
+template <typename T, int D, int GMAX>
+const void *simt_fn() {
+    return (const void *)decode_simt_kernel<T, D, GMAX>;
+}
+
+const void *simt_kernel_ptr(int dtype, int D, int G) {
+    const int gm = simt_gmax(G);
+#define PA_SIMT_CASE(TT, DD)                                        \
+    if (D == DD) {                                                  \
+        if (gm == 1) return simt_fn<TT, DD, 1>();                   \
+        if (gm == 4) return simt_fn<TT, DD, 4>();                   \
+        return simt_fn<TT, DD, 8>();                                \
+    }
+    if (dtype == PA_F32) {
+        PA_SIMT_CASE(float, 64)
+        PA_SIMT_CASE(float, 128)
+    } else {
+        PA_SIMT_CASE(__nv_bfloat16, 64)
+        PA_SIMT_CASE(__nv_bfloat16, 128)
+        PA_SIMT_CASE(__nv_bfloat16, 256)
+    }
+#undef PA_SIMT_CASE
+    return nullptr;
+}
+
+const void *mma_kernel_ptr(int D, int B) {
+    if (D == 128 && B == 16) return (const void *)decode_mma_kernel<128, 16>;
+    if (D == 128 && B == 32) return (const void *)decode_mma_kernel<128, 32>;
+    if (D == 64 && B == 16) return (const void *)decode_mma_kernel<64, 16>;
+    if (D == 64 && B == 32) return (const void *)decode_mma_kernel<64, 32>;
+    return nullptr;
+}
+
+// Occupancy-based default split count: one full wave of resident CTAs.
+int default_ctas(const void *fn, int threads, size_t smem) {
+    const int sms = num_sms();
+    if (sms <= 0) return -1;
+    int per_sm = 0;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return -1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess) return -1;
+    return sms * std::max(per_sm, 1);
+}
+
+pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_decode_opts_t *opts,
+                      bool need_default_splits, DecodePlan *p) {
+    pa_status_t st = validate_cache_desc(c);
+    if (st != PA_OK) return st;
+    if (N < 0 || H <= 0 || H % c->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    const int G = H / c->num_kv_heads;
+    const int want = opts ? opts->kernel : PA_KERNEL_AUTO;
+    if (want != PA_KERNEL_AUTO && want != PA_KERNEL_SIMT && want != PA_KERNEL_MMA) return PA_ERR_INVALID_ARG;
+    if (opts && opts->num_splits < 0) return PA_ERR_INVALID_ARG;
+    int kernel;
+    if (want == PA_KERNEL_MMA || (want == PA_KERNEL_AUTO && mma_supported(c, G))) {
+        if (!mma_supported(c, G)) return PA_ERR_UNSUPPORTED;
+        kernel = PA_KERNEL_MMA;
+    } else {
+        if (!simt_supported(c, G)) return PA_ERR_UNSUPPORTED;
+        kernel = PA_KERNEL_SIMT;
+    }
+    p->kernel = kernel;
+    if (kernel == PA_KERNEL_MMA) {
+        // stage = K + V tiles of NH heads; keep a stage <= 64 KiB so 3 stages fit
+        const int cap = std::max(1, (int)(65536 / (2 * c->block_size * c->head_dim * 2)));
+        p->NH = largest_divisor_at_most(c->num_kv_heads, std::min(8, cap));
+        p->smem = mma_smem_bytes(c->head_dim, c->block_size, p->NH);
+    } else {
+        p->NH = largest_divisor_at_most(c->num_kv_heads, 8);
+        p->smem = 0;
+    }
+    p->NG = c->num_kv_heads / p->NH;
+    p->HPG = p->NH * G;
+    int C = opts ? opts->num_splits : 0;
+    if (C == 0) {
+        if (!need_default_splits) return PA_ERR_INVALID_ARG;
+        const void *fn = kernel == PA_KERNEL_MMA ? mma_kernel_ptr(c->head_dim, c->block_size)
+                                                 : simt_kernel_ptr(c->dtype, c->head_dim, G);
+        const int threads = kernel == PA_KERNEL_MMA ? (p->NH + 1) * 32 : p->NH * 32;
+        C = default_ctas(fn, threads, p->smem);
+        if (C <= 0) return PA_ERR_CUDA;
+    }
+    p->C = C;
+    const size_t slots = (size_t)C + (size_t)p->NG * N;
+    size_t off = 0;
+    p->off_lens = off;
+    off = align256(off + sizeof(int32_t) * (size_t)std::max(N, 1));
+    p->off_cu = off;
+    off = align256(off + sizeof(int32_t) * ((size_t)N + 1));
+    p->off_ml = off;
+    off = align256(off + sizeof(float2) * slots * p->HPG);
+    p->off_acc = off;
+    off = align256(off + sizeof(float) * slots * p->HPG * c->head_dim);
+    p->total = off;
+    return PA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+    });
+    return fn;
+}
+
+// 4-D map over one bf16 cache viewed as {64, NB*B, D/64, Hk} with strides
+// {-, Hk*D*2, 128, D*2} bytes; box {64, B, D/64, NH}, 128-byte swizzle.
+bool encode_cache_map(CUtensorMap *map, const void *base, const pa_cache_desc_t *c, int NH) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int D = c->head_dim;
+    cuuint64_t dims[4] = {64, (cuuint64_t)c->num_blocks * c->block_size, (cuuint64_t)(D / 64),
+                          (cuuint64_t)c->num_kv_heads};
+    cuuint64_t strides[3] = {(cuuint64_t)c->num_kv_heads * D * 2, 128, (cuuint64_t)D * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)c->block_size, (cuuint32_t)(D / 64), (cuuint32_t)NH};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" size_t pa_decode_workspace_bytes(const pa_cache_desc_t *cache, int32_t num_seqs, int32_t num_heads,
+                                            const pa_decode_opts_t *opts) {
+    DecodePlan p;
+    if (make_plan(cache, num_seqs, num_heads, opts, true, &p) != PA_OK) return 0;
+    return p.total;
+}
+
+extern "C" int32_t pa_decode_default_splits(const pa_cache_desc_t *cache, int32_t num_heads,
+                                            const pa_decode_opts_t *opts) {
+    pa_decode_opts_t o = opts ? *opts : pa_decode_opts_t{0, PA_KERNEL_AUTO, nullptr, nullptr};
+    o.num_splits = 0;
+    DecodePlan p;
+    const pa_status_t st = make_plan(cache, 1, num_heads, &o, true, &p);
+    return st == PA_OK ? p.C : (int32_t)st;
+}
+
+extern "C" void pa_split_range(int64_t total_blocks, int32_t num_splits, int32_t c, int64_t *begin,
+                               int64_t *end) {
+    if (begin) *begin = split_begin(c, total_blocks, num_splits);
+    if (end) *end = split_begin((int64_t)c + 1, total_blocks, num_splits);
+}
+
+extern "C" int32_t pa_split_owner(int64_t total_blocks, int32_t num_splits, int64_t x) {
+    return split_owner(x, total_blocks, num_splits);
+}
+
+extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                 const pa_cache_desc_t *cache, const int32_t *block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
+                                 int32_t num_heads, float scale, void *workspace, size_t workspace_bytes,
+                                 const pa_decode_opts_t *opts, pa_stream_t stream) {
+    DecodePlan p;
+    pa_status_t st = make_plan(cache, num_seqs, num_heads, opts, true, &p);
+    if (st != PA_OK) return st;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !workspace)
+        return PA_ERR_INVALID_ARG;
+    if (max_blocks_per_seq <= 0 || (int64_t)num_seqs * max_blocks_per_seq >= ((int64_t)1 << 31) ||
+        (int64_t)max_blocks_per_seq * cache->block_size >= ((int64_t)1 << 31))
+        return PA_ERR_INVALID_ARG;
+    if (!(scale == scale)) return PA_ERR_INVALID_ARG;
+    if (((uintptr_t)workspace & 255) != 0) return PA_ERR_INVALID_ARG;
+    if (workspace_bytes < p.total) return PA_ERR_WORKSPACE;
+    const int eb = dtype_bytes(cache->dtype);
+    if (((uintptr_t)q | (uintptr_t)out) % (size_t)(eb * 2) != 0) return PA_ERR_INVALID_ARG;
+    unsigned int *err = device_error_word();
+    if (!err) return PA_ERR_CUDA;
+
+    uint8_t *ws = (uint8_t *)workspace;
+    int32_t *lens_ws = (int32_t *)(ws + p.off_lens);
+    int32_t *cu = (int32_t *)(ws + p.off_cu);
+    float2 *ml = (float2 *)(ws + p.off_ml);
+    float *acc = (float *)(ws + p.off_acc);
+    const int G = num_heads / cache->num_kv_heads;
+    const float scale_log2 = scale * 1.4426950408889634f;
+    const int32_t max_len = max_blocks_per_seq * cache->block_size;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaGetLastError();  // clear a stale launch error so the checks below are ours
+
+    decode_plan_kernel<<<1, 1024, 0, s>>>(seq_lens, num_seqs, cache->block_size, max_len, lens_ws, cu, err);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+
+    if (opts && opts->ev_partial_begin && cudaEventRecord((cudaEvent_t)opts->ev_partial_begin, s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (p.kernel == PA_KERNEL_MMA) {
+        if (((uintptr_t)k_cache | (uintptr_t)v_cache) % 16 != 0) return PA_ERR_INVALID_ARG;
+        CUtensorMap tmk, tmv;
+        if (!encode_cache_map(&tmk, k_cache, cache, p.NH) || !encode_cache_map(&tmv, v_cache, cache, p.NH))
+            return PA_ERR_CUDA;
+        const void *fn = mma_kernel_ptr(cache->head_dim, cache->block_size);
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
+            return PA_ERR_CUDA;
+        const dim3 grid(p.C), block((p.NH + 1) * 32);
+        const __nv_bfloat16 *qb = (const __nv_bfloat16 *)q;
+        __nv_bfloat16 *ob = (__nv_bfloat16 *)out;
+        int32_t NB = cache->num_blocks, Hk = cache->num_kv_heads, NHv = p.NH, Cv = p.C;
+        int32_t Nv = num_seqs, Hv = num_heads, Gv = G, mb = max_blocks_per_seq;
+        float sl = scale_log2;
+        void *args[] = {&tmk, &tmv, &qb, &ob, &block_tables, &mb, &lens_ws, &cu, &Nv, &Hv, &Hk, &Gv,
+                        &NB, &NHv, &sl, &Cv, &ml, &acc, &err};
+        if (cudaLaunchKernel(fn, grid, block, args, p.smem, s) != cudaSuccess) return PA_ERR_CUDA;
+    } else {
+        const void *fn = simt_kernel_ptr(cache->dtype, cache->head_dim, G);
+        if (!fn) return PA_ERR_UNSUPPORTED;
+        const dim3 grid(p.C), block(p.NH * 32);
+        int32_t NB = cache->num_blocks, Hk = cache->num_kv_heads, NHv = p.NH, Cv = p.C;
+        int32_t Nv = num_seqs, Hv = num_heads, Gv = G, mb = max_blocks_per_seq, Bv = cache->block_size;
+        float sl = scale_log2;
+        void *args[] = {&q, &out, &k_cache, &v_cache, &block_tables, &mb, &lens_ws, &cu, &Nv, &Hv, &Hk,
+                        &Gv, &Bv, &NB, &NHv, &sl, &Cv, &ml, &acc, &err};
+        if (cudaLaunchKernel(fn, grid, block, args, 0, s) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    if (opts && opts->ev_partial_end && cudaEventRecord((cudaEvent_t)opts->ev_partial_end, s) != cudaSuccess)
+        return PA_ERR_CUDA;
+
+    const dim3 rgrid((unsigned)(p.NG * num_seqs)), rblock(128);
+    if (cache->dtype == PA_BF16)
+        decode_reduce_kernel<__nv_bfloat16><<<rgrid, rblock, 0, s>>>((__nv_bfloat16 *)out, ml, acc, cu, num_seqs,
+                                                                     num_heads, cache->head_dim, p.NG, p.HPG, p.C);
+    else
+        decode_reduce_kernel<float><<<rgrid, rblock, 0, s>>>((float *)out, ml, acc, cu, num_seqs, num_heads,
+                                                             cache->head_dim, p.NG, p.HPG, p.C);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}

@@ -1,0 +1,198 @@
+// Shared device helpers for the paged-KV kernels (sm_103a).
+//
+// - the device error word bits,
+// - the even split of the flattened (KV-head group, sequence, block) list over
+//   persistent CTAs (host and device use these same integer formulas),
+// - thin inline-PTX wrappers: mbarrier, TMA tensor loads, ldmatrix,
+//   movmatrix, mma.sync, ex2.approx, globaltimer.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Bits of the per-device error word.
+enum : unsigned int {
+    kErrBounds = 1u,   // slot / table entry / block id outside the pool
+    kErrLength = 2u,   // sequence length outside [0, max_blocks * B]
+    kErrTimeout = 4u,  // a bounded mbarrier wait ran out
+};
+
+// Bound on any single mbarrier wait (nanoseconds of %globaltimer).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// ---------------------------------------------------------------- work split
+// CTA c of C owns flattened blocks [split_begin(c), split_begin(c + 1)).
+__host__ __device__ __forceinline__ int64_t split_begin(int64_t c, int64_t W, int64_t C) {
+    return c * W / C;
+}
+// Largest c with split_begin(c) <= x, i.e. the CTA that owns block x (0 <= x < W).
+__host__ __device__ __forceinline__ int32_t split_owner(int64_t x, int64_t W, int64_t C) {
+    return (int32_t)(((x + 1) * C + W - 1) / W - 1);
+}
+
+// Partial-result slot of (CTA c, flattened sequence sp = group * N + seq).
+// Unique because CTA ranges and sequences are both ordered along the
+// flattened block list; there are at most C + NG * N slots.
+__host__ __device__ __forceinline__ int64_t partial_slot(int32_t c, int32_t sp) {
+    return (int64_t)c + sp;
+}
+
+// ------------------------------------------------------------- small helpers
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbarrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile(
+        "{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile(
+        "{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(bar),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of the barrier to complete, giving up after
+// kWaitLimitNs.  Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// ----------------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, uint32_t bar, int32_t c0,
+                                            int32_t c1, int32_t c2, int32_t c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ----------------------------------------------------------- warp-level MMA
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                            uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                                  uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
+// D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ----------------------------------------------------------- block cursor
+// Walks the flattened (group, sequence, block) list.  cu[] holds the
+// exclusive prefix sums of per-sequence block counts (cu[N] = Wg).
+struct BlockCursor {
+    int32_t g, seq, blk;
+    int32_t nb;  // blocks of the current sequence
+
+    __device__ __forceinline__ void init(int64_t x, const int32_t *__restrict__ cu, int32_t N) {
+        const int32_t Wg = cu[N];
+        g = (int32_t)(x / Wg);
+        const int32_t r = (int32_t)(x - (int64_t)g * Wg);
+        // largest seq with cu[seq] <= r (skips empty sequences: cu[seq+1] > r)
+        int32_t lo = 0, hi = N - 1;
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            if (cu[mid] <= r)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        seq = lo;
+        blk = r - cu[seq];
+        nb = cu[seq + 1] - cu[seq];
+    }
+
+    __device__ __forceinline__ void advance(const int32_t *__restrict__ cu, int32_t N) {
+        if (++blk < nb) return;
+        blk = 0;
+        do {
+            if (++seq == N) {
+                seq = 0;
+                ++g;
+            }
+            nb = cu[seq + 1] - cu[seq];
+        } while (nb == 0);
+    }
+};
+
+}  // namespace pa

@@ -1,0 +1,134 @@
+"""The C-ABI library loads, exports every symbol include/pa.h declares, and
+validates host-visible arguments without touching a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import paged_kv_cache_150_gb300 as pa
+from paged_kv_cache_150_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    return _lib.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _lib.SIGNATURES, "binding lacks a signature for %s" % n
+
+
+def test_status_strings_and_version(lib):
+    assert lib.pa_status_string(0) == b"ok"
+    assert b"workspace" in lib.pa_status_string(-7)
+    assert b"sm_103a" in lib.pa_version()
+
+
+def _desc(nb=8, bs=16, hk=8, d=128, dt=_lib.PA_BF16):
+    return _lib.CacheDesc(nb, bs, hk, d, dt)
+
+
+def test_host_validation_rejects_bad_arguments_without_a_gpu(lib):
+    d = _desc()
+    p = ctypes.c_void_p(0x1000)
+    # null pointers / negative sizes / bad descriptors are caught before any CUDA call
+    assert lib.pa_reshape_and_cache(None, p, p, 4, p, p, ctypes.byref(d), None) == _lib.PA_ERR_INVALID_ARG
+    assert lib.pa_reshape_and_cache(p, p, p, -1, p, p, ctypes.byref(d), None) == _lib.PA_ERR_INVALID_ARG
+    assert lib.pa_reshape_and_cache(p, p, p, 0, p, p, ctypes.byref(d), None) == _lib.PA_OK
+    assert lib.pa_copy_blocks(p, p, ctypes.byref(d), p, 0, None) == _lib.PA_OK
+    assert lib.pa_copy_blocks(None, p, ctypes.byref(d), p, 3, None) == _lib.PA_ERR_INVALID_ARG
+    bad = _desc(dt=7)
+    assert lib.pa_copy_blocks(p, p, ctypes.byref(bad), p, 1, None) == _lib.PA_ERR_INVALID_ARG
+    big = _desc(nb=1 << 28, bs=16)
+    assert lib.pa_copy_blocks(p, p, ctypes.byref(big), p, 1, None) == _lib.PA_ERR_INVALID_ARG
+    o = _lib.DecodeOpts(4, _lib.PA_KERNEL_AUTO, None, None)
+    # H not a multiple of Hk, group above 8, unsupported head_dim
+    assert lib.pa_decode(p, p, p, p, ctypes.byref(d), p, 4, p, 2, 12, 1.0, p, 1 << 20, ctypes.byref(o),
+                         None) == _lib.PA_ERR_INVALID_ARG
+    assert lib.pa_decode(p, p, p, p, ctypes.byref(d), p, 4, p, 2, 128, 1.0, p, 1 << 20, ctypes.byref(o),
+                         None) == _lib.PA_ERR_UNSUPPORTED
+    d96 = _desc(d=96)
+    assert lib.pa_decode(p, p, p, p, ctypes.byref(d96), p, 4, p, 2, 32, 1.0, p, 1 << 20, ctypes.byref(o),
+                         None) == _lib.PA_ERR_UNSUPPORTED
+    # the tensor-core kernel needs bf16 and a block size multiple of 16
+    d32 = _desc(dt=_lib.PA_F32, d=64)
+    om = _lib.DecodeOpts(4, _lib.PA_KERNEL_MMA, None, None)
+    assert lib.pa_decode(p, p, p, p, ctypes.byref(d32), p, 4, p, 2, 32, 1.0, p, 1 << 20, ctypes.byref(om),
+                         None) == _lib.PA_ERR_UNSUPPORTED
+    # workspace too small, null workspace, misaligned workspace
+    assert lib.pa_decode(p, p, p, p, ctypes.byref(d), p, 4, p, 2, 32, 1.0, p, 16, ctypes.byref(o),
+                         None) == _lib.PA_ERR_WORKSPACE
+    assert lib.pa_decode(p, p, p, p, ctypes.byref(d), p, 4, p, 2, 32, 1.0, None, 1 << 20, ctypes.byref(o),
+                         None) == _lib.PA_ERR_INVALID_ARG
+    assert lib.pa_decode(p, p, p, p, ctypes.byref(d), p, 4, p, 2, 32, 1.0, ctypes.c_void_p(0x1010),
+                         1 << 20, ctypes.byref(o), None) == _lib.PA_ERR_INVALID_ARG
+    # zero sequences is a no-op
+    assert lib.pa_decode(p, p, p, p, ctypes.byref(d), p, 4, p, 0, 32, 1.0, p, 1 << 20, ctypes.byref(o),
+                         None) == _lib.PA_OK
+
+
+def test_workspace_size_follows_the_split_count(lib):
+    d = _desc()
+    sizes = []
+    for c in (1, 152, 304):
+        o = _lib.DecodeOpts(c, _lib.PA_KERNEL_MMA, None, None)
+        sizes.append(lib.pa_decode_workspace_bytes(ctypes.byref(d), 256, 32, ctypes.byref(o)))
+    assert sizes[0] < sizes[1] < sizes[2]
+    # (C + NG*N) slots x 32 heads x (128 + 2) floats, plus lengths and prefix sums
+    o = _lib.DecodeOpts(152, _lib.PA_KERNEL_MMA, None, None)
+    n = lib.pa_decode_workspace_bytes(ctypes.byref(d), 256, 32, ctypes.byref(o))
+    slots = 152 + 256
+    assert n >= slots * 32 * 130 * 4 and n < slots * 32 * 130 * 4 + 8192
+
+
+def test_split_covers_every_block_once(lib):
+    rng = np.random.default_rng(0)
+    for W, C in [(1, 1), (10, 3), (7, 20), (13264, 152), (32768, 152), (1 << 20, 1000)]:
+        begins = [pa.pa_split_range(W, C, c) for c in range(C)]
+        assert begins[0][0] == 0 and begins[-1][1] == W
+        for c in range(1, C):
+            assert begins[c][0] == begins[c - 1][1]
+        for x in rng.integers(0, W, size=50).tolist() + [0, W - 1]:
+            c = pa.pa_split_owner(W, C, x)
+            b, e = begins[c]
+            assert b <= x < e
+
+
+def test_partial_slots_are_unique():
+    # slot = c + (flattened sequence); check with random ragged sequences
+    import paged_kv_cache_150_gb300 as pa
+
+    rng = np.random.default_rng(1)
+    for _ in range(20):
+        nb = rng.integers(0, 9, size=int(rng.integers(1, 30)))
+        cu = np.concatenate([[0], np.cumsum(nb)])
+        W = int(cu[-1])
+        if W == 0:
+            continue
+        C = int(rng.integers(1, 40))
+        seen = set()
+        for c in range(C):
+            b, e = pa.pa_split_range(W, C, c)
+            for x in range(b, e):
+                seq = int(np.searchsorted(cu, x, side="right") - 1)
+                seen.add((c, seq))
+        slots = [c + s for c, s in seen]
+        assert len(slots) == len(set(slots))
+        assert max(slots) < C + len(nb)

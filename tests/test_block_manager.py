@@ -1,0 +1,140 @@
+"""The product's C++ block manager against the oracle's model of the pages'
+manager: identical tables, slots and copy-on-write pairs on every workload,
+the pages' worked example, and the failure semantics."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_cache_150_gb300 as pa
+from paged_kv_cache_150_gb300 import inputs
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+WORKLOADS = [("cfg0", {}), ("cfg1", {}), ("cfg1", {"small": True}), ("cfg2", {}),
+             ("cfg2", {"small": True}), ("cfg3", {}), ("cfg3", {"prompt_len": 2008}),
+             ("cfg3", {"small": True}), ("cfg3", {"small": True, "prompt_len": 200}),
+             ("cfg4", {}), ("cfg4", {"block_size": 32}), ("cfg4", {"small": True})]
+
+
+@pytest.mark.parametrize("cfg,kw", WORKLOADS)
+def test_manager_matches_oracle_model(cfg, kw):
+    wl = inputs.workload(cfg, **kw)
+    r = oracle.run_script(wl.num_blocks, wl.block_size, wl.free_order, wl.script)
+    bm = pa.BlockManager(wl.num_blocks, wl.block_size, wl.free_order)
+    slots, pairs = bm.apply_script(wl.script)
+    np.testing.assert_array_equal(slots, r["slots"])
+    np.testing.assert_array_equal(pairs, r["pairs"])
+    tables, lens = bm.export(list(range(wl.num_seqs)), wl.max_blocks_per_seq)
+    np.testing.assert_array_equal(tables, oracle.pad_tables(r["tables"], wl.max_blocks_per_seq))
+    np.testing.assert_array_equal(lens, r["lens"])
+    np.testing.assert_array_equal(lens, wl.seq_lens)
+    assert bm.stats() == r["manager"].stats()
+    for b, ref in list(r["manager"].ref.items())[:200]:
+        assert bm.refcount(b) == ref
+
+
+def test_go_worked_example(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "go_worked_example.json")))
+    bm = pa.BlockManager(g["num_blocks"], g["block_size"])
+    seqs = {}
+    for st in g["steps"]:
+        if st["op"] == "new":
+            seqs[st["name"]] = bm.new_seq(st["tokens"])
+        else:
+            bm.free_seq(seqs[st["name"]])
+        free, used, _ = bm.stats()
+        if "expect_free" in st:
+            assert free == st["expect_free"]
+        if "expect_used" in st:
+            assert used == st["expect_used"]
+    assert bm.block_table(seqs["e"]) == g["derived"]["table_e"]
+    assert bm.physical_index(seqs["e"], 40) == g["derived"]["physical_index_e_40"]
+
+
+def test_sharing_example(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "sharing_examples.json")))["parallel_sampling"]
+    B = g["block_size"]
+    bm = pa.BlockManager(len(g["free_order"]), B, g["free_order"])
+    parent = bm.new_seq(3 * B)
+    seqs = [parent] + [bm.fork(parent) for _ in range(3)]
+    assert all(bm.refcount(b) == 4 for b in g["prompt_blocks"])
+    for s in seqs:
+        assert bm.append_token(s)[1] is None
+    assert [bm.block_table(s)[-1] for s in seqs] == g["extra_blocks"]
+    assert bm.stats()[1] == g["physical_blocks"]
+
+
+def test_copy_on_write_pair_and_in_place_last_writer():
+    bm = pa.BlockManager(8, 4)
+    s = bm.new_seq(6)  # blocks [0, 1] (Go order: top two ids in stack order)
+    kids = [bm.fork(s) for _ in range(2)]
+    shared_last = bm.block_table(s)[1]
+    got = [bm.append_token(x) for x in [s] + kids]
+    assert got[0][1] is not None and got[1][1] is not None and got[2][1] is None
+    assert got[0][1][0] == shared_last and got[1][1][0] == shared_last
+    assert bm.block_table(kids[1])[1] == shared_last and bm.refcount(shared_last) == 1
+    for x in [s] + kids:
+        slot = bm.physical_index(x, 6)
+        assert bm.refcount(slot // 4) == 1
+
+
+def _snapshot(bm, seqs):
+    return (bm.stats(), [bm.block_table(s) for s in seqs], [bm.seq_len(s) for s in seqs])
+
+
+def test_failures_change_nothing():
+    bm = pa.BlockManager(3, 4)
+    a = bm.new_seq(8)
+    snap = _snapshot(bm, [a])
+    with pytest.raises(pa.PagedAttentionError) as e:
+        bm.new_seq(9)
+    assert e.value.status == -4 and _snapshot(bm, [a]) == snap
+    with pytest.raises(pa.PagedAttentionError):
+        bm.append_tokens(a, 5)  # needs 2 new blocks, 1 free: all or nothing
+    assert _snapshot(bm, [a]) == snap
+    bm2 = pa.BlockManager(2, 4)
+    s = bm2.new_seq(6)
+    t = bm2.fork(s)
+    snap2 = _snapshot(bm2, [s, t])
+    with pytest.raises(pa.PagedAttentionError):
+        bm2.append_token(s)  # copy needed, pool empty
+    assert _snapshot(bm2, [s, t]) == snap2
+    bm2.free_seq(t)
+    with pytest.raises(pa.PagedAttentionError):
+        bm2.free_seq(t)  # double free
+    slot, pair = bm2.append_token(s)  # now unshared: written in place
+    assert pair is None and slot == bm2.block_table(s)[1] * 4 + 2
+
+
+def test_bad_free_order_is_rejected():
+    with pytest.raises(ValueError):
+        pa.BlockManager(4, 4, [0, 1, 1, 2])
+    with pytest.raises(ValueError):
+        pa.BlockManager(4, 4, [0, 1, 2, 4])
+
+
+def test_append_tokens_matches_repeated_append_token():
+    rng = np.random.default_rng(3)
+    order = rng.permutation(64).astype(np.int32)
+    a = pa.BlockManager(64, 8, order)
+    b = pa.BlockManager(64, 8, order)
+    for m in (a, b):
+        p = m.new_seq(13)
+        m.fork(p)
+        m.fork(p)
+    for seq, count in [(0, 5), (1, 17), (2, 1), (0, 9)]:
+        slots_a, pair_a = a.append_tokens(seq, count)
+        singles = [b.append_token(seq) for _ in range(count)]
+        assert slots_a.tolist() == [x[0] for x in singles]
+        pairs_b = [x[1] for x in singles if x[1] is not None]
+        assert (pair_a is None and not pairs_b) or [pair_a] == pairs_b
+    assert a.stats() == b.stats()

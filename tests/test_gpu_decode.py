@@ -1,0 +1,162 @@
+"""GPU parity of paged decode attention against the fp64 oracle.
+
+Tolerances (max-abs against the fp64 result): 1e-5 for fp32 inputs, 2e-2 for
+bf16 inputs with fp32 accumulation.  Small cases compare every output; full
+size cases run in the benchmark's launch configuration (automatic kernel
+choice, one wave of CTAs) and compare a sample of (sequence, head) pairs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_150_gb300 as pa
+from paged_kv_cache_150_gb300 import inputs
+from _pipeline import TOL, gpu_step, host_values, max_abs_err, oracle_decode, oracle_step, sample_pairs
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [("cfg0", {}), ("cfg1", {"small": True}), ("cfg2", {"small": True}),
+         ("cfg3", {"small": True}), ("cfg3", {"small": True, "prompt_len": 200}),
+         ("cfg4", {"small": True}), ("cfg4", {"small": True, "block_size": 32})]
+
+
+@pytest.mark.parametrize("cfg,kw", SMALL)
+@pytest.mark.parametrize("kernel,splits", [("auto", 0), ("auto", 1), ("auto", 7), ("simt", 0), ("simt", 5)])
+def test_decode_small(cfg, kw, kernel, splits):
+    wl = inputs.workload(cfg, **kw)
+    dev, host = host_values(wl, "cpu")
+    r = oracle_step(wl, host)
+    ref = oracle_decode(wl, host, r)
+    g = gpu_step(wl, dev, kernel=kernel, num_splits=splits)
+    err = max_abs_err(g["out"], ref)
+    assert err <= TOL[wl.dtype], err
+
+
+FULL = [("cfg1", {}, 64), ("cfg2", {}, 96), ("cfg3", {}, 48), ("cfg3", {"prompt_len": 2008}, 48),
+        ("cfg4", {}, 24), ("cfg4", {"block_size": 32}, 24)]
+
+
+@pytest.mark.parametrize("cfg,kw,nsample", FULL)
+def test_decode_full_size_sampled(cfg, kw, nsample):
+    wl = inputs.workload(cfg, **kw)
+    dev, host = host_values(wl, "cuda")
+    r = oracle_step(wl, host)
+    g = gpu_step(wl, dev)
+    pairs = sample_pairs(wl, nsample)
+    ref = oracle_decode(wl, host, r, pairs=pairs)
+    err = max_abs_err(g["out"], ref, pairs)
+    assert err <= TOL[wl.dtype], err
+    assert torch.isfinite(g["out"].float()).all()
+
+
+# ------------------------------------------------------------- shape sweep
+SHAPES = [  # (dtype, H, Hk, D, B)
+    ("bf16", 8, 8, 128, 16), ("bf16", 16, 8, 128, 16), ("bf16", 32, 8, 128, 32), ("bf16", 64, 8, 128, 32),
+    ("bf16", 8, 1, 128, 16), ("bf16", 6, 2, 64, 16), ("bf16", 12, 4, 64, 32), ("bf16", 8, 8, 256, 16),
+    ("bf16", 4, 4, 128, 8), ("f32", 8, 2, 128, 16), ("f32", 4, 4, 64, 4), ("f32", 3, 1, 64, 5),
+]
+
+
+@pytest.mark.parametrize("dtype,H,Hk,D,B", SHAPES)
+@pytest.mark.parametrize("splits", [0, 3])
+def test_decode_shapes(dtype, H, Hk, D, B, splits):
+    lens = [1, B - 1, B, B + 1, 5 * B + 3, 2, 0, 77]
+    wl = inputs.decode_workload("shape", lens, H, Hk, D, B, dtype, seed=99, pool_factor=1.3)
+    dev, host = host_values(wl, "cpu")
+    r = oracle_step(wl, host)
+    ref = oracle_decode(wl, host, r)
+    for kernel in ("auto", "simt"):
+        g = gpu_step(wl, {k: v.clone() for k, v in dev.items()}, kernel=kernel, num_splits=splits)
+        err = max_abs_err(g["out"], ref)
+        assert err <= TOL[dtype], (kernel, err)
+        assert (g["out"][6] == 0).all()  # the empty sequence
+
+
+def test_single_token_sequences_return_their_value_rows_exactly():
+    wl = inputs.decode_workload("one", [1] * 10, 16, 2, 128, 16, "bf16", seed=5, pool_factor=2.0)
+    dev, host = host_values(wl, "cpu")
+    g = gpu_step(wl, dev)
+    for i in range(10):
+        slot = int(g["host_slots"][i])
+        row = g["v_cache"].view(-1, 2, 128)[slot]
+        for h in range(16):
+            assert torch.equal(g["out"][i, h], row[h // 8])
+
+
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
+def test_stale_slots_full_of_nan_are_never_read(kernel):
+    wl = inputs.decode_workload("nan", [3, 17, 40, 16, 100], 32, 8, 128, 16, "bf16", seed=6, pool_factor=1.5)
+    dev, host = host_values(wl, "cpu")
+    r = oracle.run_script(wl.num_blocks, wl.block_size, wl.free_order, wl.script)
+    live = np.zeros((wl.num_blocks, wl.block_size), bool)
+    for t, L in zip(r["tables"], r["lens"]):
+        for pos in range(int(L)):
+            live[t[pos // wl.block_size], pos % wl.block_size] = True
+    nan_bits = np.uint16(0x7FC0)
+    for name in ("k_cache", "v_cache"):
+        host[name][~live] = nan_bits
+        dev[name].view(torch.int16)[torch.from_numpy(~live).cuda()] = int(np.int16(0x7FC0))
+    r = oracle_step(wl, host)
+    ref = oracle_decode(wl, host, r)
+    assert np.isfinite(ref).all()
+    g = gpu_step(wl, dev, kernel=kernel, num_splits=4)
+    assert torch.isfinite(g["out"].float()).all()
+    assert max_abs_err(g["out"], ref) <= TOL["bf16"]
+
+
+def test_split_count_does_not_change_the_result():
+    wl = inputs.workload("cfg4", small=True)
+    dev, host = host_values(wl, "cpu")
+    r = oracle_step(wl, host)
+    ref = oracle_decode(wl, host, r)
+    outs = []
+    for splits in (1, 2, 7, 33, 0):
+        g = gpu_step(wl, {k: v.clone() for k, v in dev.items()}, num_splits=splits)
+        assert max_abs_err(g["out"], ref) <= TOL["bf16"]
+        outs.append(g["out"].float())
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max().item() <= TOL["bf16"]
+
+
+def test_block_size_16_and_32_agree():
+    lens = [4096 + 5, 35, 700]
+    outs = []
+    for B in (16, 32):
+        wl = inputs.decode_workload("b%d" % B, lens, 64, 8, 128, B, "bf16", seed=7, pool_factor=1.05)
+        # same logical rows for both layouts: write every token through the cache write
+        q = torch.randn(3, 64, 128, generator=torch.Generator().manual_seed(8)).to(torch.bfloat16).cuda()
+        rows_k = torch.randn(sum(lens), 8, 128, generator=torch.Generator().manual_seed(9)).to(torch.bfloat16).cuda()
+        rows_v = torch.randn(sum(lens), 8, 128, generator=torch.Generator().manual_seed(10)).to(torch.bfloat16).cuda()
+        bm = pa.BlockManager(wl.num_blocks, B, wl.free_order)
+        slots = []
+        for L in lens:
+            s = bm.new_seq(0)
+            slots.append(bm.append_tokens(s, L)[0])
+        tables, lens_np = bm.export([0, 1, 2], max(-(-L // B) for L in lens))
+        kc = torch.zeros(wl.num_blocks, B, 8, 128, dtype=torch.bfloat16, device="cuda")
+        vc = torch.zeros_like(kc)
+        pa.pa_reshape_and_cache(rows_k, rows_v, torch.from_numpy(np.concatenate(slots)).cuda(), kc, vc)
+        out = pa.pa_decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens_np).cuda(),
+                           1 / math.sqrt(128))
+        outs.append(out.float())
+    assert (outs[0] - outs[1]).abs().max().item() <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
+def test_bad_table_entry_and_length_are_reported_without_a_fault(kernel):
+    wl = inputs.decode_workload("bad", [40, 33], 16, 8, 128, 16, "bf16", seed=11, pool_factor=1.0)
+    dev, host = host_values(wl, "cpu")
+    g = gpu_step(wl, dev, decode=False)
+    tables = g["tables"].clone()
+    tables[0, 1] = wl.num_blocks + 3
+    pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], tables, g["lens"], wl.scale, kernel=kernel)
+    assert pa.pa_get_device_error(raise_on_error=False) == pa._lib.PA_ERR_DEVICE_BOUNDS
+    lens = g["lens"].clone()
+    lens[1] = 10 ** 6
+    out = pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["tables"], lens, wl.scale, kernel=kernel)
+    assert pa.pa_get_device_error(raise_on_error=False) == pa._lib.PA_ERR_DEVICE_BOUNDS
+    assert (out[1] == 0).all()  # an out-of-range length counts as 0
+    pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale, kernel=kernel)
+    assert pa.pa_get_device_error(raise_on_error=False) == 0
