@@ -1,0 +1,495 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-KV decode hot path on GB300.
+
+One step = one pass of the whole path over one batch: copy-on-write block
+copies (when the batch has any), the slot-mapped KV write of the step's new
+tokens, and paged decode attention (plan, attention kernel, split reduce).
+
+Headline workload: 16 sequences x 32768 tokens, 64 query / 8 KV heads,
+head_dim 128, bf16, block_size 16, blocks randomly placed in a pool of 1.05x
+the need (2,147,483,648 bytes of K and V read per step).  The metric is KV
+bytes read per second (GB/s); decode tokens/s and the fraction of the measured
+HBM bandwidth are reported beside it.  Other workloads (the mixed-length GQA
+batch, block_size 32, MHA, parallel sampling with copy-on-write) are timed
+the same way and reported under "workloads".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs the same per-GPU workload on its own GPU (weak
+scaling, no data-path collective); rank 0 prints one JSON line.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: KV bytes read GB/s (% of GB300 HBM peak), tokens/s"
+EXTRA = [("cfg2", {}), ("cfg4", {"block_size": 32}), ("cfg1", {}), ("cfg3", {"prompt_len": 2008}), ("cfg4", {"block_size": 16})]
+FLUSH_BYTES = 512 << 20  # > 129 MB L2: written between timed steps
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="time only the headline workload")
+    ap.add_argument("--extra-steps", type=int, default=300)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--workload", default="cfg4-b16",
+                    help="headline workload: cfg4-b16 (default), cfg4-b32, cfg2, cfg1, cfg3-p2000, cfg3-p2008")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    return ap.parse_args()
+
+
+WORKLOADS = {"cfg4-b16": ("cfg4", {"block_size": 16}), "cfg4-b32": ("cfg4", {"block_size": 32}),
+             "cfg2": ("cfg2", {}), "cfg1": ("cfg1", {}), "cfg3-p2000": ("cfg3", {}),
+             "cfg3-p2008": ("cfg3", {"prompt_len": 2008})}
+
+
+# ---------------------------------------------------------------- helpers
+def dist_setup(args):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def reduce_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_r%d.csv" % os.getpid())
+        try:
+            import torch
+
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            sel = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or "0"
+        self.sel = sel
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.sel, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_sha():
+    h = hashlib.sha256()
+    for f in ("decode.cu", "pa_common.cuh"):
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_150_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None, None
+    e = d.get(workload_name)
+    if not e or e.get("source_sha") != source_sha():
+        return None, e.get("source_sha") if e else None
+    return float(e["dram_bytes_per_launch"]), e["source_sha"]
+
+
+# ------------------------------------------------------------- the step
+class Step:
+    """Device-resident state of one workload and its step."""
+
+    def __init__(self, cfg, kw, seed_offset=0):
+        import numpy as np
+        import torch
+
+        import paged_kv_cache_150_gb300 as pa
+        from paged_kv_cache_150_gb300 import inputs
+
+        self.pa = pa
+        wl = inputs.workload(cfg, **kw)
+        wl.seed += seed_offset
+        self.wl = wl
+        vals = inputs.make_values(wl, device="cuda")
+        self.initial_host = None
+        self.vals = vals
+        bm = pa.BlockManager(wl.num_blocks, wl.block_size, wl.free_order)
+        t0 = time.perf_counter()
+        slots, pairs = bm.apply_script(wl.script)
+        tables, lens = bm.export(list(range(wl.num_seqs)), wl.max_blocks_per_seq)
+        self.bm_ms = (time.perf_counter() - t0) * 1e3
+        self.host = {"slots": slots, "pairs": pairs, "tables": tables, "lens": lens}
+        self.slots = torch.from_numpy(slots).cuda()
+        self.pairs = torch.from_numpy(pairs).cuda()
+        self.tables = torch.from_numpy(tables).cuda()
+        self.lens = torch.from_numpy(lens).cuda()
+        self.out = torch.empty_like(vals["q"])
+        ws = pa.pa_decode_workspace_bytes(vals["k_cache"], wl.num_seqs, wl.num_q_heads)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device="cuda")
+        self.kernel_launches = 4 + (1 if pairs.shape[0] else 0)
+        H, D, eb = wl.num_q_heads, wl.head_dim, wl.elem_bytes
+        self.kv_bytes = wl.kv_bytes_read()
+        nb_used = int(sum(-(-int(L) // wl.block_size) for L in wl.seq_lens))
+        # attention kernel's algorithmic bytes: K/V rows, q, out, block-table entries
+        self.kernel_bytes = self.kv_bytes + 2 * wl.num_seqs * H * D * eb + 4 * nb_used
+        self.tokens = wl.num_seqs
+
+    def keep_initial_host_copy(self):
+        from paged_kv_cache_150_gb300 import inputs
+
+        self.initial_host = {k: inputs.to_numpy_elems(v).copy() for k, v in self.vals.items()}
+
+    def run(self, events=None):
+        pa, v = self.pa, self.vals
+        if self.pairs.shape[0]:
+            pa.pa_copy_blocks(v["k_cache"], v["v_cache"], self.pairs)
+        pa.pa_reshape_and_cache(v["k"], v["v"], self.slots, v["k_cache"], v["v_cache"])
+        pa.pa_decode(v["q"], v["k_cache"], v["v_cache"], self.tables, self.lens, self.wl.scale, out=self.out,
+                     workspace=self.workspace, events=events)
+
+
+def time_steps(step, steps, warmup, world, flush, sampler=None):
+    import torch
+
+    for _ in range(warmup):
+        flush.zero_()
+        step.run()
+    torch.cuda.synchronize()
+    step.pa.pa_get_device_error()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for pair in ev + kev:  # create the CUDA events outside the timed region
+        pair[0].record()
+        pair[1].record()
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record()
+        step.run(events=kev[i])
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    step.pa.pa_get_device_error()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    return step_ms, kern_ms, clocks
+
+
+def time_e2e(step, steps):
+    """Through the public API with host buffers: pinned H2D of the step's
+    inputs, the step, and a D2H read of the output, synchronised per step."""
+    import torch
+
+    v = step.vals
+    srcs = {"q": v["q"], "k": v["k"], "v": v["v"], "slots": step.slots, "tables": step.tables,
+            "lens": step.lens, "pairs": step.pairs}
+    pinned = {k: t.cpu().pin_memory() for k, t in srcs.items()}
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = out_host.numel() * out_host.element_size()
+    times = []
+    stream = torch.cuda.current_stream()
+    for i in range(steps + 3):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for k, t in pinned.items():
+            srcs[k].copy_(t, non_blocking=True)
+        step.run()
+        out_host.copy_(step.out, non_blocking=True)
+        stream.synchronize()
+        if i >= 3:
+            times.append(time.perf_counter() - t0)
+    return statistics.mean(times), h2d, d2h
+
+
+def oracle_baseline(step, max_groups, threads):
+    """The CPU oracle, as it stands, on a bounded sample of the workload:
+    whole (sequence, KV head) groups, all G query heads of each."""
+    import oracle
+
+    wl = step.wl
+    if step.initial_host is None:
+        raise RuntimeError("initial host copy missing")
+    host = step.initial_host
+    r = oracle.run_script(wl.num_blocks, wl.block_size, wl.free_order, wl.script)
+    kc, vc = host["k_cache"].copy(), host["v_cache"].copy()
+    oracle.copy_blocks(kc, vc, r["pairs"])
+    oracle.reshape_and_cache(host["k"], host["v"], r["slots"], kc, vc)
+    tables = oracle.pad_tables(r["tables"], wl.max_blocks_per_seq)
+    G = wl.num_q_heads // wl.num_kv_heads
+    groups = [(s, kh) for s in range(wl.num_seqs) for kh in range(wl.num_kv_heads)][:max_groups]
+    pairs = [(s, kh * G + j) for s, kh in groups for j in range(G)]
+    t0 = time.perf_counter()
+    ref = oracle.decode(host["q"], kc, vc, tables, r["lens"], wl.scale, pairs=pairs, num_threads=threads)
+    dt = time.perf_counter() - t0
+    bytes_ = sum(int(wl.seq_lens[s]) * wl.head_dim * 2 * wl.elem_bytes for s, _ in groups)
+    return ref, pairs, dt, bytes_, len(groups)
+
+
+def parity_check(step, ref, pairs):
+    import numpy as np
+
+    out = step.out.double().cpu().numpy()
+    idx = np.asarray(pairs)
+    return float(np.abs(out[idx[:, 0], idx[:, 1]] - ref[idx[:, 0], idx[:, 1]]).max())
+
+
+def workload_name(step):
+    return step.wl.name
+
+
+def describe(wl):
+    G = wl.num_q_heads // wl.num_kv_heads
+    return ("%s: %d seqs (lengths %d..%d, %d tokens), %d q / %d KV heads (group %d), head_dim %d, %s, "
+            "block %d, pool %d blocks, seeded random placement; %s"
+            % (wl.name, wl.num_seqs, int(wl.seq_lens.min()), int(wl.seq_lens.max()), int(wl.seq_lens.sum()),
+               wl.num_q_heads, wl.num_kv_heads, G, wl.head_dim, wl.dtype, wl.block_size, wl.num_blocks, wl.note))
+
+
+# -------------------------------------------------------------- arms
+def run_ours(args, rank, world):
+    import torch
+
+    peak, peak_kind = measured_peaks()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    step = Step(*WORKLOADS[args.workload], seed_offset=1000 * rank)
+    do_cpu = rank == 0 and world == 1 and not args.no_cpu
+    if do_cpu:
+        step.keep_initial_host_copy()
+    sampler = ClockSampler(torch.cuda.current_device())
+    step_ms, kern_ms, clocks = time_steps(step, args.steps, args.warmup, world, flush, sampler)
+    total_ms = reduce_max(sum(step_ms), world)
+    ms_per_step = total_ms / args.steps
+    value = world * step.kv_bytes * args.steps / (total_ms / 1e3) / 1e9
+    tokens_per_s = world * step.tokens * args.steps / (total_ms / 1e3)
+    kern_avg_ms = statistics.mean(kern_ms)
+    achieved = step.kernel_bytes / (kern_avg_ms / 1e3) / 1e9
+    traffic, _ = profiled_traffic(workload_name(step))
+
+    if args.no_e2e:
+        e2e_s, h2d, d2h = float("nan"), 0, 0
+    else:
+        e2e_s, h2d, d2h = time_e2e(step, args.e2e_steps)
+    e2e_value = world * step.kv_bytes / e2e_s / 1e9
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": describe(step.wl),
+                   "kv_bytes_per_step": step.kv_bytes, "num_seqs": step.wl.num_seqs,
+                   "max_seq_len": int(step.wl.seq_lens.max()), "block_size": step.wl.block_size,
+                   "l2": "512 MiB buffer written between timed steps",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tokens_per_s": round(tokens_per_s, 1),
+        "hbm_frac": round(value / world / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": "decode attention (tensor-core kernel)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": step.kernel_bytes,
+                     "avg_launch_ms": round(kern_avg_ms, 5), "peak_source": peak_kind},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
+        "gpu_launches": step.kernel_launches * args.steps,
+        "clocks": clocks,
+        "block_manager_ms": round(step.bm_ms, 3),
+    }
+    if do_cpu:
+        import oracle
+
+        threads = oracle.available_threads()
+        ref, pairs, dt, nbytes, ngroups = oracle_baseline(step, 128, threads)
+        line["cpu_baseline"] = {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": "%d of %d (sequence, KV head) groups of the workload, all query heads, "
+                                          "fp64, %.1f s wall" % (ngroups, step.wl.num_seqs * step.wl.num_kv_heads, dt)}
+        line["parity"] = {"max_abs_err": parity_check(step, ref, pairs), "pairs_checked": len(pairs),
+                          "tolerance": 2e-2}
+    del step
+    torch.cuda.empty_cache()
+    if not args.no_extra:
+        extra = {}
+        for cfg, kw in EXTRA:
+            if WORKLOADS[args.workload] == (cfg, kw):
+                continue
+            st = Step(cfg, kw, seed_offset=1000 * rank)
+            sm, km, _ = time_steps(st, args.extra_steps, args.warmup, world, flush)
+            mean_ms = reduce_max(statistics.mean(sm), world)
+            kms = statistics.mean(km)
+            extra[st.wl.name] = {"kv_gbs": round(st.kv_bytes / (mean_ms / 1e3) / 1e9, 2),
+                                 "ms_per_step": round(mean_ms, 5),
+                                 "tokens_per_s": round(st.tokens / (mean_ms / 1e3), 1),
+                                 "hbm_frac": round(st.kv_bytes / (mean_ms / 1e3) / 1e9 / peak, 4),
+                                 "kernel_gbs": round(st.kernel_bytes / (kms / 1e3) / 1e9, 2),
+                                 "kernel_ms": round(kms, 5), "kv_bytes": st.kv_bytes,
+                                 "cow_pairs": int(st.host["pairs"].shape[0]), "new_tokens": st.wl.num_new_tokens}
+            del st
+            torch.cuda.empty_cache()
+        line["workloads"] = extra
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm, timed on this machine's host cores."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from paged_kv_cache_150_gb300 import inputs
+
+    cfg, kw = WORKLOADS[args.workload]
+    wl = inputs.workload(cfg, **kw)
+    vals = inputs.make_values(wl, device="cpu")
+    host = {k: inputs.to_numpy_elems(v).copy() for k, v in vals.items()}
+    r = oracle.run_script(wl.num_blocks, wl.block_size, wl.free_order, wl.script)
+    kc, vc = host["k_cache"], host["v_cache"]
+    oracle.copy_blocks(kc, vc, r["pairs"])
+    oracle.reshape_and_cache(host["k"], host["v"], r["slots"], kc, vc)
+    tables = oracle.pad_tables(r["tables"], wl.max_blocks_per_seq)
+    threads = oracle.available_threads()
+    G = wl.num_q_heads // wl.num_kv_heads
+    groups_all = [(s, kh) for s in range(wl.num_seqs) for kh in range(wl.num_kv_heads)]
+    # one step = a bounded sample of (sequence, KV head) groups, sized so the
+    # whole run stays within a few minutes
+    budget_s = 150.0
+    t0 = time.perf_counter()
+    oracle.decode(host["q"], kc, vc, tables, r["lens"], wl.scale,
+                  pairs=[(0, j) for j in range(G)], num_threads=threads)
+    t_group = time.perf_counter() - t0
+    per_step = max(1, min(len(groups_all), int(budget_s / max(args.steps + args.warmup, 1) / max(t_group, 1e-6))))
+    times, nbytes = [], 0
+    for i in range(args.warmup + args.steps):
+        gs = [groups_all[(i * per_step + j) % len(groups_all)] for j in range(per_step)]
+        pairs = [(s, kh * G + j) for s, kh in gs for j in range(G)]
+        t0 = time.perf_counter()
+        oracle.decode(host["q"], kc, vc, tables, r["lens"], wl.scale, pairs=pairs, num_threads=threads)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            nbytes += sum(int(wl.seq_lens[s]) * wl.head_dim * 2 * wl.elem_bytes for s, _ in gs)
+    total = sum(times)
+    value = nbytes / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(wl), "kv_bytes_per_step": wl.kv_bytes_read(),
+                   "per_step_sample": "%d (sequence, KV head) groups, all query heads" % per_step},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": "%d groups per step of %d" % (per_step, len(groups_all))},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, _ = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        import __graft_entry__
+
+        __graft_entry__.build()
+        run_ours(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -97,6 +97,9 @@ def pa_copy_blocks(k_cache, v_cache, src_dst_pairs):
 def _opts(num_splits, kernel, events):
     o = _lib.DecodeOpts(int(num_splits), _KERNELS[kernel], None, None)
     if events is not None:
+        for e in events:
+            if not e.cuda_event:  # torch creates the CUDA event on its first record
+                e.record()
         o.ev_partial_begin = ctypes.c_void_p(events[0].cuda_event)
         o.ev_partial_end = ctypes.c_void_p(events[1].cuda_event)
     return o

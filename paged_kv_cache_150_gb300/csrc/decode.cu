@@ -10,25 +10,20 @@
 //
 // How (GB300 design; the pages give only a one-CTA-per-(seq, head) sketch):
 // 1. decode_plan_kernel: one CTA turns seq_lens into block counts and their
-//    exclusive prefix sums cu[] (and clamps bad lengths, recording them).
+//    exclusive prefix sums cu[], clamps bad lengths (recording them), zeroes
+//    the merge counters and writes the zero output of empty sequences.
 // 2. A persistent grid of C CTAs splits the flattened list of
-//    (KV-head group, sequence, block) into C equal contiguous ranges
-//    (split_begin).  A CTA walks its range; each of its consumer warps owns
-//    one KV head and all G query heads that share it, so each KV byte is read
-//    from HBM once.  A range piece covering a whole sequence writes `out`
-//    directly; a piece of a longer sequence writes an unnormalised partial
-//    (running max m in log2 units, sum l, accumulator) to the workspace.
-// 3. decode_reduce_kernel merges the partials of each cut sequence:
-//    out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p, M = max_p m_p.
+//    (KV-head group, sequence, block) into Ce = min(C, W) equal contiguous
+//    ranges (split_begin).  A CTA walks its range; each of its consumer warps
+//    owns one KV head and all G query heads that share it, so each KV byte is
+//    read from HBM once.  A range piece covering a whole sequence writes `out`
+//    directly.  A piece of a longer sequence writes an unnormalised partial
+//    (running max m in log2 units, sum l, accumulator) to the workspace and
+//    bumps an arrival counter for its (sequence, KV head); the warp that
+//    arrives last merges every piece (the split-K reduce, fused):
+//      out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
+//    Nothing ever waits for another CTA: the merge is done by whoever is last.
 //
-// Two attention kernels share this plan:
-//  - decode_mma_kernel (bf16): a producer warp streams whole (block, head
-//    group) tiles of K and V into a multi-stage shared-memory ring with TMA
-//    (cp.async.bulk.tensor, 128-byte swizzle, mbarrier completion); consumer
-//    warps compute S^T = K Q^T and O^T += V^T P^T with mma.sync m16n8k16
-//    (tokens on M, the G heads on N) and an online softmax in registers.
-//  - decode_simt_kernel (fp32, or bf16 shapes the MMA kernel does not cover):
-//    plain coalesced loads, warp-shuffle dot products.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -43,18 +38,25 @@ __device__ __forceinline__ void store_out(float *p, float v) { *p = v; }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
 
 // ---------------------------------------------------------------- plan kernel
+template <typename T>
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__restrict__ seq_lens, int32_t N,
-                                                           int32_t B, int32_t max_len,
+                                                           int32_t B, int32_t max_len, int32_t HD,
                                                            int32_t *__restrict__ lens_ws,
                                                            int32_t *__restrict__ cu,
+                                                           unsigned int *__restrict__ counters,
+                                                           int32_t num_counters, T *__restrict__ out,
                                                            unsigned int *__restrict__ err) {
     __shared__ int32_t warp_incl[32];
     __shared__ int32_t carry;
+    __shared__ int32_t n_empty;
+    __shared__ int32_t empty_ids[1024];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
     if (threadIdx.x == 0) carry = 0;
-    __syncthreads();
+    for (int32_t i = threadIdx.x; i < num_counters; i += blockDim.x) counters[i] = 0u;
     for (int32_t base = 0; base < N; base += blockDim.x) {
+        if (threadIdx.x == 0) n_empty = 0;
+        __syncthreads();
         const int32_t i = base + threadIdx.x;
         int32_t nb = 0;
         if (i < N) {
@@ -65,6 +67,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
             }
             lens_ws[i] = L;
             nb = (L + B - 1) / B;
+            if (L == 0) empty_ids[atomicAdd(&n_empty, 1)] = i;
         }
         int32_t x = nb;  // inclusive scan within the warp
 #pragma unroll
@@ -86,6 +89,11 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
         __syncthreads();
         const int32_t incl = x + (w > 0 ? warp_incl[w - 1] : 0) + carry;
         if (i < N) cu[i] = incl - nb;
+        // empty sequences of this pass: their output is zero
+        for (int32_t k = 0; k < n_empty; ++k) {
+            T *o = out + (int64_t)empty_ids[k] * HD;
+            for (int32_t e = threadIdx.x; e < HD; e += blockDim.x) store_out(o + e, 0.f);
+        }
         __syncthreads();
         if (threadIdx.x == blockDim.x - 1) carry = incl;
         __syncthreads();
@@ -93,48 +101,77 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
     if (threadIdx.x == 0) cu[N] = carry;
 }
 
-// -------------------------------------------------------------- reduce kernel
-// One CTA per (group, sequence); one warp per query head of the group.
-template <typename T>
-__global__ void __launch_bounds__(128) decode_reduce_kernel(T *__restrict__ out,
-                                                            const float2 *__restrict__ ml_ws,
-                                                            const float *__restrict__ acc_ws,
-                                                            const int32_t *__restrict__ cu, int32_t N,
-                                                            int32_t H, int32_t D, int32_t NG,
-                                                            int32_t HPG, int32_t C) {
-    const int32_t sp = blockIdx.x;
-    const int32_t g = sp / N, i = sp - g * N;
-    const int32_t Wg = cu[N];
-    const int64_t W = (int64_t)NG * Wg;
-    const int32_t nb = cu[i + 1] - cu[i];
-    T *o = out + ((int64_t)i * H + (int64_t)g * HPG) * D;
-    if (nb == 0) {  // empty sequence: output zero
-        for (int e = threadIdx.x; e < HPG * D; e += blockDim.x) store_out(o + e, 0.f);
-        return;
-    }
-    const int64_t x0 = (int64_t)g * Wg + cu[i];
-    const int32_t c0 = split_owner(x0, W, C);
-    const int32_t c1 = split_owner(x0 + nb - 1, W, C);
-    if (c0 == c1) return;  // written directly by the attention kernel
-    const int lane = threadIdx.x & 31;
-    for (int hh = threadIdx.x >> 5; hh < HPG; hh += blockDim.x >> 5) {
-        float M = -INFINITY;
-        for (int32_t c = c0; c <= c1; ++c) M = fmaxf(M, ml_ws[partial_slot(c, sp) * HPG + hh].x);
-        float Lsum = 0.f;
-        for (int32_t c = c0; c <= c1; ++c) {
-            const float2 v = ml_ws[partial_slot(c, sp) * HPG + hh];
-            Lsum += ex2_approx(v.x - M) * v.y;
+// ------------------------------------------------------------ piece merge
+// Run by the warp that finished the last piece of one (sequence, KV head):
+// merges the pieces held by CTAs c0..c1 for its G query heads.  Lanes split
+// the G heads x D outputs (lane -> head lane / LPH, a contiguous slice of
+// D / LPH elements); one pass over the pieces with a running max, so every
+// load is independent of the previous piece's arithmetic.
+template <typename T, int D>
+__device__ __forceinline__ void merge_pieces(T *__restrict__ out_base, const float2 *__restrict__ ml_ws,
+                                             const float *__restrict__ acc_ws, int32_t c0, int32_t c1,
+                                             int32_t sp, int32_t HPG, int32_t hoff, int32_t G, int lane) {
+    // lanes per head: 32 / (G rounded up to a power of two), at least D/32 elements per lane
+    const int g2 = G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : 8));
+    const int lph = min(32 / g2, D / 4);  // slices of >= 4 elements (float4 loads)
+    const int h = lane / lph;
+    const int part = lane - h * lph;
+    constexpr int EMAX = D / 4;  // elements per lane when lph == 4
+    const int E = D / lph;
+    if (h >= G) return;
+    float a[EMAX];
+#pragma unroll
+    for (int j = 0; j < EMAX; ++j) a[j] = 0.f;
+    float M = -INFINITY, Ls = 0.f;
+    for (int32_t c = c0; c <= c1; ++c) {
+        const int64_t idx = partial_slot(c, sp) * HPG + hoff + h;
+        const float2 v = __ldcg(&ml_ws[idx]);
+        const float4 *ap = reinterpret_cast<const float4 *>(acc_ws + idx * D + part * E);
+        const float Mn = fmaxf(M, v.x);
+        const float s_old = ex2_approx(M - Mn), s_new = ex2_approx(v.x - Mn);
+        Ls = Ls * s_old + v.y * s_new;
+#pragma unroll
+        for (int j4 = 0; j4 < EMAX / 4; ++j4) {
+            if (j4 * 4 >= E) break;
+            const float4 x = __ldcg(ap + j4);
+            a[4 * j4 + 0] = fmaf(a[4 * j4 + 0], s_old, s_new * x.x);
+            a[4 * j4 + 1] = fmaf(a[4 * j4 + 1], s_old, s_new * x.y);
+            a[4 * j4 + 2] = fmaf(a[4 * j4 + 2], s_old, s_new * x.z);
+            a[4 * j4 + 3] = fmaf(a[4 * j4 + 3], s_old, s_new * x.w);
         }
-        const float inv = 1.f / Lsum;
-        for (int d = lane; d < D; d += 32) {
-            float a = 0.f;
-            for (int32_t c = c0; c <= c1; ++c) {
-                const int64_t slot = partial_slot(c, sp);
-                a += ex2_approx(ml_ws[slot * HPG + hh].x - M) * acc_ws[(slot * HPG + hh) * D + d];
-            }
-            store_out(o + (int64_t)hh * D + d, a * inv);
-        }
+        M = Mn;
     }
+    const float inv = 1.f / Ls;
+    T *o = out_base + (int64_t)h * D + part * E;
+#pragma unroll
+    for (int j = 0; j < EMAX; ++j) {
+        if (j >= E) break;
+        store_out(o + j, a[j] * inv);
+    }
+}
+
+// After a warp wrote its partial for (sequence seq of group g, KV head kvh):
+// publish it, count the arrival, and merge if this warp is the last one.
+template <typename T, int D>
+__device__ __forceinline__ void finish_piece(T *__restrict__ out, const float2 *__restrict__ ml_ws,
+                                             const float *__restrict__ acc_ws, unsigned int *__restrict__ counters,
+                                             const int32_t *__restrict__ cu, int32_t N, int32_t H, int32_t G,
+                                             int32_t NH, int32_t warp, int32_t g, int32_t seq, int32_t nb,
+                                             int64_t W, int32_t Ce, int lane) {
+    const int32_t sp = g * N + seq;
+    const int64_t x0 = (int64_t)g * cu[N] + cu[seq];
+    const int32_t c0 = split_owner(x0, W, Ce);
+    const int32_t c1 = split_owner(x0 + nb - 1, W, Ce);
+    __threadfence();  // this lane's partial stores, before the arrival below
+    __syncwarp();
+    unsigned int last = 0;
+    if (lane == 0) last = atomicAdd(&counters[(int64_t)sp * NH + warp], 1u) == (unsigned int)(c1 - c0);
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    __threadfence();  // every other piece is published: read them
+    const int32_t kvh = g * NH + warp;
+    merge_pieces<T, D>(out + ((int64_t)seq * H + (int64_t)kvh * G) * D, ml_ws, acc_ws, c0, c1, sp, NH * G,
+                       warp * G, G, lane);
 }
 
 // ------------------------------------------------------- CUDA-core kernel
@@ -159,14 +196,16 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(
     const T *__restrict__ v_cache, const int32_t *__restrict__ tables, int32_t max_blocks,
     const int32_t *__restrict__ lens, const int32_t *__restrict__ cu, int32_t N, int32_t H,
     int32_t Hk, int32_t G, int32_t B, int32_t NB, int32_t NH, float scale_log2, int32_t C,
-    float2 *__restrict__ ml_ws, float *__restrict__ acc_ws, unsigned int *__restrict__ err) {
+    float2 *__restrict__ ml_ws, float *__restrict__ acc_ws, unsigned int *__restrict__ counters,
+    unsigned int *__restrict__ err) {
     constexpr int VPL = D / 32;
     const int32_t NG = Hk / NH;
     const int32_t HPG = NH * G;
     const int64_t W = (int64_t)NG * cu[N];
+    const int32_t Ce = (int32_t)(W < (int64_t)C ? W : (int64_t)C);  // no CTA with an empty range
     const int32_t c = blockIdx.x;
-    const int64_t lo = split_begin(c, W, C), hi = split_begin(c + 1, W, C);
-    if (lo >= hi) return;
+    if (c >= Ce) return;
+    const int64_t lo = split_begin(c, W, Ce), hi = split_begin(c + 1, W, Ce);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     BlockCursor cur;
@@ -250,6 +289,8 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(
                     for (int j = 0; j < VPL; ++j) ap[j] = acc[h][j];
                     if (lane == 0) ml_ws[hh] = make_float2(m[h], l[h]);
                 }
+                finish_piece<T, D>(out, ml_ws, acc_ws, counters, cu, N, H, G, NH, warp, cur.g, cur.seq, cur.nb, W,
+                                   Ce, lane);
             }
             seg_start = true;
         }
@@ -279,7 +320,7 @@ __global__ void __launch_bounds__(288, 1) decode_mma_kernel(
     const int32_t *__restrict__ tables, int32_t max_blocks, const int32_t *__restrict__ lens,
     const int32_t *__restrict__ cu, int32_t N, int32_t H, int32_t Hk, int32_t G, int32_t NB,
     int32_t NH, float scale_log2, int32_t C, float2 *__restrict__ ml_ws, float *__restrict__ acc_ws,
-    unsigned int *__restrict__ err) {
+    unsigned int *__restrict__ counters, unsigned int *__restrict__ err) {
     using Tile = MmaTile<D, B>;
     constexpr int S = Tile::kStages;
     constexpr int KT = D / 16;  // k-steps of q.k and m-tiles of O^T
@@ -293,9 +334,10 @@ __global__ void __launch_bounds__(288, 1) decode_mma_kernel(
 
     const int32_t NG = Hk / NH;
     const int64_t W = (int64_t)NG * cu[N];
+    const int32_t Ce = (int32_t)(W < (int64_t)C ? W : (int64_t)C);  // no CTA with an empty range
     const int32_t c = blockIdx.x;
-    const int64_t lo = split_begin(c, W, C), hi = split_begin(c + 1, W, C);
-    if (lo >= hi) return;
+    if (c >= Ce) return;
+    const int64_t lo = split_begin(c, W, Ce), hi = split_begin(c + 1, W, Ce);
     const int64_t n = hi - lo;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -503,6 +545,8 @@ __global__ void __launch_bounds__(288, 1) decode_mma_kernel(
                     if (h0 < G) ml_ws[slot * HPG + warp * G + h0] = make_float2(m0, lt0);
                     if (h1 < G) ml_ws[slot * HPG + warp * G + h1] = make_float2(m1, lt1);
                 }
+                finish_piece<__nv_bfloat16, D>(out, ml_ws, acc_ws, counters, cu, N, H, G, NH, warp, cur.g,
+                                               cur.seq, cur.nb, W, Ce, lane);
             }
             seg_start = true;
         }
@@ -521,7 +565,7 @@ struct DecodePlan {
     int C;         // persistent CTAs
     size_t smem;   // dynamic shared memory of the attention kernel
     // workspace layout (byte offsets)
-    size_t off_lens, off_cu, off_ml, off_acc, total;
+    size_t off_lens, off_cu, off_cnt, off_ml, off_acc, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -640,6 +684,8 @@ pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_d
     off = align256(off + sizeof(int32_t) * (size_t)std::max(N, 1));
     p->off_cu = off;
     off = align256(off + sizeof(int32_t) * ((size_t)N + 1));
+    p->off_cnt = off;
+    off = align256(off + sizeof(uint32_t) * (size_t)std::max(N, 1) * c->num_kv_heads);
     p->off_ml = off;
     off = align256(off + sizeof(float2) * slots * p->HPG);
     p->off_acc = off;
@@ -735,6 +781,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
     uint8_t *ws = (uint8_t *)workspace;
     int32_t *lens_ws = (int32_t *)(ws + p.off_lens);
     int32_t *cu = (int32_t *)(ws + p.off_cu);
+    unsigned int *cnt = (unsigned int *)(ws + p.off_cnt);
     float2 *ml = (float2 *)(ws + p.off_ml);
     float *acc = (float *)(ws + p.off_acc);
     const int G = num_heads / cache->num_kv_heads;
@@ -743,7 +790,14 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
     cudaStream_t s = (cudaStream_t)stream;
     cudaGetLastError();  // clear a stale launch error so the checks below are ours
 
-    decode_plan_kernel<<<1, 1024, 0, s>>>(seq_lens, num_seqs, cache->block_size, max_len, lens_ws, cu, err);
+    const int32_t HD = num_heads * cache->head_dim;
+    const int32_t ncnt = num_seqs * cache->num_kv_heads;
+    if (cache->dtype == PA_BF16)
+        decode_plan_kernel<__nv_bfloat16><<<1, 1024, 0, s>>>(seq_lens, num_seqs, cache->block_size, max_len, HD,
+                                                             lens_ws, cu, cnt, ncnt, (__nv_bfloat16 *)out, err);
+    else
+        decode_plan_kernel<float><<<1, 1024, 0, s>>>(seq_lens, num_seqs, cache->block_size, max_len, HD, lens_ws,
+                                                     cu, cnt, ncnt, (float *)out, err);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
 
     if (opts && opts->ev_partial_begin && cudaEventRecord((cudaEvent_t)opts->ev_partial_begin, s) != cudaSuccess)
@@ -763,7 +817,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         int32_t Nv = num_seqs, Hv = num_heads, Gv = G, mb = max_blocks_per_seq;
         float sl = scale_log2;
         void *args[] = {&tmk, &tmv, &qb, &ob, &block_tables, &mb, &lens_ws, &cu, &Nv, &Hv, &Hk, &Gv,
-                        &NB, &NHv, &sl, &Cv, &ml, &acc, &err};
+                        &NB, &NHv, &sl, &Cv, &ml, &acc, &cnt, &err};
         if (cudaLaunchKernel(fn, grid, block, args, p.smem, s) != cudaSuccess) return PA_ERR_CUDA;
     } else {
         const void *fn = simt_kernel_ptr(cache->dtype, cache->head_dim, G);
@@ -773,18 +827,11 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         int32_t Nv = num_seqs, Hv = num_heads, Gv = G, mb = max_blocks_per_seq, Bv = cache->block_size;
         float sl = scale_log2;
         void *args[] = {&q, &out, &k_cache, &v_cache, &block_tables, &mb, &lens_ws, &cu, &Nv, &Hv, &Hk,
-                        &Gv, &Bv, &NB, &NHv, &sl, &Cv, &ml, &acc, &err};
+                        &Gv, &Bv, &NB, &NHv, &sl, &Cv, &ml, &acc, &cnt, &err};
         if (cudaLaunchKernel(fn, grid, block, args, 0, s) != cudaSuccess) return PA_ERR_CUDA;
     }
     if (opts && opts->ev_partial_end && cudaEventRecord((cudaEvent_t)opts->ev_partial_end, s) != cudaSuccess)
         return PA_ERR_CUDA;
 
-    const dim3 rgrid((unsigned)(p.NG * num_seqs)), rblock(128);
-    if (cache->dtype == PA_BF16)
-        decode_reduce_kernel<__nv_bfloat16><<<rgrid, rblock, 0, s>>>((__nv_bfloat16 *)out, ml, acc, cu, num_seqs,
-                                                                     num_heads, cache->head_dim, p.NG, p.HPG, p.C);
-    else
-        decode_reduce_kernel<float><<<rgrid, rblock, 0, s>>>((float *)out, ml, acc, cu, num_seqs, num_heads,
-                                                             cache->head_dim, p.NG, p.HPG, p.C);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -91,11 +91,11 @@ def test_workspace_size_follows_the_split_count(lib):
         o = _lib.DecodeOpts(c, _lib.PA_KERNEL_MMA, None, None)
         sizes.append(lib.pa_decode_workspace_bytes(ctypes.byref(d), 256, 32, ctypes.byref(o)))
     assert sizes[0] < sizes[1] < sizes[2]
-    # (C + NG*N) slots x 32 heads x (128 + 2) floats, plus lengths and prefix sums
+    # (C + NG*N) slots x 32 heads x (128 + 2) floats, plus lengths, prefix sums, counters
     o = _lib.DecodeOpts(152, _lib.PA_KERNEL_MMA, None, None)
     n = lib.pa_decode_workspace_bytes(ctypes.byref(d), 256, 32, ctypes.byref(o))
     slots = 152 + 256
-    assert n >= slots * 32 * 130 * 4 and n < slots * 32 * 130 * 4 + 8192
+    assert n >= slots * 32 * 130 * 4 and n < slots * 32 * 130 * 4 + 4 * (256 + 257 + 256 * 8) + 1024
 
 
 def test_split_covers_every_block_once(lib):
@@ -132,3 +132,25 @@ def test_partial_slots_are_unique():
         slots = [c + s for c, s in seen]
         assert len(slots) == len(set(slots))
         assert max(slots) < C + len(nb)
+
+
+def test_reduce_visits_exactly_the_ctas_holding_a_piece():
+    # The reduce walks CTAs split_owner(first block) .. split_owner(last block)
+    # and skips empty ranges; that set must equal the owners of the blocks,
+    # also when there are more CTAs than blocks.
+    rng = np.random.default_rng(2)
+    for _ in range(200):
+        nb = rng.integers(0, 6, size=int(rng.integers(1, 12)))
+        W = int(nb.sum())
+        if W == 0:
+            continue
+        C = int(rng.integers(1, 60))
+        cu = np.concatenate([[0], np.cumsum(nb)])
+        for i in range(len(nb)):
+            if nb[i] == 0:
+                continue
+            c0 = pa.pa_split_owner(W, C, int(cu[i]))
+            c1 = pa.pa_split_owner(W, C, int(cu[i + 1] - 1))
+            visited = {c for c in range(c0, c1 + 1) if pa.pa_split_range(W, C, c)[0] < pa.pa_split_range(W, C, c)[1]}
+            owners = {pa.pa_split_owner(W, C, x) for x in range(int(cu[i]), int(cu[i + 1]))}
+            assert visited == owners
