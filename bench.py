@@ -50,6 +50,9 @@ def parse():
                     help="headline workload: cfg4-b16 (default), cfg4-b32, cfg2, cfg1, cfg3-p2000, cfg3-p2008")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--l2", choices=["none", "write"], default="none",
+                    help="between timed steps: nothing (every workload's KV is several times the 129 MB L2) "
+                         "or write a 512 MiB buffer (leaves dirty lines whose write-back the next step pays)")
     return ap.parse_args()
 
 
@@ -234,33 +237,53 @@ class Step:
                      workspace=self.workspace, events=events)
 
 
-def time_steps(step, steps, warmup, world, flush, sampler=None):
+def _events(n):
+    import torch
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in ev:  # create the CUDA events outside any timed region
+        a.record()
+        b.record()
+    return ev
+
+
+def time_steps(step, steps, warmup, world, flush, sampler=None, kernel_steps=None):
+    """Per-step device time of whole steps (events around each step, L2 flushed
+    before each), then, in a second loop, the attention kernel's own duration
+    (events the library records around that kernel on the launching stream)."""
     import torch
 
     for _ in range(warmup):
-        flush.zero_()
+        if flush.numel():
+            flush.zero_()
         step.run()
     torch.cuda.synchronize()
     step.pa.pa_get_device_error()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for pair in ev + kev:  # create the CUDA events outside the timed region
-        pair[0].record()
-        pair[1].record()
+    ev = _events(steps)
     barrier(world)
     torch.cuda.synchronize()
     if sampler:
         sampler.start()
     for i in range(steps):
-        flush.zero_()
+        if flush.numel():
+            flush.zero_()
         ev[i][0].record()
-        step.run(events=kev[i])
+        step.run()
         ev[i][1].record()
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop() if sampler else None
     step.pa.pa_get_device_error()
     step_ms = [a.elapsed_time(b) for a, b in ev]
+    nk = min(steps, kernel_steps or steps)
+    kev = _events(nk)
+    torch.cuda.synchronize()
+    for i in range(nk):
+        if flush.numel():
+            flush.zero_()
+        step.run(events=kev[i])
+    torch.cuda.synchronize()
+    step.pa.pa_get_device_error()
     kern_ms = [a.elapsed_time(b) for a, b in kev]
     return step_ms, kern_ms, clocks
 
@@ -341,13 +364,13 @@ def run_ours(args, rank, world):
     import torch
 
     peak, peak_kind = measured_peaks()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = torch.empty(FLUSH_BYTES if args.l2 == "write" else 0, dtype=torch.uint8, device="cuda")
     step = Step(*WORKLOADS[args.workload], seed_offset=1000 * rank)
     do_cpu = rank == 0 and world == 1 and not args.no_cpu
     if do_cpu:
         step.keep_initial_host_copy()
     sampler = ClockSampler(torch.cuda.current_device())
-    step_ms, kern_ms, clocks = time_steps(step, args.steps, args.warmup, world, flush, sampler)
+    step_ms, kern_ms, clocks = time_steps(step, args.steps, args.warmup, world, flush, sampler, kernel_steps=1000)
     total_ms = reduce_max(sum(step_ms), world)
     ms_per_step = total_ms / args.steps
     value = world * step.kv_bytes * args.steps / (total_ms / 1e3) / 1e9
@@ -357,10 +380,11 @@ def run_ours(args, rank, world):
     traffic, _ = profiled_traffic(workload_name(step))
 
     if args.no_e2e:
-        e2e_s, h2d, d2h = float("nan"), 0, 0
+        e2e = None
     else:
         e2e_s, h2d, d2h = time_e2e(step, args.e2e_steps)
-    e2e_value = world * step.kv_bytes / e2e_s / 1e9
+        e2e = {"value": round(world * step.kv_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -369,7 +393,8 @@ def run_ours(args, rank, world):
         "config": {"workload": describe(step.wl),
                    "kv_bytes_per_step": step.kv_bytes, "num_seqs": step.wl.num_seqs,
                    "max_seq_len": int(step.wl.seq_lens.max()), "block_size": step.wl.block_size,
-                   "l2": "512 MiB buffer written between timed steps",
+                   "l2": ("inputs larger than L2: %.2f GB of KV per step vs 129 MB L2, no flush" % (step.kv_bytes / 1e9)
+                          if args.l2 == "none" else "512 MiB buffer written between timed steps"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tokens_per_s": round(tokens_per_s, 1),
         "hbm_frac": round(value / world / peak, 4),
@@ -378,8 +403,7 @@ def run_ours(args, rank, world):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": step.kernel_bytes,
                      "avg_launch_ms": round(kern_avg_ms, 5), "peak_source": peak_kind},
-        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
+        "e2e": e2e,
         "gpu_launches": step.kernel_launches * args.steps,
         "clocks": clocks,
         "block_manager_ms": round(step.bm_ms, 3),
@@ -403,7 +427,7 @@ def run_ours(args, rank, world):
             if WORKLOADS[args.workload] == (cfg, kw):
                 continue
             st = Step(cfg, kw, seed_offset=1000 * rank)
-            sm, km, _ = time_steps(st, args.extra_steps, args.warmup, world, flush)
+            sm, km, _ = time_steps(st, args.extra_steps, args.warmup, world, flush, kernel_steps=args.extra_steps)
             mean_ms = reduce_max(statistics.mean(sm), world)
             kms = statistics.mean(km)
             extra[st.wl.name] = {"kv_gbs": round(st.kv_bytes / (mean_ms / 1e3) / 1e9, 2),

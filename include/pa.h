@@ -185,6 +185,17 @@ int32_t pa_split_owner(int64_t total_blocks, int32_t num_splits, int64_t x);
 pa_status_t pa_get_device_error(pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * pa_selftest_wait_timeout - check of the kernels' bounded waits.  Launches
+ * one thread that waits on a shared-memory mbarrier that nothing arrives at,
+ * through the same bounded-wait routine the attention kernel uses, with a
+ * limit of limit_ns nanoseconds (0 < limit_ns <= 2e9).  The wait runs out, the
+ * kernel records a timeout in the error word and returns; the context stays
+ * usable, and the next pa_get_device_error returns PA_ERR_DEVICE_TIMEOUT.
+ * (Library self-test; the pages have no counterpart.)
+ * ---------------------------------------------------------------------- */
+pa_status_t pa_selftest_wait_timeout(int64_t limit_ns, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Host block manager (all host memory; not thread-safe per handle).
  *
  * A stack of free block ids, a refcount per block and a block table per

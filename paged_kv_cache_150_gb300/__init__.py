@@ -165,6 +165,11 @@ def pa_get_device_error(raise_on_error=True):
     return st
 
 
+def pa_selftest_wait_timeout(limit_ns):
+    """Launch the bounded-wait self-test kernel (its wait runs out by design)."""
+    _lib.check("pa_selftest_wait_timeout", _lib.load().pa_selftest_wait_timeout(int(limit_ns), _stream()))
+
+
 def pa_split_range(total_blocks, num_splits, c):
     b, e = ctypes.c_int64(), ctypes.c_int64()
     _lib.load().pa_split_range(int(total_blocks), int(num_splits), int(c), ctypes.byref(b), ctypes.byref(e))
@@ -298,6 +303,7 @@ def version():
 
 __all__ = [
     "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_workspace_bytes",
-    "pa_decode_default_splits", "pa_get_device_error", "pa_split_range", "pa_split_owner",
+    "pa_decode_default_splits", "pa_get_device_error", "pa_selftest_wait_timeout", "pa_split_range",
+    "pa_split_owner",
     "BlockManager", "PagedAttentionError", "version",
 ]

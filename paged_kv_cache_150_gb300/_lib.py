@@ -57,6 +57,7 @@ SIGNATURES = {
     "pa_split_range": (None, [_I64, _I32, _I32, _PI64, _PI64]),
     "pa_split_owner": (_I32, [_I64, _I32, _I64]),
     "pa_get_device_error": (_I32, [_P]),
+    "pa_selftest_wait_timeout": (_I32, [_I64, _P]),
     "pa_bm_create": (_P, [_I32, _I32, _PI32]),
     "pa_bm_destroy": (None, [_P]),
     "pa_bm_new_seq": (_I32, [_P, _I32, _PI32]),

@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     const V *__restrict__ k, const V *__restrict__ v, const int32_t *__restrict__ slots,
     int32_t num_tokens, V *__restrict__ k_cache, V *__restrict__ v_cache, int64_t num_slots,
     int32_t row_vecs, unsigned int *__restrict__ err) {
+    grid_launch_dependents();  // a programmatically launched successor may get resident early
     const int64_t total = (int64_t)num_tokens * row_vecs;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
@@ -42,6 +43,7 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(V *__restrict__ k_cach
                                                           int32_t num_pairs, int32_t num_blocks,
                                                           int64_t block_vecs, int32_t chunks_per_pair,
                                                           unsigned int *__restrict__ err) {
+    grid_launch_dependents();  // a programmatically launched successor may get resident early
     const int32_t p = blockIdx.x / chunks_per_pair;
     const int32_t chunk = blockIdx.x - p * chunks_per_pair;
     if (p >= num_pairs) return;

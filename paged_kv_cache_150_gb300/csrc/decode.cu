@@ -46,6 +46,8 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
                                                            unsigned int *__restrict__ counters,
                                                            int32_t num_counters, T *__restrict__ out,
                                                            unsigned int *__restrict__ err) {
+    grid_dependency_wait();     // inputs written by earlier work on the stream
+    grid_launch_dependents();   // the attention kernel may become resident now
     __shared__ int32_t warp_incl[32];
     __shared__ int32_t carry;
     __shared__ int32_t n_empty;
@@ -199,6 +201,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(
     float2 *__restrict__ ml_ws, float *__restrict__ acc_ws, unsigned int *__restrict__ counters,
     unsigned int *__restrict__ err) {
     constexpr int VPL = D / 32;
+    grid_dependency_wait();  // the plan kernel's cu[] / lens (programmatic launch)
     const int32_t NG = Hk / NH;
     const int32_t HPG = NH * G;
     const int64_t W = (int64_t)NG * cu[N];
@@ -212,10 +215,11 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(
     cur.init(lo, cu, N);
     float qv[GMAX][VPL], acc[GMAX][VPL], m[GMAX], l[GMAX];
     bool seg_start = true, seg_from_first = false;
+    int32_t L = 0;
     for (int64_t x = lo; x < hi; ++x) {
         const int32_t kvh = cur.g * NH + warp;
-        const int32_t L = lens[cur.seq];
         if (seg_start) {
+            L = lens[cur.seq];
             const T *qp = q + ((int64_t)cur.seq * H + (int64_t)kvh * G) * D + lane * VPL;
 #pragma unroll
             for (int h = 0; h < GMAX; ++h) {
@@ -332,6 +336,7 @@ __global__ void __launch_bounds__(288, 1) decode_mma_kernel(
     uint64_t *full = (uint64_t *)(smem + S * stage_bytes);
     uint64_t *empty = full + S;
 
+    grid_dependency_wait();  // the plan kernel's cu[] / lens (programmatic launch)
     const int32_t NG = Hk / NH;
     const int64_t W = (int64_t)NG * cu[N];
     const int32_t Ce = (int32_t)(W < (int64_t)C ? W : (int64_t)C);  // no CTA with an empty range
@@ -356,17 +361,34 @@ __global__ void __launch_bounds__(288, 1) decode_mma_kernel(
         if (lane == 0) {
             prefetch_tmap(&tmk);
             prefetch_tmap(&tmv);
-            BlockCursor cur;
+            BlockCursor cur, ahead;
             cur.init(lo, cu, N);
+            ahead.init(lo, cu, N);
+            // Block-table entries are loaded kTablePrefetch blocks ahead of their
+            // TMA issue (a register shift ring), so the L2 latency of the table
+            // read is off the issue path.
+            constexpr int PD = kTablePrefetch;
+            int32_t ring[PD];
+#pragma unroll
+            for (int j = 0; j < PD; ++j) {
+                ring[j] = (j < n) ? tables[(int64_t)ahead.seq * max_blocks + ahead.blk] : 0;
+                if (j < n) ahead.advance(cu, N);
+            }
             int64_t issued = 0;
             for (; issued < n; ++issued) {
                 const int s = (int)(issued % S);
                 const uint32_t ph = (uint32_t)((issued / S) & 1);
+                int32_t phys = ring[0];
+#pragma unroll
+                for (int j = 0; j + 1 < PD; ++j) ring[j] = ring[j + 1];
+                if (issued + PD < n) {
+                    ring[PD - 1] = tables[(int64_t)ahead.seq * max_blocks + ahead.blk];
+                    ahead.advance(cu, N);
+                }
                 if (issued >= S && !mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u)) {
                     atomicOr(err, kErrTimeout);
                     break;
                 }
-                int32_t phys = tables[(int64_t)cur.seq * max_blocks + cur.blk];
                 if (phys < 0 || phys >= NB) {  // read zeros: the box lies past the pool
                     atomicOr(err, kErrBounds);
                     phys = NB;
@@ -395,12 +417,13 @@ __global__ void __launch_bounds__(288, 1) decode_mma_kernel(
     cur.init(lo, cu, N);
     bool seg_start = true, seg_from_first = false;
 
+    int32_t L = 0;
     for (int64_t it = 0; it < n; ++it) {
         const int s = (int)(it % S);
         const uint32_t ph = (uint32_t)((it / S) & 1);
         const int32_t kvh = cur.g * NH + warp;
-        const int32_t L = lens[cur.seq];
         if (seg_start) {
+            L = lens[cur.seq];
             // B operand of S^T = K Q^T: column n = query head r of this KV head.
             const bool hv = r < G;
             const __nv_bfloat16 *qp = q + ((int64_t)cur.seq * H + (int64_t)kvh * G + (hv ? r : 0)) * D;
@@ -694,6 +717,23 @@ pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_d
     return PA_OK;
 }
 
+// Launch with programmatic stream serialization: the grid may be scheduled
+// while the previous kernel on the stream finishes; the kernel itself calls
+// griddepcontrol.wait before touching anything that kernel produced.
+cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, void **args, size_t smem, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -792,13 +832,14 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
 
     const int32_t HD = num_heads * cache->head_dim;
     const int32_t ncnt = num_seqs * cache->num_kv_heads;
-    if (cache->dtype == PA_BF16)
-        decode_plan_kernel<__nv_bfloat16><<<1, 1024, 0, s>>>(seq_lens, num_seqs, cache->block_size, max_len, HD,
-                                                             lens_ws, cu, cnt, ncnt, (__nv_bfloat16 *)out, err);
-    else
-        decode_plan_kernel<float><<<1, 1024, 0, s>>>(seq_lens, num_seqs, cache->block_size, max_len, HD, lens_ws,
-                                                     cu, cnt, ncnt, (float *)out, err);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    {
+        int32_t Nv = num_seqs, Bv = cache->block_size, ml_v = max_len, HDv = HD, nc = ncnt;
+        void *outp = out;
+        void *pargs[] = {&seq_lens, &Nv, &Bv, &ml_v, &HDv, &lens_ws, &cu, &cnt, &nc, &outp, &err};
+        const void *pfn = cache->dtype == PA_BF16 ? (const void *)decode_plan_kernel<__nv_bfloat16>
+                                                  : (const void *)decode_plan_kernel<float>;
+        if (launch_pdl(pfn, dim3(1), dim3(1024), pargs, 0, s) != cudaSuccess) return PA_ERR_CUDA;
+    }
 
     if (opts && opts->ev_partial_begin && cudaEventRecord((cudaEvent_t)opts->ev_partial_begin, s) != cudaSuccess)
         return PA_ERR_CUDA;
@@ -818,7 +859,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         float sl = scale_log2;
         void *args[] = {&tmk, &tmv, &qb, &ob, &block_tables, &mb, &lens_ws, &cu, &Nv, &Hv, &Hk, &Gv,
                         &NB, &NHv, &sl, &Cv, &ml, &acc, &cnt, &err};
-        if (cudaLaunchKernel(fn, grid, block, args, p.smem, s) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_pdl(fn, grid, block, args, p.smem, s) != cudaSuccess) return PA_ERR_CUDA;
     } else {
         const void *fn = simt_kernel_ptr(cache->dtype, cache->head_dim, G);
         if (!fn) return PA_ERR_UNSUPPORTED;
@@ -828,7 +869,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         float sl = scale_log2;
         void *args[] = {&q, &out, &k_cache, &v_cache, &block_tables, &mb, &lens_ws, &cu, &Nv, &Hv, &Hk,
                         &Gv, &Bv, &NB, &NHv, &sl, &Cv, &ml, &acc, &cnt, &err};
-        if (cudaLaunchKernel(fn, grid, block, args, 0, s) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_pdl(fn, grid, block, args, 0, s) != cudaSuccess) return PA_ERR_CUDA;
     }
     if (opts && opts->ev_partial_end && cudaEventRecord((cudaEvent_t)opts->ev_partial_end, s) != cudaSuccess)
         return PA_ERR_CUDA;

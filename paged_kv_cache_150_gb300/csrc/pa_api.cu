@@ -9,6 +9,17 @@ namespace pa {
 
 __device__ unsigned int g_error_word;
 
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// arrives at, with the same helper the attention kernel uses, and records a
+// timeout in the error word when the limit runs out.
+__global__ void selftest_wait_kernel(unsigned long long limit_ns, unsigned int *err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbarrier_init();
+    if (!mbar_wait_bounded(smem_u32(&bar), 0, limit_ns)) atomicOr(err, kErrTimeout);
+}
+
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -72,4 +83,12 @@ extern "C" pa_status_t pa_get_device_error(pa_stream_t stream) {
     if (word & kErrTimeout) return PA_ERR_DEVICE_TIMEOUT;
     if (word & (kErrBounds | kErrLength)) return PA_ERR_DEVICE_BOUNDS;
     return PA_OK;
+}
+
+extern "C" pa_status_t pa_selftest_wait_timeout(int64_t limit_ns, pa_stream_t stream) {
+    if (limit_ns <= 0 || limit_ns > (int64_t)kWaitLimitNs) return PA_ERR_INVALID_ARG;
+    unsigned int *err = device_error_word();
+    if (!err) return PA_ERR_CUDA;
+    selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((unsigned long long)limit_ns, err);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -23,6 +23,9 @@ enum : unsigned int {
 // Bound on any single mbarrier wait (nanoseconds of %globaltimer).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
+// Block-table entries the TMA producer reads ahead of their use.
+constexpr int kTablePrefetch = 4;
+
 // ---------------------------------------------------------------- work split
 // CTA c of C owns flattened blocks [split_begin(c), split_begin(c + 1)).
 __host__ __device__ __forceinline__ int64_t split_begin(int64_t c, int64_t W, int64_t C) {
@@ -60,6 +63,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ------------------------------------------- programmatic dependent launch
+// Wait until the preceding grid on the stream has completed and its memory
+// is visible (a no-op when this grid was not launched programmatically).
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allow the next grid on the stream (if launched programmatically) to start.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ mbarrier
@@ -100,15 +114,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for phase `parity` of the barrier to complete, giving up after
-// kWaitLimitNs.  Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// limit_ns nanoseconds of %globaltimer.  Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 

@@ -160,3 +160,18 @@ def test_bad_table_entry_and_length_are_reported_without_a_fault(kernel):
     assert (out[1] == 0).all()  # an out-of-range length counts as 0
     pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale, kernel=kernel)
     assert pa.pa_get_device_error(raise_on_error=False) == 0
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable():
+    import time
+
+    t0 = time.perf_counter()
+    pa.pa_selftest_wait_timeout(20_000_000)  # 20 ms; nothing ever arrives
+    assert pa.pa_get_device_error(raise_on_error=False) == pa._lib.PA_ERR_DEVICE_TIMEOUT
+    assert time.perf_counter() - t0 < 5.0
+    assert pa.pa_get_device_error(raise_on_error=False) == 0
+    wl = inputs.workload("cfg0")
+    dev, host = host_values(wl, "cpu")
+    r = oracle_step(wl, host)
+    g = gpu_step(wl, dev)
+    assert max_abs_err(g["out"], oracle_decode(wl, host, r)) <= TOL["f32"]
