@@ -165,6 +165,41 @@ pa_status_t pa_decode(void *out, const void *q, const void *k_cache, const void 
                       int32_t num_heads, float scale, void *workspace, size_t workspace_bytes,
                       const pa_decode_opts_t *opts, pa_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * pa_decode_no_alloc - pa_decode for callers that cannot allocate device
+ * memory.  (The pages have no counterpart; this is a library convenience.)
+ *
+ * Some callers have no way to hand pa_decode a workspace: a serving process
+ * that reserved nearly all device memory for its KV pool at startup has none
+ * left for per-call scratch, a plugin that runs inside a host framework may
+ * be forbidden to call cudaMalloc because the framework owns the allocator,
+ * and a latency-critical loop cannot afford the device-wide synchronisation
+ * that cudaMalloc/cudaFree can imply.  This call takes the same arguments as
+ * pa_decode minus the workspace and allocates nothing: its scratch is a
+ * fixed array of PA_NO_ALLOC_SCRATCH_BYTES bytes compiled into the library,
+ * one copy per GPU that loads it, held until the process exits.
+ *
+ * - The first call on a device looks up that array's device address (once,
+ *   with that device current) and caches it; make this first call before
+ *   any stream capture.
+ * - A shape whose workspace (pa_decode_workspace_bytes with the same
+ *   options) exceeds PA_NO_ALLOC_SCRATCH_BYTES returns PA_ERR_WORKSPACE and
+ *   launches nothing.
+ * - Every call on a device shares the one array, and the array keeps the
+ *   last call's contents; each call zeroes what it needs zeroed (its arrival
+ *   counters) before use.  Calls that can overlap on the GPU (for example
+ *   on two streams with no ordering between them) race on the array: order
+ *   them on one stream.
+ * - No cudaMalloc, cudaFree or allocating library routine is called.
+ * ---------------------------------------------------------------------- */
+#define PA_NO_ALLOC_SCRATCH_BYTES (16u << 20)
+
+pa_status_t pa_decode_no_alloc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                               const pa_cache_desc_t *cache, const int32_t *block_tables,
+                               int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
+                               int32_t num_heads, float scale, const pa_decode_opts_t *opts,
+                               pa_stream_t stream);
+
 /* Number of CTAs a default (num_splits = 0) decode launch uses on the current
  * device for this shape, or a negative pa_status_t. */
 int32_t pa_decode_default_splits(const pa_cache_desc_t *cache, int32_t num_heads,

@@ -157,6 +157,32 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None, work
     return out
 
 
+def pa_decode_no_alloc(q, k_cache, v_cache, block_tables, seq_lens, scale, out, num_splits=0, kernel="auto"):
+    """pa_decode without a workspace argument, for callers that cannot allocate
+    device memory (a pool that took all free memory at startup, a framework
+    that owns the allocator, a loop that cannot afford cudaMalloc's implicit
+    synchronisation).  Its scratch is a fixed array of
+    PA_NO_ALLOC_SCRATCH_BYTES inside the library, shared by every call on a
+    device; calls that can overlap on the GPU race on it.  ``out`` is
+    required: this path allocates nothing."""
+    torch = _torch()
+    desc = _cache_desc(k_cache, v_cache)
+    N, H, D = q.shape
+    if D != k_cache.shape[3] or q.dtype != k_cache.dtype:
+        raise ValueError("q must be [num_seqs, num_heads, head_dim] in the cache's element type")
+    if block_tables.dim() != 2 or block_tables.shape[0] != N or seq_lens.shape != (N,):
+        raise ValueError("block_tables must be [num_seqs, max_blocks] and seq_lens [num_seqs]")
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must match q")
+    o = _opts(num_splits, kernel, None)
+    st = _lib.load().pa_decode_no_alloc(
+        _dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(desc),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(seq_lens, "seq_lens", torch.int32), N, H, float(scale), ctypes.byref(o), _stream())
+    _lib.check("pa_decode_no_alloc", st)
+    return out
+
+
 def pa_get_device_error(raise_on_error=True):
     """Synchronise the current stream and read/clear the device error word."""
     st = _lib.load().pa_get_device_error(_stream())
@@ -302,7 +328,7 @@ def version():
 
 
 __all__ = [
-    "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_workspace_bytes",
+    "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_workspace_bytes", "pa_decode_no_alloc",
     "pa_decode_default_splits", "pa_get_device_error", "pa_selftest_wait_timeout", "pa_split_range",
     "pa_split_owner",
     "BlockManager", "PagedAttentionError", "version",

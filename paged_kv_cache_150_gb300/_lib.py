@@ -20,6 +20,8 @@ PA_ERR_WORKSPACE = -7
 PA_F32 = 0
 PA_BF16 = 1
 
+PA_NO_ALLOC_SCRATCH_BYTES = 16 << 20  # include/pa.h
+
 PA_KERNEL_AUTO = 0
 PA_KERNEL_SIMT = 1
 PA_KERNEL_MMA = 2
@@ -54,6 +56,7 @@ SIGNATURES = {
     "pa_decode": (_I32, [_P, _P, _P, _P, _DESC, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P,
                          ctypes.c_size_t, _OPTS, _P]),
     "pa_decode_default_splits": (_I32, [_DESC, _I32, _OPTS]),
+    "pa_decode_no_alloc": (_I32, [_P, _P, _P, _P, _DESC, _P, _I32, _P, _I32, _I32, ctypes.c_float, _OPTS, _P]),
     "pa_split_range": (None, [_I64, _I32, _I32, _PI64, _PI64]),
     "pa_split_owner": (_I32, [_I64, _I32, _I64]),
     "pa_get_device_error": (_I32, [_P]),

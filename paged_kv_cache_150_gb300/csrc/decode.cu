@@ -876,3 +876,45 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
 
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
+
+// ------------------------------------------------------------ no-alloc entry
+// Scratch of pa_decode_no_alloc: a fixed array in the library's device image
+// (one per GPU that loads the library, alive until exit).  Host code must not
+// pass `g_decode_scratch` itself to a kernel: on the host that name is only a
+// stand-in, so its device address is looked up per device below.
+static __device__ __align__(256) unsigned char g_decode_scratch[PA_NO_ALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_scratch_mu;
+void *g_scratch_addr[64];
+
+// Device address of g_decode_scratch on the current device, looked up on the
+// first call per device (with that device current) and cached; nullptr on
+// failure.
+void *no_alloc_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || !ptr) return nullptr;
+        g_scratch_addr[dev] = ptr;
+    }
+    return g_scratch_addr[dev];
+}
+}  // namespace
+
+extern "C" pa_status_t pa_decode_no_alloc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                          const pa_cache_desc_t *cache, const int32_t *block_tables,
+                                          int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
+                                          int32_t num_heads, float scale, const pa_decode_opts_t *opts,
+                                          pa_stream_t stream) {
+    DecodePlan p;
+    const pa_status_t st = make_plan(cache, num_seqs, num_heads, opts, true, &p);
+    if (st != PA_OK) return st;
+    if (p.total > (size_t)PA_NO_ALLOC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
+    void *scratch = no_alloc_scratch();
+    if (!scratch) return PA_ERR_CUDA;
+    return pa_decode(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                     num_heads, scale, scratch, (size_t)PA_NO_ALLOC_SCRATCH_BYTES, opts, stream);
+}

@@ -15,3 +15,11 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built_library():
+    """Compile libpa.so and the oracle if they are missing or stale (a no-op otherwise)."""
+    import __graft_entry__
+
+    __graft_entry__.build()
