@@ -410,12 +410,23 @@ __global__ void __launch_bounds__(288, 1) decode_mma_kernel(
     // ----------------------------------------------------------- consumers
     const int r = lane >> 2, cq = lane & 3;  // mma groupID / thread-in-group
     const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: matrix id / row id
-    uint32_t qf[KT][2];
+    uint32_t qf[KT][2], qn[KT][2];
     float o[KT][4];
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     BlockCursor cur;
     cur.init(lo, cu, N);
-    bool seg_start = true, seg_from_first = false;
+    bool seg_start = true, seg_from_first = false, have_next_q = false;
+    // B operand of S^T = K Q^T: column n = query head r of this KV head.
+    auto load_q = [&](uint32_t (&dst)[KT][2], int32_t seq, int32_t grp) {
+        const bool hv = r < G;
+        const __nv_bfloat16 *qp =
+            q + ((int64_t)seq * H + (int64_t)(grp * NH + warp) * G + (hv ? r : 0)) * D;
+#pragma unroll
+        for (int kk = 0; kk < KT; ++kk) {
+            dst[kk][0] = hv ? *reinterpret_cast<const uint32_t *>(qp + kk * 16 + 2 * cq) : 0u;
+            dst[kk][1] = hv ? *reinterpret_cast<const uint32_t *>(qp + kk * 16 + 8 + 2 * cq) : 0u;
+        }
+    };
 
     int32_t L = 0;
     for (int64_t it = 0; it < n; ++it) {
@@ -424,20 +435,32 @@ __global__ void __launch_bounds__(288, 1) decode_mma_kernel(
         const int32_t kvh = cur.g * NH + warp;
         if (seg_start) {
             L = lens[cur.seq];
-            // B operand of S^T = K Q^T: column n = query head r of this KV head.
-            const bool hv = r < G;
-            const __nv_bfloat16 *qp = q + ((int64_t)cur.seq * H + (int64_t)kvh * G + (hv ? r : 0)) * D;
+            if (have_next_q) {
 #pragma unroll
-            for (int kk = 0; kk < KT; ++kk) {
-                qf[kk][0] = hv ? *reinterpret_cast<const uint32_t *>(qp + kk * 16 + 2 * cq) : 0u;
-                qf[kk][1] = hv ? *reinterpret_cast<const uint32_t *>(qp + kk * 16 + 8 + 2 * cq) : 0u;
+                for (int kk = 0; kk < KT; ++kk) {
+                    qf[kk][0] = qn[kk][0];
+                    qf[kk][1] = qn[kk][1];
+                }
+            } else {
+                load_q(qf, cur.seq, cur.g);
+            }
+            have_next_q = false;
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) o[kk][e] = 0.f;
-            }
             m0 = m1 = -INFINITY;
             l0 = l1 = 0.f;
             seg_from_first = (cur.blk == 0);
             seg_start = false;
+        }
+        // Last block of this sequence with more range after it: fetch the next
+        // segment's q now, so the switch does not wait on a global load.
+        if (cur.blk == cur.nb - 1 && it + 1 < n) {
+            BlockCursor nx = cur;
+            nx.advance(cu, N);
+            load_q(qn, nx.seq, nx.g);
+            have_next_q = true;
         }
 
         const bool ok = mbar_wait_bounded(smem_u32(&full[s]), ph);
