@@ -12,7 +12,7 @@
 #include <new>
 #include <vector>
 
-#include "../../include/pa.h"
+#include "pa.h"
 
 struct pa_bm {
     int32_t num_blocks = 0;

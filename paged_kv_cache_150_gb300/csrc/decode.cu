@@ -310,7 +310,7 @@ template <int D, int B>
 struct MmaTile {
     static constexpr int kHalves = D / 64;
     static constexpr int kSlabBytes = kHalves * B * 128;  // one head
-    static constexpr int kStages = 3;
+    static constexpr int kStages = kMmaStages;
 };
 
 __device__ __forceinline__ uint32_t swz_addr(uint32_t slab, int line, int chunk) {
@@ -637,7 +637,7 @@ int simt_gmax(int G) { return G <= 1 ? 1 : (G <= 4 ? 4 : 8); }
 
 size_t mma_smem_bytes(int D, int B, int NH) {
     const size_t tile = (size_t)NH * (D / 64) * B * 128;
-    return 3 * 2 * tile + 2 * 3 * sizeof(uint64_t) + 1024;
+    return (size_t)kMmaStages * 2 * tile + 2 * kMmaStages * sizeof(uint64_t) + 1024;
 }
 
 template <typename T, int D, int GMAX>
@@ -704,8 +704,8 @@ pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_d
     }
     p->kernel = kernel;
     if (kernel == PA_KERNEL_MMA) {
-        // stage = K + V tiles of NH heads; keep a stage <= 64 KiB so 3 stages fit
-        const int cap = std::max(1, (int)(65536 / (2 * c->block_size * c->head_dim * 2)));
+        // stage = K + V tiles of NH heads, at most kMmaStageBytes
+        const int cap = std::max(1, (int)(kMmaStageBytes / (2 * c->block_size * c->head_dim * 2)));
         p->NH = largest_divisor_at_most(c->num_kv_heads, std::min(8, cap));
         p->smem = mma_smem_bytes(c->head_dim, c->block_size, p->NH);
     } else {

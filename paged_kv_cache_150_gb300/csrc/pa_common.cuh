@@ -26,6 +26,12 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 // Block-table entries the TMA producer reads ahead of their use.
 constexpr int kTablePrefetch = 4;
 
+// Tensor-core decode pipeline: stages in the shared-memory ring and the
+// largest K+V stage (one (block, head-group) tile of each) in bytes.  The
+// head-group size NH is the largest divisor of Hk (<= 8) whose stage fits.
+constexpr int kMmaStages = 3;
+constexpr int kMmaStageBytes = 65536;
+
 // ---------------------------------------------------------------- work split
 // CTA c of C owns flattened blocks [split_begin(c), split_begin(c + 1)).
 __host__ __device__ __forceinline__ int64_t split_begin(int64_t c, int64_t W, int64_t C) {

@@ -5,7 +5,7 @@
 #include <cstdint>
 #include <cstring>
 
-#include "../../include/pa.h"
+#include "pa.h"
 #include "pa_common.cuh"
 
 namespace pa {
