@@ -318,7 +318,7 @@ __device__ __forceinline__ uint32_t swz_addr(uint32_t slab, int line, int chunk)
 }
 
 template <int D, int B>
-__global__ void __launch_bounds__(288, 1) decode_mma_kernel(
+__global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
     const __nv_bfloat16 *__restrict__ q, __nv_bfloat16 *__restrict__ out,
     const int32_t *__restrict__ tables, int32_t max_blocks, const int32_t *__restrict__ lens,
@@ -704,9 +704,7 @@ pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_d
     }
     p->kernel = kernel;
     if (kernel == PA_KERNEL_MMA) {
-        // stage = K + V tiles of NH heads, at most kMmaStageBytes
-        const int cap = std::max(1, (int)(kMmaStageBytes / (2 * c->block_size * c->head_dim * 2)));
-        p->NH = largest_divisor_at_most(c->num_kv_heads, std::min(8, cap));
+        p->NH = largest_divisor_at_most(c->num_kv_heads, kMmaMaxHeads);
         p->smem = mma_smem_bytes(c->head_dim, c->block_size, p->NH);
     } else {
         p->NH = largest_divisor_at_most(c->num_kv_heads, 8);

@@ -26,11 +26,15 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 // Block-table entries the TMA producer reads ahead of their use.
 constexpr int kTablePrefetch = 4;
 
-// Tensor-core decode pipeline: stages in the shared-memory ring and the
-// largest K+V stage (one (block, head-group) tile of each) in bytes.  The
-// head-group size NH is the largest divisor of Hk (<= 8) whose stage fits.
-constexpr int kMmaStages = 3;
-constexpr int kMmaStageBytes = 65536;
+// Tensor-core decode pipeline: stages in the shared-memory ring, and the
+// most KV heads one CTA covers (NH = the largest divisor of Hk not above it).
+// A stage holds one (block, head-group) tile of K and of V: 32 KiB at
+// block_size 16 and 64 KiB at 32 for head_dim 128, so about 128 KiB is in
+// flight per SM (two CTAs per SM at block_size 16, one at 32).  Measured
+// on GB300 against 3-4 stages and 8 heads per CTA: deeper rings (192 KiB per
+// SM) were 2-3% slower on every workload.
+constexpr int kMmaStages = 2;
+constexpr int kMmaMaxHeads = 4;
 
 // ---------------------------------------------------------------- work split
 // CTA c of C owns flattened blocks [split_begin(c), split_begin(c + 1)).
