@@ -35,12 +35,12 @@ def _load():
         lib.orc_slot_mapping.restype = None
         lib.orc_slot_mapping.argtypes = [p, i32, p, p, i32, i32, p]
         lib.orc_reshape_and_cache.restype = i32
-        lib.orc_reshape_and_cache.argtypes = [p, p, p, i32, p, p, i32, i32, i32, i32, i32]
+        lib.orc_reshape_and_cache.argtypes = [p, p, p, i32, p, p, i32, i32, i32, i32, i32, i32]
         lib.orc_copy_blocks.restype = None
         lib.orc_copy_blocks.argtypes = [p, p, i64, p, i32]
         lib.orc_decode.restype = i32
         lib.orc_decode.argtypes = [p, i32, p, p, p, i32, i32, i32, i32, p, i32, p, i32, i32,
-                                   ctypes.c_double, p, i32, i32]
+                                   ctypes.c_double, p, i32, i32, i32]
         _lib = lib
     return _lib
 
@@ -51,6 +51,21 @@ def _dtype_code(arr: np.ndarray) -> int:
     if arr.dtype == np.uint16:
         return BF16
     raise TypeError("oracle element arrays are float32 or uint16 (bfloat16 bits), got %s" % arr.dtype)
+
+
+ROW = 0    # K and V [num_blocks, B, Hk, D]
+SPLIT = 1  # K [num_blocks, Hk, D/x, B, x], V [num_blocks, Hk, D, B], x = 16 / element bytes
+
+
+def cache_geometry(k_cache: np.ndarray, v_cache: np.ndarray):
+    """(layout, num_blocks, B, Hk, D) read off the cache shapes."""
+    if k_cache.ndim == 4:
+        nb, bs, hk, d = k_cache.shape
+        assert v_cache.shape == k_cache.shape
+        return ROW, nb, bs, hk, d
+    nb, hk, dx, bs, x = k_cache.shape
+    assert x * k_cache.itemsize == 16 and v_cache.shape == (nb, hk, dx * x, bs)
+    return SPLIT, nb, bs, hk, dx * x
 
 
 def _ptr(arr: np.ndarray):
@@ -86,7 +101,7 @@ def slot_mapping(tables: np.ndarray, seq_ids, positions, block_size: int) -> np.
 
 def reshape_and_cache(k: np.ndarray, v: np.ndarray, slots, k_cache: np.ndarray,
                       v_cache: np.ndarray) -> int:
-    """In-place cache write (k, v: [T, Hk, D]; caches: [NB, B, Hk, D]).
+    """In-place cache write (k, v: [T, Hk, D]; caches in either layout).
 
     Returns the number of slots that lay beyond the pool (skipped)."""
     assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
@@ -94,9 +109,9 @@ def reshape_and_cache(k: np.ndarray, v: np.ndarray, slots, k_cache: np.ndarray,
     k = _c(k, k_cache.dtype)
     v = _c(v, k_cache.dtype)
     slots = _c(slots, np.int64)
-    nb, bs, hk, d = k_cache.shape
+    layout, nb, bs, hk, d = cache_geometry(k_cache, v_cache)
     return int(_load().orc_reshape_and_cache(_ptr(k), _ptr(v), _ptr(slots), slots.shape[0],
-                                             _ptr(k_cache), _ptr(v_cache), nb, bs, hk, d, code))
+                                             _ptr(k_cache), _ptr(v_cache), nb, bs, hk, d, code, layout))
 
 
 def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, pairs) -> None:
@@ -109,7 +124,7 @@ def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, pairs) -> None:
 
 def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables: np.ndarray,
            seq_lens, scale: float, pairs=None, num_threads: int = 1) -> np.ndarray:
-    """fp64 decode attention.  q: [N, H, D]; caches [NB, B, Hk, D]; tables [N, max_blocks].
+    """fp64 decode attention.  q: [N, H, D]; caches in either layout; tables [N, max_blocks].
 
     Returns float64 [N, H, D].  With ``pairs`` (a list of (seq, head)) only those
     entries are computed; the others are left as NaN."""
@@ -120,7 +135,7 @@ def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables
     tables = _c(block_tables, np.int32)
     lens = _c(seq_lens, np.int32)
     n, h, d = q.shape
-    nb, bs, hk, d2 = k_cache.shape
+    layout, nb, bs, hk, d2 = cache_geometry(k_cache, v_cache)
     assert d == d2 and tables.shape[0] == n and lens.shape[0] == n
     out = np.full((n, h, d), np.nan, dtype=np.float64)
     if pairs is None:
@@ -132,7 +147,7 @@ def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables
     rc = _load().orc_decode(_ptr(out), code, _ptr(q), _ptr(k_cache), _ptr(v_cache), nb, bs, hk, d,
                             _ptr(tables), tables.shape[1], _ptr(lens), n, h, float(scale),
                             None if pairs_arr is None else _ptr(pairs_arr), npairs,
-                            int(num_threads))
+                            int(num_threads), layout)
     if rc != 0:
         raise ValueError("oracle decode: a sequence length or block-table entry is out of range")
     return out
@@ -147,7 +162,7 @@ def available_threads() -> int:
 
 
 __all__ = [
-    "F32", "BF16", "OracleBlockManager", "run_script", "pad_tables",
+    "F32", "BF16", "ROW", "SPLIT", "cache_geometry", "OracleBlockManager", "run_script", "pad_tables",
     "bf16_bits_to_f64", "physical_index", "slot_mapping", "reshape_and_cache", "copy_blocks",
     "decode", "available_threads", "build_oracle",
 ]

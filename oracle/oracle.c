@@ -41,6 +41,13 @@
  *
  * Element types: 0 = IEEE fp32, 1 = bfloat16 (upper 16 bits of an fp32).
  * bfloat16 values are widened exactly (bits << 16) before any arithmetic.
+ *
+ * Cache layouts (the element of token slot blk * B + off, KV head h, dim d):
+ *   0  block rows  K and V [num_blocks, B, Hk, D]   ([PidokuInfra 10]
+ *                  section 5 "The kernel side", comment on k_cache)
+ *   1  split       K [num_blocks, Hk, D/x, B, x], V [num_blocks, Hk, D, B],
+ *                  x = 16 / element bytes ([PidokuInfra 10] section 5
+ *                  "The layout, more precisely")
  */
 #include <math.h>
 #include <pthread.h>
@@ -68,6 +75,19 @@ static double load_as_double(const void *base, int dtype, int64_t index) {
     return (double)f;
 }
 
+/* Element offsets of (blk, off, h, d) in the K and the V cache. */
+static int64_t k_offset(int layout, int64_t blk, int64_t off, int64_t h, int64_t d, int64_t B, int64_t Hk,
+                        int64_t D, int64_t x) {
+    if (layout == 1) return (((blk * Hk + h) * (D / x) + d / x) * B + off) * x + d % x;
+    return ((blk * B + off) * Hk + h) * D + d;
+}
+
+static int64_t v_offset(int layout, int64_t blk, int64_t off, int64_t h, int64_t d, int64_t B, int64_t Hk,
+                        int64_t D) {
+    if (layout == 1) return ((blk * Hk + h) * D + d) * B + off;
+    return ((blk * B + off) * Hk + h) * D + d;
+}
+
 /* PhysicalIndex: where token `pos` of a sequence lives in the pool. */
 int64_t orc_physical_index(const int32_t *table, int32_t block_size, int64_t pos) {
     int64_t logical_block = pos / block_size;
@@ -92,9 +112,10 @@ void orc_slot_mapping(const int32_t *tables, int32_t max_blocks, const int32_t *
 int32_t orc_reshape_and_cache(const void *k, const void *v, const int64_t *slots,
                               int32_t num_tokens, void *k_cache, void *v_cache,
                               int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
-                              int32_t head_dim, int32_t dtype) {
+                              int32_t head_dim, int32_t dtype, int32_t layout) {
     int32_t out_of_range = 0;
     int64_t eb = elem_bytes(dtype);
+    int64_t x = 16 / eb;
     for (int32_t t = 0; t < num_tokens; ++t) {
         int64_t s = slots[t];
         if (s < 0) continue;
@@ -105,10 +126,13 @@ int32_t orc_reshape_and_cache(const void *k, const void *v, const int64_t *slots
         int64_t blk = s / block_size;
         int64_t off = s % block_size;
         for (int32_t h = 0; h < num_kv_heads; ++h) {
-            int64_t dst = ((blk * block_size + off) * num_kv_heads + h) * head_dim;
-            int64_t src = ((int64_t)t * num_kv_heads + h) * head_dim;
-            memcpy((char *)k_cache + dst * eb, (const char *)k + src * eb, head_dim * eb);
-            memcpy((char *)v_cache + dst * eb, (const char *)v + src * eb, head_dim * eb);
+            for (int32_t d = 0; d < head_dim; ++d) {
+                int64_t src = ((int64_t)t * num_kv_heads + h) * head_dim + d;
+                int64_t kd = k_offset(layout, blk, off, h, d, block_size, num_kv_heads, head_dim, x);
+                int64_t vd = v_offset(layout, blk, off, h, d, block_size, num_kv_heads, head_dim);
+                memcpy((char *)k_cache + kd * eb, (const char *)k + src * eb, eb);
+                memcpy((char *)v_cache + vd * eb, (const char *)v + src * eb, eb);
+            }
         }
     }
     return out_of_range;
@@ -132,7 +156,7 @@ typedef struct {
     double *out;
     int dtype;
     const void *q, *k_cache, *v_cache;
-    int32_t num_blocks, block_size, num_kv_heads, head_dim;
+    int32_t num_blocks, block_size, num_kv_heads, head_dim, layout;
     const int32_t *tables;
     int32_t max_blocks;
     const int32_t *seq_lens;
@@ -166,11 +190,12 @@ static int32_t decode_one(const decode_job *j, int32_t seq, int32_t head, double
         int64_t slot = orc_physical_index(table, j->block_size, pos);
         int64_t blk = slot / j->block_size;
         int64_t off = slot % j->block_size;
-        int64_t kbase = ((blk * j->block_size + off) * j->num_kv_heads + kv_head) * D;
         double dot = 0.0;
         for (int32_t d = 0; d < D; ++d)
             dot += load_as_double(j->q, j->dtype, qbase + d) *
-                   load_as_double(j->k_cache, j->dtype, kbase + d);
+                   load_as_double(j->k_cache, j->dtype,
+                                  k_offset(j->layout, blk, off, kv_head, d, j->block_size,
+                                           j->num_kv_heads, D, 16 / elem_bytes(j->dtype)));
         scores[pos] = j->scale * dot;
     }
     /* softmax weights */
@@ -187,9 +212,11 @@ static int32_t decode_one(const decode_job *j, int32_t seq, int32_t head, double
         int64_t slot = orc_physical_index(table, j->block_size, pos);
         int64_t blk = slot / j->block_size;
         int64_t off = slot % j->block_size;
-        int64_t vbase = ((blk * j->block_size + off) * j->num_kv_heads + kv_head) * D;
         double w = scores[pos] / z;
-        for (int32_t d = 0; d < D; ++d) o[d] += w * load_as_double(j->v_cache, j->dtype, vbase + d);
+        for (int32_t d = 0; d < D; ++d)
+            o[d] += w * load_as_double(j->v_cache, j->dtype,
+                                       v_offset(j->layout, blk, off, kv_head, d, j->block_size,
+                                                j->num_kv_heads, D));
     }
     return 0;
 }
@@ -226,8 +253,9 @@ int32_t orc_decode(double *out, int32_t dtype, const void *q, const void *k_cach
                    int32_t num_kv_heads, int32_t head_dim, const int32_t *tables,
                    int32_t max_blocks, const int32_t *seq_lens, int32_t num_seqs,
                    int32_t num_heads, double scale, const int32_t *pairs, int32_t num_pairs,
-                   int32_t num_threads) {
+                   int32_t num_threads, int32_t layout) {
     if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return -1;
+    if (layout == 1 && head_dim % (16 / elem_bytes(dtype)) != 0) return -1;
     if (num_threads < 1) num_threads = 1;
     decode_job base;
     base.out = out;
@@ -239,6 +267,7 @@ int32_t orc_decode(double *out, int32_t dtype, const void *q, const void *k_cach
     base.block_size = block_size;
     base.num_kv_heads = num_kv_heads;
     base.head_dim = head_dim;
+    base.layout = layout;
     base.tables = tables;
     base.max_blocks = max_blocks;
     base.seq_lens = seq_lens;

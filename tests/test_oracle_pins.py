@@ -312,3 +312,56 @@ def test_slot_mapping_worked_examples(golden_dir):
     m = oracle.OracleBlockManager(1, B)
     for c in g["blocks_needed"]:
         assert m.blocks_needed(c["tokens"]) == c["blocks"]
+
+
+# ------------------------------------------------ split (vLLM) cache layout
+def _to_split(kc, vc):
+    """Row layout [NB, B, Hk, D] -> K [NB, Hk, D/x, B, x], V [NB, Hk, D, B] with
+    x = 16 / element bytes, by torch reshapes and permutes ("10 PagedAttention",
+    section 5, "The layout, more precisely")."""
+    nb, bs, hk, d = kc.shape
+    x = 16 // kc.element_size()
+    k = kc.view(nb, bs, hk, d // x, x).permute(0, 2, 3, 1, 4).contiguous()
+    v = vc.permute(0, 2, 3, 1).contiguous()
+    return k, v
+
+
+@pytest.mark.parametrize("dtype,x", [("bf16", 8), ("f32", 4)])
+def test_split_layout_vector_width(dtype, x):
+    q, kc, vc, tables, lens = _rand_case(dtype, 1, [5], 2, 2, 32, 4, 4, 30)
+    ks, vs = _to_split(kc, vc)
+    layout, nb, bs, hk, d = oracle.cache_geometry(_np(ks), _np(vs))
+    assert layout == oracle.SPLIT and ks.shape[-1] == x and (nb, bs, hk, d) == (4, 4, 2, 32)
+
+
+@pytest.mark.parametrize("dtype,H,Hk,D,B", [("bf16", 8, 2, 32, 16), ("f32", 4, 4, 16, 4), ("bf16", 6, 3, 64, 8)])
+def test_split_layout_decode_equals_row_layout_decode(dtype, H, Hk, D, B):
+    lens = [1, B - 1, B + 1, 3 * B + 2, 0]
+    nblocks = sum(-(-L // B) for L in lens) + 3
+    q, kc, vc, tables, lens = _rand_case(dtype, len(lens), lens, H, Hk, D, B, nblocks, 31)
+    ks, vs = _to_split(kc, vc)
+    row = _oracle(q, kc, vc, tables, lens, 0.2)
+    split = _oracle(q, ks, vs, tables, lens, 0.2)
+    np.testing.assert_array_equal(row, split)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_split_layout_write_equals_permuted_row_write(dtype):
+    g = torch.Generator().manual_seed(32)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    NB, B, Hk, D, T = 5, 8, 2, 16, 11
+    kc = torch.randn(NB, B, Hk, D, generator=g).to(tdt)
+    vc = torch.randn(NB, B, Hk, D, generator=g).to(tdt)
+    k = torch.randn(T, Hk, D, generator=g).to(tdt)
+    v = torch.randn(T, Hk, D, generator=g).to(tdt)
+    slots = torch.randperm(NB * B, generator=g)[:T].numpy()
+    slots[3] = -1
+    ks, vs = (_np(t).copy() for t in _to_split(kc, vc))
+    kr, vr = _np(kc).copy(), _np(vc).copy()
+    assert oracle.reshape_and_cache(_np(k), _np(v), slots, kr, vr) == 0
+    assert oracle.reshape_and_cache(_np(k), _np(v), slots, ks, vs) == 0
+    tk = torch.from_numpy(kr.view(np.int16) if dtype == "bf16" else kr)
+    tv = torch.from_numpy(vr.view(np.int16) if dtype == "bf16" else vr)
+    ek, ev = _to_split(tk, tv)
+    np.testing.assert_array_equal(ks.view(ek.numpy().dtype), ek.numpy())
+    np.testing.assert_array_equal(vs.view(ev.numpy().dtype), ev.numpy())
