@@ -32,7 +32,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention: KV bytes read GB/s (% of GB300 HBM peak), tokens/s"
-EXTRA = [("cfg2", {}), ("cfg4", {"block_size": 32}), ("cfg1", {}), ("cfg3", {"prompt_len": 2008}), ("cfg4", {"block_size": 16})]
+EXTRA = [("cfg2", {}), ("cfg4", {"block_size": 32}), ("cfg1", {}), ("cfg3", {"prompt_len": 2008}), ("cfg4", {"block_size": 16}),
+         ("cfg4", {"block_size": 16, "layout": "split"}), ("cfg2", {"layout": "split"})]
 FLUSH_BYTES = 512 << 20  # > 129 MB L2: written between timed steps
 FALLBACK_HBM_GBS = 6800.0
 
@@ -47,7 +48,8 @@ def parse():
     ap.add_argument("--extra-steps", type=int, default=300)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--workload", default="cfg4-b16",
-                    help="headline workload: cfg4-b16 (default), cfg4-b32, cfg2, cfg1, cfg3-p2000, cfg3-p2008")
+                    help="headline workload: cfg4-b16 (default), cfg4-b32, cfg2, cfg1, cfg3-p2000, cfg3-p2008, "
+                         "cfg4-b16-split, cfg2-split")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--l2", choices=["none", "write"], default="none",
@@ -58,7 +60,9 @@ def parse():
 
 WORKLOADS = {"cfg4-b16": ("cfg4", {"block_size": 16}), "cfg4-b32": ("cfg4", {"block_size": 32}),
              "cfg2": ("cfg2", {}), "cfg1": ("cfg1", {}), "cfg3-p2000": ("cfg3", {}),
-             "cfg3-p2008": ("cfg3", {"prompt_len": 2008})}
+             "cfg3-p2008": ("cfg3", {"prompt_len": 2008}),
+             "cfg4-b16-split": ("cfg4", {"block_size": 16, "layout": "split"}),
+             "cfg2-split": ("cfg2", {"layout": "split"})}
 
 
 # ---------------------------------------------------------------- helpers
@@ -196,10 +200,17 @@ class Step:
         from paged_kv_cache_150_gb300 import inputs
 
         self.pa = pa
+        kw = dict(kw)
+        layout = kw.pop("layout", "row")
         wl = inputs.workload(cfg, **kw)
         wl.seed += seed_offset
+        if layout == "split":
+            wl.name += "-split"
         self.wl = wl
+        self.layout = layout
         vals = inputs.make_values(wl, device="cuda")
+        if layout == "split":  # same values, vLLM split cache layout
+            vals["k_cache"], vals["v_cache"] = inputs.to_split_layout(vals["k_cache"], vals["v_cache"])
         self.initial_host = None
         self.vals = vals
         bm = pa.BlockManager(wl.num_blocks, wl.block_size, wl.free_order)
@@ -437,6 +448,7 @@ def run_ours(args, rank, world):
         for cfg, kw in EXTRA:
             if WORKLOADS[args.workload] == (cfg, kw):
                 continue
+            torch.cuda.empty_cache()
             st = Step(cfg, kw, seed_offset=1000 * rank)
             sm, km, _ = time_steps(st, args.extra_steps, args.warmup, world, flush, kernel_steps=args.extra_steps)
             mean_ms = reduce_max(statistics.mean(sm), world)
@@ -447,7 +459,8 @@ def run_ours(args, rank, world):
                                  "hbm_frac": round(st.kv_bytes / (mean_ms / 1e3) / 1e9 / peak, 4),
                                  "kernel_gbs": round(st.kernel_bytes / (kms / 1e3) / 1e9, 2),
                                  "kernel_ms": round(kms, 5), "kv_bytes": st.kv_bytes,
-                                 "cow_pairs": int(st.host["pairs"].shape[0]), "new_tokens": st.wl.num_new_tokens}
+                                 "cow_pairs": int(st.host["pairs"].shape[0]), "new_tokens": st.wl.num_new_tokens,
+                                 "cache_layout": st.layout}
             del st
             torch.cuda.empty_cache()
         line["workloads"] = extra

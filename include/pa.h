@@ -8,10 +8,11 @@
  *
  * Conventions shared by every call
  * --------------------------------
- * - KV cache layout (both K and V): [num_blocks, block_size, num_kv_heads,
- *   head_dim], row-major, head_dim contiguous ([PidokuInfra 10] section 5
- *   "The kernel side", comment on k_cache).  Token slot s of the pool is the
- *   row k_cache[s / block_size, s % block_size, :, :].
+ * - KV cache layout: pa_cache_desc_t.layout, PA_LAYOUT_ROW by default:
+ *   [num_blocks, block_size, num_kv_heads, head_dim] for both K and V,
+ *   row-major, head_dim contiguous ([PidokuInfra 10] section 5 "The kernel
+ *   side", comment on k_cache).  Token slot s of the pool is block s / B,
+ *   offset s % B.  PA_LAYOUT_SPLIT is the vLLM layout (see pa_layout_t).
  * - Element types: PA_F32 (IEEE fp32) or PA_BF16 (bfloat16).  q, k, v, out
  *   and both caches share the cache's element type.  Arithmetic is fp32.
  * - Pointers named "device" must be CUDA device memory (or managed memory)
@@ -55,6 +56,18 @@ typedef enum pa_status {
 
 typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1 } pa_dtype_t;
 
+/* Cache layouts.  Both keep each physical block contiguous (B * Hk * D
+ * elements per tensor), so block copies and the block-table walk are the same.
+ *   PA_LAYOUT_ROW    K and V [NB, B, Hk, D]: one token's Hk * D elements
+ *                    contiguous ([PidokuInfra 10] section 5 "The kernel side").
+ *   PA_LAYOUT_SPLIT  K [NB, Hk, D/x, B, x] and V [NB, Hk, D, B], x = 16 /
+ *                    element bytes (8 for bf16, 4 for fp32): the layout of
+ *                    [PidokuInfra 10] section 5 "The layout, more precisely",
+ *                    where 16-byte K chunks of consecutive tokens are adjacent
+ *                    and V is stored token-minor.  Needs (D * element bytes)
+ *                    % 16 == 0. */
+typedef enum pa_layout { PA_LAYOUT_ROW = 0, PA_LAYOUT_SPLIT = 1 } pa_layout_t;
+
 /* Shape of the paged KV pool (host struct, read during the call only). */
 typedef struct pa_cache_desc {
     int32_t num_blocks;   /* NB: physical blocks in the pool */
@@ -62,6 +75,7 @@ typedef struct pa_cache_desc {
     int32_t num_kv_heads; /* Hk */
     int32_t head_dim;     /* D */
     int32_t dtype;        /* pa_dtype_t */
+    int32_t layout;       /* pa_layout_t (0 = PA_LAYOUT_ROW) */
 } pa_cache_desc_t;
 
 /* Human-readable name of a status code (static string). */
@@ -75,7 +89,8 @@ const char *pa_version(void);
  *
  * For every new token t with slot s = slot_mapping[t]:
  *     k_cache[s / B, s % B, h, :] = k[t, h, :]   and the same for v,
- * for every KV head h, as bit copies.  The slot is the one the block manager
+ * for every KV head h, as bit copies (in PA_LAYOUT_SPLIT the same elements
+ * go to their split-layout positions).  The slot is the one the block manager
  * gives (physical_block * B + offset; [nano-vLLM ch.04] section 4,
  * Mechanism 3 "The slot mapping"; [tokentrails] Code).
  *
@@ -83,7 +98,7 @@ const char *pa_version(void);
  * slot_mapping  device int32 [num_tokens].  A negative slot is padding and is
  *               skipped.  A slot >= NB * B is skipped and recorded as
  *               PA_ERR_DEVICE_BOUNDS.
- * k_cache, v_cache  device, [NB, B, Hk, D]; written in place.
+ * k_cache, v_cache  device, in the descriptor's layout; written in place.
  * Slots must be distinct (two tokens with one slot race).
  * num_tokens == 0 is a no-op.  Pointers must be 16-byte aligned when a
  * token row (Hk * D elements) is a multiple of 16 bytes.

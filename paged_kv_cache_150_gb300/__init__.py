@@ -40,12 +40,21 @@ def _dtype_code(t):
 
 
 def _cache_desc(k_cache, v_cache):
-    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
-        raise ValueError("caches must both be [num_blocks, block_size, num_kv_heads, head_dim]")
+    """Descriptor read off the cache shapes: K and V [NB, B, Hk, D] (row
+    layout) or K [NB, Hk, D/x, B, x] with V [NB, Hk, D, B] (split layout,
+    x = 16 / element bytes)."""
     if k_cache.dtype != v_cache.dtype:
         raise TypeError("k_cache and v_cache element types differ")
-    nb, bs, hk, d = k_cache.shape
-    return _lib.CacheDesc(nb, bs, hk, d, _dtype_code(k_cache))
+    if k_cache.dim() == 4 and v_cache.shape == k_cache.shape:
+        nb, bs, hk, d = k_cache.shape
+        return _lib.CacheDesc(nb, bs, hk, d, _dtype_code(k_cache), _lib.PA_LAYOUT_ROW)
+    if k_cache.dim() == 5 and v_cache.dim() == 4:
+        nb, hk, dx, bs, x = k_cache.shape
+        if x * k_cache.element_size() == 16 and tuple(v_cache.shape) == (nb, hk, dx * x, bs):
+            return _lib.CacheDesc(nb, bs, hk, dx * x, _dtype_code(k_cache), _lib.PA_LAYOUT_SPLIT)
+    raise ValueError("caches must be K, V [num_blocks, block_size, num_kv_heads, head_dim], or "
+                     "K [num_blocks, num_kv_heads, head_dim/x, block_size, x] with "
+                     "V [num_blocks, num_kv_heads, head_dim, block_size], x = 16 / element bytes")
 
 
 def _dev(t, name, dtype=None):
@@ -67,7 +76,7 @@ def pa_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache):
     torch = _torch()
     desc = _cache_desc(k_cache, v_cache)
     T = k.shape[0]
-    if k.shape != v.shape or k.shape[1:] != k_cache.shape[2:]:
+    if k.shape != v.shape or tuple(k.shape[1:]) != (desc.num_kv_heads, desc.head_dim):
         raise ValueError("k, v must be [num_tokens, num_kv_heads, head_dim] matching the cache")
     if slot_mapping.shape != (T,):
         raise ValueError("slot_mapping must be [num_tokens]")
@@ -133,7 +142,7 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None, work
     torch = _torch()
     desc = _cache_desc(k_cache, v_cache)
     N, H, D = q.shape
-    if D != k_cache.shape[3] or q.dtype != k_cache.dtype:
+    if D != desc.head_dim or q.dtype != k_cache.dtype:
         raise ValueError("q must be [num_seqs, num_heads, head_dim] in the cache's element type")
     if block_tables.dim() != 2 or block_tables.shape[0] != N or seq_lens.shape != (N,):
         raise ValueError("block_tables must be [num_seqs, max_blocks] and seq_lens [num_seqs]")
@@ -168,7 +177,7 @@ def pa_decode_no_alloc(q, k_cache, v_cache, block_tables, seq_lens, scale, out, 
     torch = _torch()
     desc = _cache_desc(k_cache, v_cache)
     N, H, D = q.shape
-    if D != k_cache.shape[3] or q.dtype != k_cache.dtype:
+    if D != desc.head_dim or q.dtype != k_cache.dtype:
         raise ValueError("q must be [num_seqs, num_heads, head_dim] in the cache's element type")
     if block_tables.dim() != 2 or block_tables.shape[0] != N or seq_lens.shape != (N,):
         raise ValueError("block_tables must be [num_seqs, max_blocks] and seq_lens [num_seqs]")

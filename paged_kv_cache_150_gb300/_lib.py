@@ -27,10 +27,14 @@ PA_KERNEL_SIMT = 1
 PA_KERNEL_MMA = 2
 
 
+PA_LAYOUT_ROW = 0
+PA_LAYOUT_SPLIT = 1
+
+
 class CacheDesc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("dtype", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("layout", ctypes.c_int32)]
 
 
 class DecodeOpts(ctypes.Structure):

@@ -8,7 +8,7 @@
 // contiguous at element offset slot * Hk * D, so one token is one contiguous
 // row copy.
 // Block copy: "PagedAttention" (tokentrails), step 4 and Code (copy_block); a
-// whole block is B * Hk * D contiguous elements.
+// whole block is B * Hk * D contiguous elements in both cache layouts.
 #include "pa_internal.h"
 
 namespace pa {
@@ -34,6 +34,39 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
         const int64_t src = (int64_t)t * row_vecs + j;
         k_cache[dst] = __ldcs(k + src);
         v_cache[dst] = __ldcs(v + src);
+    }
+}
+
+// Split layout: K [NB, Hk, D/x, B, x] receives each token's 16-byte chunks at
+// their (head, chunk, offset) positions; V [NB, Hk, D, B] receives one element
+// per (head, d) at stride B.
+template <typename T>
+__global__ void __launch_bounds__(256) reshape_and_cache_split_kernel(
+    const T *__restrict__ k, const T *__restrict__ v, const int32_t *__restrict__ slots, int32_t num_tokens,
+    T *__restrict__ k_cache, T *__restrict__ v_cache, int64_t num_slots, int32_t B, int32_t Hk, int32_t D,
+    unsigned int *__restrict__ err) {
+    grid_launch_dependents();
+    constexpr int X = 16 / (int)sizeof(T);
+    const int64_t per_tok = (int64_t)Hk * D;
+    const int64_t total = (int64_t)num_tokens * per_tok;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int32_t t = (int32_t)(i / per_tok);
+        const int32_t r = (int32_t)(i - (int64_t)t * per_tok);
+        const int32_t h = r / D, d = r - h * D;
+        const int32_t s = __ldg(slots + t);
+        if (s < 0) continue;
+        if ((int64_t)s >= num_slots) {
+            if (r == 0) atomicOr(err, kErrBounds);
+            continue;
+        }
+        const int64_t blk = s / B, off = s - blk * B;
+        const int64_t head = blk * Hk + h;
+        if (d % X == 0) {  // one 16-byte K chunk
+            const int64_t kd = ((head * (D / X) + d / X) * B + off) * X;
+            *reinterpret_cast<uint4 *>(k_cache + kd) = __ldcs(reinterpret_cast<const uint4 *>(k + i));
+        }
+        v_cache[(head * D + d) * B + off] = v[i];
     }
 }
 
@@ -88,15 +121,31 @@ extern "C" pa_status_t pa_reshape_and_cache(const void *k, const void *v, const 
     if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
     unsigned int *err = device_error_word();
     if (!err) return PA_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int64_t num_slots = (int64_t)cache->num_blocks * cache->block_size;
+    if (cache->layout == PA_LAYOUT_SPLIT) {
+        if (((uintptr_t)k | (uintptr_t)k_cache) % 16 != 0) return PA_ERR_INVALID_ARG;
+        const int64_t total = (int64_t)num_tokens * cache->num_kv_heads * cache->head_dim;
+        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256,
+                                                                      (int64_t)std::max(num_sms(), 1) * 16));
+        if (cache->dtype == PA_BF16)
+            reshape_and_cache_split_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+                (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, slot_mapping, num_tokens,
+                (__nv_bfloat16 *)k_cache, (__nv_bfloat16 *)v_cache, num_slots, cache->block_size,
+                cache->num_kv_heads, cache->head_dim, err);
+        else
+            reshape_and_cache_split_kernel<float><<<grid, 256, 0, s>>>(
+                (const float *)k, (const float *)v, slot_mapping, num_tokens, (float *)k_cache, (float *)v_cache,
+                num_slots, cache->block_size, cache->num_kv_heads, cache->head_dim, err);
+        return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
     const int64_t row_bytes = (int64_t)cache->num_kv_heads * cache->head_dim * dtype_bytes(cache->dtype);
     const int vb = vec_bytes_for(row_bytes, k, v, k_cache, v_cache);
     const int32_t row_vecs = (int32_t)(row_bytes / vb);
-    const int64_t num_slots = (int64_t)cache->num_blocks * cache->block_size;
     const int64_t total = (int64_t)num_tokens * row_vecs;
     const int threads = 256;
     const int64_t want = (total + threads - 1) / threads;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)std::max(num_sms(), 1) * 16));
-    cudaStream_t s = (cudaStream_t)stream;
     switch (vb) {
         case 16:
             reshape_and_cache_kernel<uint4><<<grid, threads, 0, s>>>(

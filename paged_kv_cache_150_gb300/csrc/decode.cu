@@ -192,7 +192,7 @@ __device__ __forceinline__ void load_row_slice(const T *__restrict__ p, float (&
 
 // Block tile: NH warps, warp w handles KV head g*NH + w and its G (<= GMAX)
 // query heads, one token at a time (lane holds D/32 consecutive elements).
-template <typename T, int D, int GMAX>
+template <typename T, int D, int GMAX, int LAYOUT>
 __global__ void __launch_bounds__(256) decode_simt_kernel(
     const T *__restrict__ q, T *__restrict__ out, const T *__restrict__ k_cache,
     const T *__restrict__ v_cache, const int32_t *__restrict__ tables, int32_t max_blocks,
@@ -244,10 +244,20 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(
         const int32_t ntok = min(B, L - tok0);
         for (int32_t t = 0; t < ntok; ++t) {
             float kx[VPL], vx[VPL];
-            if (valid) {
+            if (valid && LAYOUT == PA_LAYOUT_ROW) {
                 const int64_t row = (((int64_t)phys * B + t) * Hk + kvh) * D + lane * VPL;
                 load_row_slice<T, VPL>(k_cache + row, kx);
                 load_row_slice<T, VPL>(v_cache + row, vx);
+            } else if (valid) {
+                // split layout: K [NB, Hk, D/X, B, X], V [NB, Hk, D, B]
+                constexpr int X = 16 / (int)sizeof(T);
+                const int64_t head = (int64_t)phys * Hk + kvh;
+#pragma unroll
+                for (int j = 0; j < VPL; ++j) {
+                    const int d = lane * VPL + j;
+                    kx[j] = to_f32<T>(k_cache[((head * (D / X) + d / X) * B + t) * X + d % X]);
+                    vx[j] = to_f32<T>(v_cache[(head * D + d) * B + t]);
+                }
             } else {  // an invalid block id reads zeros (as the TMA kernel does)
 #pragma unroll
                 for (int j = 0; j < VPL; ++j) kx[j] = vx[j] = 0.f;
@@ -317,7 +327,7 @@ __device__ __forceinline__ uint32_t swz_addr(uint32_t slab, int line, int chunk)
     return slab + (uint32_t)line * 128u + ((uint32_t)(chunk ^ (line & 7)) << 4);
 }
 
-template <int D, int B>
+template <int D, int B, int LAYOUT>
 __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
     const __nv_bfloat16 *__restrict__ q, __nv_bfloat16 *__restrict__ out,
@@ -396,8 +406,13 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
                 const uint32_t fb = smem_u32(&full[s]);
                 const uint32_t dst = smem_u32(smem + (size_t)s * stage_bytes);
                 mbar_arrive_expect_tx(fb, stage_bytes);
-                tma_load_4d(dst, &tmk, fb, 0, phys * B, 0, cur.g * NH);
-                tma_load_4d(dst + tile_bytes, &tmv, fb, 0, phys * B, 0, cur.g * NH);
+                if (LAYOUT == PA_LAYOUT_ROW) {
+                    tma_load_4d(dst, &tmk, fb, 0, phys * B, 0, cur.g * NH);
+                    tma_load_4d(dst + tile_bytes, &tmv, fb, 0, phys * B, 0, cur.g * NH);
+                } else {
+                    tma_load_4d(dst, &tmk, fb, 0, 0, cur.g * NH, phys);
+                    tma_load_4d(dst + tile_bytes, &tmv, fb, 0, 0, cur.g * NH, phys);
+                }
                 cur.advance(cu, N);
             }
             // Let every copy still in flight land before the CTA may exit.
@@ -473,19 +488,29 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
         const int32_t tok0 = cur.blk * B;
         const int32_t ntok = min(B, L - tok0);
         if (ntok < B) {
-            // Rows past the sequence end hold stale data (maybe NaN): zero
-            // them in V so that p = 0 rows contribute exactly 0.
+            // Token rows past the sequence end hold stale data (maybe NaN):
+            // zero them in V so that p = 0 rows contribute exactly 0.
             const int rows = B - ntok;
-            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-            for (int e = lane; e < Tile::kHalves * rows * 8; e += 32) {
-                const int chunk = e & 7;
-                const int ri = e >> 3;
-                const int half = ri / rows;
-                const int t = ntok + (ri - half * rows);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                 vslab + (uint32_t)((half * B + t) * 128 + chunk * 16)),
-                             "r"(z.x), "r"(z.y), "r"(z.z), "r"(z.w)
-                             : "memory");
+            if (LAYOUT == PA_LAYOUT_ROW) {
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                for (int e = lane; e < Tile::kHalves * rows * 8; e += 32) {
+                    const int chunk = e & 7;
+                    const int ri = e >> 3;
+                    const int half = ri / rows;
+                    const int t = ntok + (ri - half * rows);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                     vslab + (uint32_t)((half * B + t) * 128 + chunk * 16)),
+                                 "r"(z.x), "r"(z.y), "r"(z.z), "r"(z.w)
+                                 : "memory");
+                }
+            } else {  // split V tile: [d][token], tokens contiguous
+                for (int e = lane; e < D * rows; e += 32) {
+                    const int d = e / rows;
+                    const int t = ntok + (e - d * rows);
+                    asm volatile("st.shared.u16 [%0], %1;" ::"r"(vslab + (uint32_t)((d * B + t) * 2)),
+                                 "h"((unsigned short)0)
+                                 : "memory");
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -501,7 +526,10 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
                 const int t = mt * 16 + rr + (mi & 1) * 8;
                 const int d = kk * 16 + (mi >> 1) * 8;
                 uint32_t a0, a1, a2, a3;
-                ldmatrix_x4(swz_addr(kslab, (d >> 6) * B + t, (d & 63) >> 3), a0, a1, a2, a3);
+                if (LAYOUT == PA_LAYOUT_ROW)
+                    ldmatrix_x4(swz_addr(kslab, (d >> 6) * B + t, (d & 63) >> 3), a0, a1, a2, a3);
+                else  // split K tile [d / 8][token][8]: 8 tokens of a chunk are 128 contiguous bytes
+                    ldmatrix_x4(kslab + (uint32_t)(((d >> 3) * B + t) * 16), a0, a1, a2, a3);
                 mma_bf16_16816(sacc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
             }
             // online softmax in log2 units; rows = tokens, columns = heads
@@ -537,10 +565,16 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
             // O^T (D x 8 heads) += V^T (D x 16 tokens) P^T (16 tokens x 8 heads)
 #pragma unroll
             for (int dm = 0; dm < KT; ++dm) {
-                const int t = mt * 16 + rr + (mi >> 1) * 8;
-                const int d = dm * 16 + (mi & 1) * 8;
                 uint32_t a0, a1, a2, a3;
-                ldmatrix_x4_trans(swz_addr(vslab, (d >> 6) * B + t, (d & 63) >> 3), a0, a1, a2, a3);
+                if (LAYOUT == PA_LAYOUT_ROW) {  // rows are tokens: transpose on load
+                    const int t = mt * 16 + rr + (mi >> 1) * 8;
+                    const int d = dm * 16 + (mi & 1) * 8;
+                    ldmatrix_x4_trans(swz_addr(vslab, (d >> 6) * B + t, (d & 63) >> 3), a0, a1, a2, a3);
+                } else {  // split V tile [d][token]: rows are already V^T
+                    const int d = dm * 16 + rr + (mi & 1) * 8;
+                    const int t = mt * 16 + (mi >> 1) * 8;
+                    ldmatrix_x4(vslab + (uint32_t)((d * B + t) * 2), a0, a1, a2, a3);
+                }
                 mma_bf16_16816(o[dm], a0, a1, a2, a3, pb0, pb1);
             }
         }
@@ -641,17 +675,18 @@ size_t mma_smem_bytes(int D, int B, int NH) {
 }
 
 template <typename T, int D, int GMAX>
-const void *simt_fn() {
-    return (const void *)decode_simt_kernel<T, D, GMAX>;
+const void *simt_fn(int layout) {
+    return layout == PA_LAYOUT_SPLIT ? (const void *)decode_simt_kernel<T, D, GMAX, PA_LAYOUT_SPLIT>
+                                     : (const void *)decode_simt_kernel<T, D, GMAX, PA_LAYOUT_ROW>;
 }
 
-const void *simt_kernel_ptr(int dtype, int D, int G) {
+const void *simt_kernel_ptr(int dtype, int D, int G, int layout) {
     const int gm = simt_gmax(G);
 #define PA_SIMT_CASE(TT, DD)                                        \
     if (D == DD) {                                                  \
-        if (gm == 1) return simt_fn<TT, DD, 1>();                   \
-        if (gm == 4) return simt_fn<TT, DD, 4>();                   \
-        return simt_fn<TT, DD, 8>();                                \
+        if (gm == 1) return simt_fn<TT, DD, 1>(layout);             \
+        if (gm == 4) return simt_fn<TT, DD, 4>(layout);             \
+        return simt_fn<TT, DD, 8>(layout);                          \
     }
     if (dtype == PA_F32) {
         PA_SIMT_CASE(float, 64)
@@ -665,12 +700,17 @@ const void *simt_kernel_ptr(int dtype, int D, int G) {
     return nullptr;
 }
 
-const void *mma_kernel_ptr(int D, int B) {
-    if (D == 128 && B == 16) return (const void *)decode_mma_kernel<128, 16>;
-    if (D == 128 && B == 32) return (const void *)decode_mma_kernel<128, 32>;
-    if (D == 64 && B == 16) return (const void *)decode_mma_kernel<64, 16>;
-    if (D == 64 && B == 32) return (const void *)decode_mma_kernel<64, 32>;
+template <int LAYOUT>
+const void *mma_fn(int D, int B) {
+    if (D == 128 && B == 16) return (const void *)decode_mma_kernel<128, 16, LAYOUT>;
+    if (D == 128 && B == 32) return (const void *)decode_mma_kernel<128, 32, LAYOUT>;
+    if (D == 64 && B == 16) return (const void *)decode_mma_kernel<64, 16, LAYOUT>;
+    if (D == 64 && B == 32) return (const void *)decode_mma_kernel<64, 32, LAYOUT>;
     return nullptr;
+}
+
+const void *mma_kernel_ptr(int D, int B, int layout) {
+    return layout == PA_LAYOUT_SPLIT ? mma_fn<PA_LAYOUT_SPLIT>(D, B) : mma_fn<PA_LAYOUT_ROW>(D, B);
 }
 
 // Occupancy-based default split count: one full wave of resident CTAs.
@@ -715,8 +755,8 @@ pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_d
     int C = opts ? opts->num_splits : 0;
     if (C == 0) {
         if (!need_default_splits) return PA_ERR_INVALID_ARG;
-        const void *fn = kernel == PA_KERNEL_MMA ? mma_kernel_ptr(c->head_dim, c->block_size)
-                                                 : simt_kernel_ptr(c->dtype, c->head_dim, G);
+        const void *fn = kernel == PA_KERNEL_MMA ? mma_kernel_ptr(c->head_dim, c->block_size, c->layout)
+                                                 : simt_kernel_ptr(c->dtype, c->head_dim, G, c->layout);
         const int threads = kernel == PA_KERNEL_MMA ? (p->NH + 1) * 32 : p->NH * 32;
         C = default_ctas(fn, threads, p->smem);
         if (C <= 0) return PA_ERR_CUDA;
@@ -769,20 +809,35 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 4-D map over one bf16 cache viewed as {64, NB*B, D/64, Hk} with strides
-// {-, Hk*D*2, 128, D*2} bytes; box {64, B, D/64, NH}, 128-byte swizzle.
+// 4-D maps over one bf16 cache (both use 128-byte rows of 64 elements).
+// Row layout: {64, NB*B, D/64, Hk} with byte strides {Hk*D*2, 128, D*2}, box
+// {64, B, D/64, NH}, 128-byte swizzle -> shared [head][half][token][64].
+// Split layout (K [NB, Hk, D/8, B, 8] or V [NB, Hk, D, B]): each (block, head)
+// slab is D*B contiguous elements, viewed as {64, D*B/64, Hk, NB} with strides
+// {128, D*B*2, Hk*D*B*2}, box {64, D*B/64, NH, 1}, no swizzle -> the slab's
+// own byte order in shared memory.
 bool encode_cache_map(CUtensorMap *map, const void *base, const pa_cache_desc_t *c, int NH) {
     auto fn = encode_fn();
     if (!fn) return false;
     const int D = c->head_dim;
-    cuuint64_t dims[4] = {64, (cuuint64_t)c->num_blocks * c->block_size, (cuuint64_t)(D / 64),
-                          (cuuint64_t)c->num_kv_heads};
-    cuuint64_t strides[3] = {(cuuint64_t)c->num_kv_heads * D * 2, 128, (cuuint64_t)D * 2};
-    cuuint32_t box[4] = {64, (cuuint32_t)c->block_size, (cuuint32_t)(D / 64), (cuuint32_t)NH};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
-                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const int B = c->block_size;
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r;
+    if (c->layout == PA_LAYOUT_SPLIT) {
+        cuuint64_t dims[4] = {64, (cuuint64_t)D * B / 64, (cuuint64_t)c->num_kv_heads, (cuuint64_t)c->num_blocks};
+        cuuint64_t strides[3] = {128, (cuuint64_t)D * B * 2, (cuuint64_t)c->num_kv_heads * D * B * 2};
+        cuuint32_t box[4] = {64, (cuuint32_t)(D * B / 64), (cuuint32_t)NH, 1};
+        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[4] = {64, (cuuint64_t)c->num_blocks * B, (cuuint64_t)(D / 64), (cuuint64_t)c->num_kv_heads};
+        cuuint64_t strides[3] = {(cuuint64_t)c->num_kv_heads * D * 2, 128, (cuuint64_t)D * 2};
+        cuuint32_t box[4] = {64, (cuuint32_t)B, (cuuint32_t)(D / 64), (cuuint32_t)NH};
+        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r == CUDA_SUCCESS;
 }
 
@@ -869,7 +924,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         CUtensorMap tmk, tmv;
         if (!encode_cache_map(&tmk, k_cache, cache, p.NH) || !encode_cache_map(&tmv, v_cache, cache, p.NH))
             return PA_ERR_CUDA;
-        const void *fn = mma_kernel_ptr(cache->head_dim, cache->block_size);
+        const void *fn = mma_kernel_ptr(cache->head_dim, cache->block_size, cache->layout);
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
             return PA_ERR_CUDA;
         const dim3 grid(p.C), block((p.NH + 1) * 32);
@@ -882,7 +937,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
                         &NB, &NHv, &sl, &Cv, &ml, &acc, &cnt, &err};
         if (launch_pdl(fn, grid, block, args, p.smem, s) != cudaSuccess) return PA_ERR_CUDA;
     } else {
-        const void *fn = simt_kernel_ptr(cache->dtype, cache->head_dim, G);
+        const void *fn = simt_kernel_ptr(cache->dtype, cache->head_dim, G, cache->layout);
         if (!fn) return PA_ERR_UNSUPPORTED;
         const dim3 grid(p.C), block(p.NH * 32);
         int32_t NB = cache->num_blocks, Hk = cache->num_kv_heads, NHv = p.NH, Cv = p.C;

@@ -268,3 +268,14 @@ def shard_sequences(seq_bytes, world_size: int):
         parts[r].append(int(i))
         loads[r] += seq_bytes[i]
     return [np.asarray(sorted(p), dtype=np.int64) for p in parts]
+
+
+def to_split_layout(k_cache, v_cache):
+    """The same cache contents in the split layout: K [NB, Hk, D/x, B, x] and
+    V [NB, Hk, D, B], x = 16 / element bytes (a reshape/permute of the random
+    values, for workloads run in that layout)."""
+    nb, bs, hk, d = k_cache.shape
+    x = 16 // k_cache.element_size()
+    k = k_cache.view(nb, bs, hk, d // x, x).permute(0, 2, 3, 1, 4).contiguous()
+    v = v_cache.permute(0, 2, 3, 1).contiguous()
+    return k, v

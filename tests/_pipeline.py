@@ -15,9 +15,12 @@ from paged_kv_cache_150_gb300 import inputs
 TOL = {"f32": 1e-5, "bf16": 2e-2}
 
 
-def host_values(wl, device):
-    """Seeded values generated on ``device``; returns (device tensors, host numpy)."""
+def host_values(wl, device, layout="row"):
+    """Seeded values generated on ``device`` (caches in the row or the split
+    layout); returns (device tensors, host numpy)."""
     vals = inputs.make_values(wl, device=device)
+    if layout == "split":
+        vals["k_cache"], vals["v_cache"] = inputs.to_split_layout(vals["k_cache"], vals["v_cache"])
     dev = {k: v.to("cuda") for k, v in vals.items()}
     host = {k: inputs.to_numpy_elems(v).copy() for k, v in vals.items()}
     return dev, host

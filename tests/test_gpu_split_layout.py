@@ -1,0 +1,75 @@
+"""GPU parity in the split cache layout (K [NB, Hk, D/x, B, x], V [NB, Hk, D, B],
+x = 16 / element bytes; "10 PagedAttention", section 5, "The layout, more
+precisely"): bit-exact cache write and block copy, decode within tolerance,
+and agreement with the row layout on the same logical contents."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_150_gb300 import inputs
+from _pipeline import TOL, gpu_step, host_values, max_abs_err, oracle_decode, oracle_step, sample_pairs
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [("cfg0", {}), ("cfg1", {"small": True}), ("cfg2", {"small": True}),
+         ("cfg3", {"small": True, "prompt_len": 200}), ("cfg4", {"small": True}),
+         ("cfg4", {"small": True, "block_size": 32})]
+
+
+@pytest.mark.parametrize("cfg,kw", SMALL)
+@pytest.mark.parametrize("kernel,splits", [("auto", 0), ("auto", 5), ("simt", 0)])
+def test_split_layout_step_matches_oracle(cfg, kw, kernel, splits):
+    wl = inputs.workload(cfg, **kw)
+    dev, host = host_values(wl, "cpu", layout="split")
+    r = oracle_step(wl, host)
+    ref = oracle_decode(wl, host, r)
+    g = gpu_step(wl, dev, kernel=kernel, num_splits=splits)
+    assert np.array_equal(inputs.to_numpy_elems(g["k_cache"]), r["k_cache"])
+    assert np.array_equal(inputs.to_numpy_elems(g["v_cache"]), r["v_cache"])
+    assert max_abs_err(g["out"], ref) <= TOL[wl.dtype]
+
+
+@pytest.mark.parametrize("cfg,kw,nsample", [("cfg2", {}, 96), ("cfg4", {}, 24), ("cfg3", {"prompt_len": 2008}, 48)])
+def test_split_layout_full_size(cfg, kw, nsample):
+    wl = inputs.workload(cfg, **kw)
+    dev, host = host_values(wl, "cuda", layout="split")
+    r = oracle_step(wl, host)
+    g = gpu_step(wl, dev)
+    assert np.array_equal(inputs.to_numpy_elems(g["k_cache"]), r["k_cache"])
+    assert np.array_equal(inputs.to_numpy_elems(g["v_cache"]), r["v_cache"])
+    pairs = sample_pairs(wl, nsample)
+    assert max_abs_err(g["out"], oracle_decode(wl, host, r, pairs=pairs), pairs) <= TOL[wl.dtype]
+
+
+def test_split_and_row_layouts_agree():
+    wl = inputs.workload("cfg2", small=True)
+    outs = []
+    for layout in ("row", "split"):
+        dev, _ = host_values(wl, "cpu", layout=layout)
+        outs.append(gpu_step(wl, dev)["out"].float())
+    assert (outs[0] - outs[1]).abs().max().item() <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
+def test_split_layout_stale_nan_slots_are_never_read(kernel):
+    wl = inputs.decode_workload("nan", [3, 17, 40, 16, 100], 32, 8, 128, 16, "bf16", seed=6, pool_factor=1.5)
+    r = oracle.run_script(wl.num_blocks, wl.block_size, wl.free_order, wl.script)
+    live = np.zeros((wl.num_blocks, wl.block_size), bool)
+    for t, L in zip(r["tables"], r["lens"]):
+        for pos in range(int(L)):
+            live[t[pos // wl.block_size], pos % wl.block_size] = True
+    vals = inputs.make_values(wl, "cpu")
+    mask = torch.from_numpy(~live)
+    for name in ("k_cache", "v_cache"):
+        vals[name].view(torch.int16)[mask] = 0x7FC0  # bf16 NaN in every stale slot
+    ks, vs = inputs.to_split_layout(vals["k_cache"], vals["v_cache"])
+    vals["k_cache"], vals["v_cache"] = ks, vs
+    dev = {k: v.cuda() for k, v in vals.items()}
+    host = {k: inputs.to_numpy_elems(v).copy() for k, v in vals.items()}
+    r = oracle_step(wl, host)
+    ref = oracle_decode(wl, host, r)
+    assert np.isfinite(ref).all()
+    g = gpu_step(wl, dev, kernel=kernel, num_splits=4)
+    assert torch.isfinite(g["out"].float()).all()
+    assert max_abs_err(g["out"], ref) <= TOL["bf16"]
