@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention: KV bytes read GB/s (% of GB300 HBM peak), tokens/s"
 EXTRA = [("cfg2", {}), ("cfg4", {"block_size": 32}), ("cfg1", {}), ("cfg3", {"prompt_len": 2008}), ("cfg4", {"block_size": 16}),
-         ("cfg4", {"block_size": 16, "layout": "split"}), ("cfg2", {"layout": "split"})]
+         ("cfg4", {"block_size": 16, "layout": "split"}), ("cfg2", {"layout": "split"}), ("prefix", {})]
 FLUSH_BYTES = 512 << 20  # > 129 MB L2: written between timed steps
 FALLBACK_HBM_GBS = 6800.0
 
@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--workload", default="cfg4-b16",
                     help="headline workload: cfg4-b16 (default), cfg4-b32, cfg2, cfg1, cfg3-p2000, cfg3-p2008, "
-                         "cfg4-b16-split, cfg2-split")
+                         "cfg4-b16-split, cfg2-split, prefix")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--l2", choices=["none", "write"], default="none",
@@ -62,7 +62,7 @@ WORKLOADS = {"cfg4-b16": ("cfg4", {"block_size": 16}), "cfg4-b32": ("cfg4", {"bl
              "cfg2": ("cfg2", {}), "cfg1": ("cfg1", {}), "cfg3-p2000": ("cfg3", {}),
              "cfg3-p2008": ("cfg3", {"prompt_len": 2008}),
              "cfg4-b16-split": ("cfg4", {"block_size": 16, "layout": "split"}),
-             "cfg2-split": ("cfg2", {"layout": "split"})}
+             "cfg2-split": ("cfg2", {"layout": "split"}), "prefix": ("prefix", {})}
 
 
 # ---------------------------------------------------------------- helpers
@@ -244,6 +244,9 @@ class Step:
         self.kernel_launches = 4 + (1 if pairs.shape[0] else 0)
         H, D, eb = wl.num_q_heads, wl.head_dim, wl.elem_bytes
         self.kv_bytes = wl.kv_bytes_read()
+        # distinct physical blocks the decode reads (shared prefixes counted once)
+        used = {int(b) for i, L in enumerate(lens) for b in tables[i, :-(-int(L) // wl.block_size)]}
+        self.unique_block_bytes = len(used) * wl.block_size * wl.num_kv_heads * wl.head_dim * 2 * wl.elem_bytes
         nb_used = int(sum(-(-int(L) // wl.block_size) for L in wl.seq_lens))
         # attention kernel's algorithmic bytes: K/V rows, q, out, block-table entries
         self.kernel_bytes = self.kv_bytes + 2 * wl.num_seqs * H * D * eb + 4 * nb_used
@@ -460,6 +463,8 @@ def run_ours(args, rank, world):
                                  "kernel_gbs": round(st.kernel_bytes / (kms / 1e3) / 1e9, 2),
                                  "kernel_ms": round(kms, 5), "kv_bytes": st.kv_bytes,
                                  "cow_pairs": int(st.host["pairs"].shape[0]), "new_tokens": st.wl.num_new_tokens,
+                                 "unique_block_bytes": st.unique_block_bytes,
+                                 "written_rows": int((st.host["slots"] >= 0).sum()),
                                  "cache_layout": st.layout}
             del st
             torch.cuda.empty_cache()

@@ -297,6 +297,28 @@ pa_status_t pa_bm_refcount(const pa_bm_t *bm, int32_t block, int32_t *ref_out);
 pa_status_t pa_bm_stats(const pa_bm_t *bm, int32_t *free_out, int32_t *used_out,
                         int32_t *shared_out);
 
+/* Prefix caching ([PidokuInfra 10] section 5 "The relationship to prefix
+ * caching"; [nano-vLLM ch.04] section 7, hash_to_block).  Creates a sequence
+ * for a prompt of num_tokens token ids (host), reusing the blocks of the
+ * longest cached prefix made of full blocks (refcount + 1); the other blocks
+ * are allocated, and its full blocks are registered.  A block's key is a
+ * chained hash: 64-bit FNV-1a over the parent block's key (8 bytes
+ * little-endian; 0 for the first block) and the block's token ids (4 bytes
+ * little-endian each); a hit also compares the ids.  *num_cached_tokens_out
+ * receives the number of leading positions whose K/V already sit in the cache
+ * (a multiple of B): the caller writes only positions from there on.  A block
+ * leaves the cache when its refcount reaches 0.  PA_ERR_NO_BLOCKS changes
+ * nothing.  Only prompt blocks are registered; tokens appended later are not. */
+pa_status_t pa_bm_new_seq_cached(pa_bm_t *bm, const int32_t *token_ids, int32_t num_tokens, int32_t *seq_out,
+                                 int32_t *num_cached_tokens_out);
+
+/* Slots of positions [first_pos, first_pos + count) of seq (host slots_out). */
+pa_status_t pa_bm_slots(const pa_bm_t *bm, int32_t seq, int32_t first_pos, int32_t count, int32_t *slots_out);
+
+/* Prefix-cache counters: registered blocks, block hits, block lookups. */
+pa_status_t pa_bm_cache_stats(const pa_bm_t *bm, int32_t *cached_blocks_out, int64_t *hits_out,
+                              int64_t *lookups_out);
+
 /* Export tables for a decode batch: tables_out [n, max_blocks] (host) padded
  * with -1, lens_out [n]; PA_ERR_INVALID_ARG if a table is longer than
  * max_blocks. */

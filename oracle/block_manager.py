@@ -20,7 +20,22 @@ What it follows, by page title and section:
   [tokentrails]     "PagedAttention", step 4: only a partly filled shared block
                     is ever written, so only such a block is copied.
 
+Prefix caching ([PidokuInfra 10] section 5 "The relationship to prefix
+caching"; [nano-vLLM ch.04] section 7, hash_to_block): the token ids of each
+full block are hashed and kept in a hash -> block map; a new sequence whose
+first blocks hash to existing blocks points at them (refcount + 1) instead of
+computing them.
+
 Readings where the pages are silent or differ:
+  * A block's hash covers its parent block's hash and its own token ids
+    (chained), so only a true prefix matches: K/V at a position depend on
+    every earlier token.  Matching stops at the first miss.  The hash is
+    64-bit FNV-1a over the parent hash (8 bytes, little-endian) followed by the
+    block's token ids (4 bytes each, little-endian); the parent of block 0 is
+    0.  A hit also compares the stored token ids.
+  * Only full blocks of a prompt are registered, when the sequence is
+    created, so a cached block is never written (no copy-on-write for it).
+    A block leaves the map when its refcount reaches 0.
   * The free order is a parameter (the stack's bottom first).  The default is
     the Go constructor's: ids pushed from num_blocks-1 down to 0.
   * A failed append (no free block for a new block or for a copy) changes no
@@ -30,6 +45,26 @@ Readings where the pages are silent or differ:
   * Copy-on-write: with refcount n on the written block, each of the first
     n-1 writers copies, and the last one writes in place.
 """
+
+
+FNV_OFFSET = 0xCBF29CE484222325
+FNV_PRIME = 0x100000001B3
+
+
+def fnv1a64(data):
+    """64-bit FNV-1a of a byte string (offset basis, then xor-multiply per byte)."""
+    h = FNV_OFFSET
+    for byte in data:
+        h ^= byte
+        h = (h * FNV_PRIME) & 0xFFFFFFFFFFFFFFFF
+    return h
+
+
+def fnv1a64_block(parent, tokens):
+    """Hash of one full block: FNV-1a over the parent hash (8 bytes LE) then
+    each token id (4 bytes LE)."""
+    data = int(parent).to_bytes(8, "little") + b"".join(int(t & 0xFFFFFFFF).to_bytes(4, "little") for t in tokens)
+    return fnv1a64(data)
 
 
 class OracleBlockManager:
@@ -50,6 +85,10 @@ class OracleBlockManager:
         self.tables = {}
         self.lens = {}
         self._next_seq = 0
+        self.cached = {}      # hash -> block (full prompt blocks)
+        self.block_key = {}   # block -> (hash, token ids) while registered
+        self.hits = 0
+        self.lookups = 0
 
     # ---- block-level calls (PidokuInfra section 4) ----
     def blocks_needed(self, tokens):
@@ -73,6 +112,8 @@ class OracleBlockManager:
             if self.ref[b] == 0:
                 del self.ref[b]
                 self.free.append(b)
+                if b in self.block_key:
+                    del self.cached[self.block_key.pop(b)[0]]
 
     def fork_blocks(self, blocks):
         for b in blocks:
@@ -89,6 +130,41 @@ class OracleBlockManager:
         self.tables[seq] = blocks
         self.lens[seq] = int(prompt_len)
         return seq
+
+    def new_sequence_cached(self, token_ids):
+        """Create a sequence for a prompt, reusing cached full blocks of its
+        prefix.  Returns (seq, cached_tokens) or None (no state change)."""
+        tokens = [int(t) for t in token_ids]
+        B = self.block_size
+        n_full = len(tokens) // B
+        hashes, parent = [], 0
+        for j in range(n_full):
+            parent = fnv1a64_block(parent, tokens[j * B:(j + 1) * B])
+            hashes.append(parent)
+        reused, lookups = [], 0
+        for j in range(n_full):
+            lookups += 1
+            b = self.cached.get(hashes[j])
+            if b is None or self.block_key[b][1] != tuple(tokens[j * B:(j + 1) * B]):
+                break
+            reused.append(b)
+        fresh = self.allocate(self.blocks_needed(len(tokens)) - len(reused))
+        if fresh is None:
+            return None
+        self.lookups += lookups
+        self.hits += len(reused)
+        for b in reused:
+            self.ref[b] += 1
+        table = reused + fresh
+        for j in range(len(reused), n_full):
+            b = table[j]
+            self.cached[hashes[j]] = b
+            self.block_key[b] = (hashes[j], tuple(tokens[j * B:(j + 1) * B]))
+        seq = self._next_seq
+        self._next_seq += 1
+        self.tables[seq] = table
+        self.lens[seq] = len(tokens)
+        return seq, len(reused) * B
 
     def append_token(self, seq):
         """Make room for the next token of ``seq``.
@@ -139,9 +215,10 @@ class OracleBlockManager:
         return len(self.free), self.num_blocks - len(self.free), shared
 
 
-def run_script(num_blocks, block_size, free_order, script):
-    """Run a workload's block-manager script: ("new", tokens), ("fork", parent),
-    ("append", seq, count).  Sequences are numbered in creation order.
+def run_script(num_blocks, block_size, free_order, script, manager=None):
+    """Run a workload's block-manager script: ("new", tokens), ("new_cached",
+    token_ids), ("fork", parent), ("free", seq), ("append", seq, count), on a
+    fresh manager or on ``manager``.  Sequences are numbered in creation order.
 
     Returns a dict with the manager, the final ``tables`` (list per sequence),
     ``lens``, the ``slots`` of every appended token in script order, the
@@ -149,14 +226,26 @@ def run_script(num_blocks, block_size, free_order, script):
     ``written_refcounts``: the refcount of each written block at write time."""
     import numpy as np
 
-    m = OracleBlockManager(num_blocks, block_size, free_order)
+    m = manager if manager is not None else OracleBlockManager(num_blocks, block_size, free_order)
     slots, pairs, written_refs = [], [], []
     for op in script:
         if op[0] == "new":
             if m.new_sequence(op[1]) is None:
                 raise RuntimeError("pool exhausted creating a sequence")
+        elif op[0] == "new_cached":
+            got = m.new_sequence_cached(op[1])
+            if got is None:
+                raise RuntimeError("pool exhausted creating a sequence")
+            seq, cached = got
+            # every prompt position has a K/V row; cached ones are not written
+            for pos in range(len(op[1])):
+                slots.append(-1 if pos < cached else m.physical_index(seq, pos))
+                if pos >= cached:
+                    written_refs.append(m.ref[m.tables[seq][pos // block_size]])
         elif op[0] == "fork":
             m.fork(op[1])
+        elif op[0] == "free":
+            m.free_seq(op[1])
         elif op[0] == "append":
             for _ in range(op[2]):
                 got = m.append_token(op[1])

@@ -114,8 +114,16 @@ def _opts(num_splits, kernel, events):
     return o
 
 
+def _cache_desc_from_k(k_cache):
+    """Descriptor from the K cache alone (its shape fixes the layout)."""
+    if k_cache.dim() == 5:
+        nb, hk, dx, bs, x = k_cache.shape
+        return _cache_desc(k_cache, k_cache.new_empty((nb, hk, dx * x, bs)))
+    return _cache_desc(k_cache, k_cache)
+
+
 def pa_decode_workspace_bytes(k_cache, num_seqs, num_heads, num_splits=0, kernel="auto"):
-    desc = _cache_desc(k_cache, k_cache)
+    desc = _cache_desc_from_k(k_cache)
     o = _opts(num_splits, kernel, None)
     n = _lib.load().pa_decode_workspace_bytes(ctypes.byref(desc), int(num_seqs), int(num_heads),
                                               ctypes.byref(o))
@@ -125,7 +133,7 @@ def pa_decode_workspace_bytes(k_cache, num_seqs, num_heads, num_splits=0, kernel
 
 
 def pa_decode_default_splits(k_cache, num_heads, kernel="auto"):
-    desc = _cache_desc(k_cache, k_cache)
+    desc = _cache_desc_from_k(k_cache)
     o = _opts(0, kernel, None)
     n = _lib.load().pa_decode_default_splits(ctypes.byref(desc), int(num_heads), ctypes.byref(o))
     if n < 0:
@@ -253,6 +261,25 @@ class BlockManager:
         self._call("pa_bm_new_seq", int(num_tokens), ctypes.byref(s))
         return s.value
 
+    def new_seq_cached(self, token_ids):
+        """Prompt with prefix caching: (seq, cached_tokens); positions below
+        cached_tokens already have K/V in shared blocks."""
+        toks = np.ascontiguousarray(np.asarray(token_ids, dtype=np.int32))
+        s, c = ctypes.c_int32(), ctypes.c_int32()
+        self._call("pa_bm_new_seq_cached", _i32p(toks), toks.shape[0], ctypes.byref(s), ctypes.byref(c))
+        return s.value, c.value
+
+    def slots(self, seq, first_pos, count):
+        out = np.empty(max(int(count), 1), dtype=np.int32)
+        self._call("pa_bm_slots", int(seq), int(first_pos), int(count), _i32p(out))
+        return out[:int(count)]
+
+    def cache_stats(self):
+        """(registered blocks, block hits, block lookups) of the prefix cache."""
+        n, h, l = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int64()
+        self._call("pa_bm_cache_stats", ctypes.byref(n), ctypes.byref(h), ctypes.byref(l))
+        return n.value, h.value, l.value
+
     def fork(self, parent):
         s = ctypes.c_int32()
         self._call("pa_bm_fork", int(parent), ctypes.byref(s))
@@ -319,8 +346,18 @@ class BlockManager:
         for op in script:
             if op[0] == "new":
                 self.new_seq(op[1])
+            elif op[0] == "new_cached":
+                # every prompt position has a K/V row; cached positions get
+                # slot -1 (padding: the cache write skips them)
+                seq, cached = self.new_seq_cached(op[1])
+                n = len(op[1])
+                s = np.full(n, -1, dtype=np.int32)
+                s[cached:] = self.slots(seq, cached, n - cached)
+                slots.append(s)
             elif op[0] == "fork":
                 self.fork(op[1])
+            elif op[0] == "free":
+                self.free_seq(op[1])
             elif op[0] == "append":
                 s, pair = self.append_tokens(op[1], op[2])
                 slots.append(s)

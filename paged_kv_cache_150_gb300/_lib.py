@@ -78,6 +78,9 @@ SIGNATURES = {
     "pa_bm_refcount": (_I32, [_P, _I32, _PI32]),
     "pa_bm_stats": (_I32, [_P, _PI32, _PI32, _PI32]),
     "pa_bm_export": (_I32, [_P, _PI32, _I32, _I32, _PI32, _PI32]),
+    "pa_bm_new_seq_cached": (_I32, [_P, _PI32, _I32, _PI32, _PI32]),
+    "pa_bm_slots": (_I32, [_P, _I32, _I32, _I32, _PI32]),
+    "pa_bm_cache_stats": (_I32, [_P, _PI32, _PI64, _PI64]),
 }
 
 _lib = None

@@ -8,8 +8,17 @@
 // "Copy-on-write block sharing" and section 7 "The BlockManager in code"
 // (refcount > 1 means copy before writing; allocation failure is reported,
 // not raised).  Every failing call leaves the state unchanged.
+//
+// Prefix caching ("10 PagedAttention" section 5, "The relationship to prefix
+// caching"; nano-vLLM's hash_to_block): full prompt blocks are registered
+// under a chained hash (64-bit FNV-1a over the parent block's hash, 8 bytes
+// little-endian, then the block's token ids, 4 bytes little-endian each; the
+// parent of block 0 is 0), and a new prompt reuses the blocks of its longest
+// registered prefix (refcount + 1).  A hit also compares the token ids.  A
+// block leaves the map when its refcount reaches 0.
 #include <cstdint>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 #include "pa.h"
@@ -25,6 +34,20 @@ struct pa_bm {
         std::vector<int32_t> table;
     };
     std::vector<Seq> seqs;          // indexed by sequence id
+    // prefix cache
+    std::unordered_map<uint64_t, int32_t> cached;  // chained hash -> block
+    std::vector<uint64_t> block_hash;               // per block, valid when registered
+    std::vector<char> registered;
+    std::vector<int32_t> block_tokens;              // B token ids per registered block
+    int64_t hits = 0, lookups = 0;
+
+    void release(int32_t b) {  // refcount reached 0
+        free.push_back(b);
+        if (!registered.empty() && registered[b]) {
+            cached.erase(block_hash[b]);
+            registered[b] = 0;
+        }
+    }
 
     int32_t blocks_needed(int64_t tokens) const {
         return (int32_t)((tokens + block_size - 1) / block_size);
@@ -116,7 +139,7 @@ extern "C" pa_status_t pa_bm_free_seq(pa_bm_t *bm, int32_t seq) {
     pa_bm::Seq *s = bm->get(seq);
     if (!s) return PA_ERR_INVALID_ARG;
     for (int32_t b : s->table) {
-        if (--bm->ref[b] == 0) bm->free.push_back(b);
+        if (--bm->ref[b] == 0) bm->release(b);
     }
     s->table.clear();
     s->table.shrink_to_fit();
@@ -233,5 +256,94 @@ extern "C" pa_status_t pa_bm_export(const pa_bm_t *bm, const int32_t *seqs, int3
         for (int32_t j = 0; j < max_blocks; ++j) row[j] = j < nb ? s->table[j] : -1;
         lens_out[i] = s->len;
     }
+    return PA_OK;
+}
+
+namespace {
+constexpr uint64_t kFnvOffset = 0xCBF29CE484222325ull;
+constexpr uint64_t kFnvPrime = 0x100000001B3ull;
+
+uint64_t block_chain_hash(uint64_t parent, const int32_t *tokens, int32_t B) {
+    uint64_t h = kFnvOffset;
+    for (int i = 0; i < 8; ++i) {
+        h ^= (parent >> (8 * i)) & 0xFFu;
+        h *= kFnvPrime;
+    }
+    for (int32_t t = 0; t < B; ++t) {
+        const uint32_t v = (uint32_t)tokens[t];
+        for (int i = 0; i < 4; ++i) {
+            h ^= (v >> (8 * i)) & 0xFFu;
+            h *= kFnvPrime;
+        }
+    }
+    return h;
+}
+}  // namespace
+
+extern "C" pa_status_t pa_bm_new_seq_cached(pa_bm_t *bm, const int32_t *token_ids, int32_t num_tokens,
+                                            int32_t *seq_out, int32_t *num_cached_tokens_out) {
+    if (!bm || num_tokens < 0 || (num_tokens > 0 && !token_ids) || !seq_out) return PA_ERR_INVALID_ARG;
+    const int32_t B = bm->block_size;
+    const int32_t n_full = num_tokens / B;
+    if (bm->registered.empty()) {
+        bm->registered.assign((size_t)bm->num_blocks, 0);
+        bm->block_hash.assign((size_t)bm->num_blocks, 0);
+        bm->block_tokens.assign((size_t)bm->num_blocks * B, 0);
+    }
+    std::vector<uint64_t> hashes((size_t)n_full);
+    uint64_t parent = 0;
+    for (int32_t j = 0; j < n_full; ++j) parent = hashes[j] = block_chain_hash(parent, token_ids + (int64_t)j * B, B);
+    std::vector<int32_t> table;
+    int64_t lookups = 0;
+    for (int32_t j = 0; j < n_full; ++j) {
+        ++lookups;
+        auto it = bm->cached.find(hashes[j]);
+        if (it == bm->cached.end()) break;
+        const int32_t b = it->second;
+        bool same = true;
+        for (int32_t t = 0; t < B && same; ++t)
+            same = bm->block_tokens[(int64_t)b * B + t] == token_ids[(int64_t)j * B + t];
+        if (!same) break;
+        table.push_back(b);
+    }
+    const int32_t reused = (int32_t)table.size();
+    const int32_t need = bm->blocks_needed(num_tokens) - reused;
+    if ((int64_t)need > (int64_t)bm->free.size()) return PA_ERR_NO_BLOCKS;
+    for (int32_t b : table) bm->ref[b] += 1;
+    bm->take(need, table);
+    for (int32_t j = reused; j < n_full; ++j) {
+        const int32_t b = table[j];
+        bm->cached[hashes[j]] = b;
+        bm->block_hash[b] = hashes[j];
+        bm->registered[b] = 1;
+        for (int32_t t = 0; t < B; ++t) bm->block_tokens[(int64_t)b * B + t] = token_ids[(int64_t)j * B + t];
+    }
+    bm->lookups += lookups;
+    bm->hits += reused;
+    pa_bm::Seq s;
+    s.live = true;
+    s.len = num_tokens;
+    s.table = std::move(table);
+    bm->seqs.push_back(std::move(s));
+    *seq_out = (int32_t)bm->seqs.size() - 1;
+    if (num_cached_tokens_out) *num_cached_tokens_out = reused * B;
+    return PA_OK;
+}
+
+extern "C" pa_status_t pa_bm_slots(const pa_bm_t *bm, int32_t seq, int32_t first_pos, int32_t count,
+                                   int32_t *slots_out) {
+    if (!bm || count < 0 || first_pos < 0 || (count > 0 && !slots_out)) return PA_ERR_INVALID_ARG;
+    const pa_bm::Seq *s = bm->get(seq);
+    if (!s || (int64_t)first_pos + count > s->len) return PA_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < count; ++i) slots_out[i] = bm->slot(*s, first_pos + i);
+    return PA_OK;
+}
+
+extern "C" pa_status_t pa_bm_cache_stats(const pa_bm_t *bm, int32_t *cached_blocks_out, int64_t *hits_out,
+                                         int64_t *lookups_out) {
+    if (!bm) return PA_ERR_INVALID_ARG;
+    if (cached_blocks_out) *cached_blocks_out = (int32_t)bm->cached.size();
+    if (hits_out) *hits_out = bm->hits;
+    if (lookups_out) *lookups_out = bm->lookups;
     return PA_OK;
 }

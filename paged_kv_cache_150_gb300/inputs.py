@@ -22,6 +22,9 @@ Workload shapes follow the pages' examples and the five benchmark workloads:
         and appends of 1..40 tokens.
   cfg4  bf16 long context: 16 sequences of 32768 tokens, 64 q / 8 KV heads,
         head_dim 128, block_size 16 or 32, pool 1.05x the need.
+  prefix  bf16 prefix caching: 8 system prompts of 2000 tokens, 10 requests
+        each with a U[16, 512]-token suffix (32 q / 8 KV heads, head_dim 128,
+        block_size 16); the reduced twin has 2 prompts of 200 tokens x 3.
 
 Conventions (readings of the workload text):
   * Workload k is seeded with 1500 + k (numpy PCG64 for structure, a torch
@@ -161,12 +164,141 @@ def sampling_workload(name: str, num_prompts: int, prompt_len: int, samples: int
                            "num_prompts": num_prompts})
 
 
+NEW_CACHED = "new_cached"  # ("new_cached", token_ids): a prompt that may reuse cached prefix blocks
+FREE = "free"              # ("free", seq): release a sequence's blocks
+
+
+@dataclass
+class BeamWorkload:
+    """Beam search over one prompt: a list of steps, each a block-manager
+    script (one appended token per live beam) followed by a decode over the
+    live beams; after the decode the step's selection ops (free the beams not
+    chosen, fork the ones chosen more than once) run.  Values: one K/V row per
+    appended token, in script order over all steps."""
+    name: str
+    dtype: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    seed: int
+    free_order: np.ndarray
+    prompt_len: int
+    beams: int
+    steps: list              # [{"ops": [...], "decode": [seq ids], "select": [...]}]
+    num_new_tokens: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def elem_bytes(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+
+def beam_workload(name: str, prompt_len: int, beams: int, num_steps: int, num_q_heads: int, num_kv_heads: int,
+                  head_dim: int, block_size: int, dtype: str, seed: int) -> BeamWorkload:
+    """Each step every live beam appends a token; then `beams` parents are
+    drawn (uniformly, with replacement) among the live beams: a parent drawn
+    c >= 1 times stays and is forked c - 1 times, a parent never drawn is
+    freed.  Sequence ids are assigned in creation order (the prompt is 0)."""
+    rng = np.random.default_rng(seed)
+    live = [0]
+    next_id = 1
+    steps = []
+    init = [(NEW, prompt_len)]
+    for _ in range(beams - 1):
+        init.append((FORK, 0))
+        live.append(next_id)
+        next_id += 1
+    ntok = 0
+    for s in range(num_steps):
+        ops = list(init) if s == 0 else []
+        for b in live:
+            ops.append((APPEND, b, 1))
+            ntok += 1
+        decode = list(live)
+        picks = rng.integers(0, len(live), size=beams)
+        counts = np.bincount(picks, minlength=len(live))
+        select, new_live = [], []
+        for i, b in enumerate(live):
+            if counts[i] == 0:
+                select.append((FREE, b))
+            else:
+                new_live.append(b)
+                for _ in range(int(counts[i]) - 1):
+                    select.append((FORK, b))
+                    new_live.append(next_id)
+                    next_id += 1
+        steps.append({"ops": ops, "decode": decode, "select": select})
+        live = new_live
+    prompt_blocks = -(-prompt_len // block_size)
+    num_blocks = prompt_blocks + beams * (num_steps // block_size + 2) * 2 + 16
+    free_order = _shuffled_free_order(rng, num_blocks)
+    return BeamWorkload(name, dtype, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, seed, free_order,
+                        prompt_len, beams, steps, ntok)
+
+
+def beam(small: bool = False) -> BeamWorkload:
+    """4 beams over a 2008-token prompt (last block partly filled), 40 steps
+    (the reduced twin: 4 beams, 40-token prompt, 24 steps); 32 q / 8 KV heads,
+    head_dim 128, block_size 16, bf16."""
+    if small:
+        return beam_workload("beam-small", 40, 4, 24, 32, 8, 128, 16, "bf16", 2605)
+    return beam_workload("beam", 2008, 4, 40, 32, 8, 128, 16, "bf16", 1605)
+
+
+def prefix_workload(name: str, num_prompts: int, requests_per_prompt: int, system_len: int,
+                    suffix_range, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                    dtype: str, seed: int, spare_blocks: int = 64) -> Workload:
+    """Requests that share system prompts: each of num_prompts system prompts
+    (system_len random token ids) is followed by a per-request random suffix of
+    U[suffix_range] tokens; every request then decodes one token.  With prefix
+    caching the full blocks of a shared system prompt are stored once
+    ("10 PagedAttention" section 2: ten requests with the same 2000-token system
+    prompt would otherwise store ten copies).  K/V rows exist for every prompt
+    position (in script order) and for each decode token; rows of positions
+    that turn out cached are simply not written."""
+    rng = np.random.default_rng(seed)
+    systems = [rng.integers(0, 32000, size=system_len).astype(np.int32) for _ in range(num_prompts)]
+    script: List[Tuple] = []
+    lens = []
+    ntok = 0
+    for r in range(requests_per_prompt):
+        for p in range(num_prompts):
+            suf = rng.integers(0, 32000, size=int(rng.integers(suffix_range[0], suffix_range[1] + 1)))
+            toks = np.concatenate([systems[p], suf.astype(np.int32)])
+            script.append((NEW_CACHED, toks))
+            lens.append(len(toks) + 1)
+            ntok += len(toks)
+    for i in range(len(lens)):
+        script.append((APPEND, i, 1))
+        ntok += 1
+    bs = block_size
+    # pool: every request's own blocks plus one copy of each system prompt
+    per_req = sum(-(-(L) // bs) for L in lens)
+    num_blocks = per_req + spare_blocks
+    free_order = _shuffled_free_order(rng, num_blocks)
+    return Workload(name, dtype, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, seed,
+                    free_order, script, np.asarray(lens, dtype=np.int32), ntok,
+                    note="%d system prompts x %d requests, system %d tokens, suffix U[%d,%d]"
+                         % (num_prompts, requests_per_prompt, system_len, suffix_range[0], suffix_range[1]),
+                    extra={"system_len": system_len, "num_prompts": num_prompts,
+                           "requests_per_prompt": requests_per_prompt})
+
+
 def workload(cfg: str, small: bool = False, block_size: Optional[int] = None,
              prompt_len: Optional[int] = None) -> Workload:
     """The named benchmark workload ("cfg0".."cfg4"), or its reduced-size twin.
 
     ``block_size`` selects 16 or 32 for cfg4; ``prompt_len`` overrides cfg3's
     prompt (2000 as written, 2008 for the copy-on-write variant)."""
+    if cfg == "prefix":
+        if small:
+            return prefix_workload("prefix-small", 2, 3, 200, (1, 40), 32, 8, 128, 16, "bf16", 2600, spare_blocks=8)
+        return prefix_workload("prefix", 8, 10, 2000, (16, 512), 32, 8, 128, 16, "bf16", 1600)
     k = int(cfg[-1])
     seed = (2500 if small else 1500) + k
     rng = np.random.default_rng(seed)
@@ -230,16 +362,18 @@ def _randn(shape, dtype: str, gen, device, chunk_elems: int = 1 << 27):
     return out
 
 
-def make_values(wl: Workload, device="cpu"):
+def make_values(wl, device="cpu"):
     """Random tensors for one step: q [N,H,D], k/v new rows [T,Hk,D] and the
-    pool caches [NB,B,Hk,D], all N(0,1) in the workload's element type."""
+    pool caches [NB,B,Hk,D], all N(0,1) in the workload's element type.  For a
+    beam-search workload q holds one row per (step, decoded beam) in order."""
     import torch
     gen = torch.Generator(device=device)
     gen.manual_seed(wl.seed)
     cache_shape = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
     k_cache = _randn(cache_shape, wl.dtype, gen, device)
     v_cache = _randn(cache_shape, wl.dtype, gen, device)
-    q = _randn((wl.num_seqs, wl.num_q_heads, wl.head_dim), wl.dtype, gen, device)
+    nq = sum(len(s["decode"]) for s in wl.steps) if isinstance(wl, BeamWorkload) else wl.num_seqs
+    q = _randn((nq, wl.num_q_heads, wl.head_dim), wl.dtype, gen, device)
     k_new = _randn((wl.num_new_tokens, wl.num_kv_heads, wl.head_dim), wl.dtype, gen, device)
     v_new = _randn((wl.num_new_tokens, wl.num_kv_heads, wl.head_dim), wl.dtype, gen, device)
     return {"q": q, "k": k_new, "v": v_new, "k_cache": k_cache, "v_cache": v_cache}

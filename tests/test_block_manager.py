@@ -22,7 +22,8 @@ def _built():
 WORKLOADS = [("cfg0", {}), ("cfg1", {}), ("cfg1", {"small": True}), ("cfg2", {}),
              ("cfg2", {"small": True}), ("cfg3", {}), ("cfg3", {"prompt_len": 2008}),
              ("cfg3", {"small": True}), ("cfg3", {"small": True, "prompt_len": 200}),
-             ("cfg4", {}), ("cfg4", {"block_size": 32}), ("cfg4", {"small": True})]
+             ("cfg4", {}), ("cfg4", {"block_size": 32}), ("cfg4", {"small": True}),
+             ("prefix", {}), ("prefix", {"small": True})]
 
 
 @pytest.mark.parametrize("cfg,kw", WORKLOADS)
@@ -38,6 +39,8 @@ def test_manager_matches_oracle_model(cfg, kw):
     np.testing.assert_array_equal(lens, r["lens"])
     np.testing.assert_array_equal(lens, wl.seq_lens)
     assert bm.stats() == r["manager"].stats()
+    m = r["manager"]
+    assert bm.cache_stats() == (len(m.cached), m.hits, m.lookups)
     for b, ref in list(r["manager"].ref.items())[:200]:
         assert bm.refcount(b) == ref
 
@@ -138,3 +141,44 @@ def test_append_tokens_matches_repeated_append_token():
         pairs_b = [x[1] for x in singles if x[1] is not None]
         assert (pair_a is None and not pairs_b) or [pair_a] == pairs_b
     assert a.stats() == b.stats()
+
+
+def test_prefix_cache_matches_oracle_through_frees_and_reuse():
+    rng = np.random.default_rng(5)
+    order = rng.permutation(256).astype(np.int32)
+    bm = pa.BlockManager(256, 8, order)
+    m = oracle.OracleBlockManager(256, 8, order)
+    prompts = [rng.integers(0, 50, size=int(rng.integers(20, 90))).tolist() for _ in range(4)]
+    live = []
+    for step in range(40):
+        p = prompts[int(rng.integers(0, 4))]
+        toks = p[:int(rng.integers(len(p) // 2, len(p) + 1))] + rng.integers(0, 50, size=int(rng.integers(0, 9))).tolist()
+        got = bm.new_seq_cached(toks)
+        want = m.new_sequence_cached(toks)
+        assert got == want
+        live.append(got[0])
+        assert bm.block_table(got[0]) == m.tables[want[0]]
+        if len(live) > 6:
+            victim = live.pop(int(rng.integers(0, len(live))))
+            bm.free_seq(victim)
+            m.free_seq(victim)
+        assert bm.stats() == m.stats()
+        assert bm.cache_stats() == (len(m.cached), m.hits, m.lookups)
+
+
+@pytest.mark.parametrize("small", [True, False])
+def test_beam_search_manager_matches_oracle(small):
+    wl = inputs.beam(small)
+    m = oracle.OracleBlockManager(wl.num_blocks, wl.block_size, wl.free_order)
+    bm = pa.BlockManager(wl.num_blocks, wl.block_size, wl.free_order)
+    for st in wl.steps:
+        r = oracle.run_script(0, wl.block_size, None, st["ops"], manager=m)
+        slots, pairs = bm.apply_script(st["ops"])
+        np.testing.assert_array_equal(slots, r["slots"])
+        np.testing.assert_array_equal(pairs, r["pairs"])
+        mb = max(len(m.tables[s]) for s in st["decode"])
+        tables, lens = bm.export(st["decode"], mb)
+        np.testing.assert_array_equal(tables, oracle.pad_tables([m.tables[s] for s in st["decode"]], mb))
+        oracle.run_script(0, wl.block_size, None, st["select"], manager=m)
+        bm.apply_script(st["select"])
+        assert bm.stats() == m.stats()

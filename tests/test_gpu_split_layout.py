@@ -73,3 +73,15 @@ def test_split_layout_stale_nan_slots_are_never_read(kernel):
     g = gpu_step(wl, dev, kernel=kernel, num_splits=4)
     assert torch.isfinite(g["out"].float()).all()
     assert max_abs_err(g["out"], ref) <= TOL["bf16"]
+
+
+def test_workspace_query_accepts_either_layout():
+    import paged_kv_cache_150_gb300 as pa
+
+    wl = inputs.workload("cfg2", small=True)
+    sizes = []
+    for layout in ("row", "split"):
+        dev, _ = host_values(wl, "cpu", layout=layout)
+        sizes.append(pa.pa_decode_workspace_bytes(dev["k_cache"], wl.num_seqs, wl.num_q_heads))
+        assert pa.pa_decode_default_splits(dev["k_cache"], wl.num_q_heads) > 0
+    assert sizes[0] == sizes[1] > 0

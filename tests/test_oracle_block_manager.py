@@ -149,3 +149,112 @@ def test_decode_workload_tables_cover_lengths():
             assert len(t) == -(-int(L) // wl.block_size)
         assert len(r["slots"]) == wl.num_new_tokens
         _check_invariants(r["manager"])
+
+
+# ------------------------------------------------------------ prefix caching
+def test_fnv1a64_published_test_vectors():
+    from oracle.block_manager import fnv1a64
+
+    assert fnv1a64(b"") == 0xCBF29CE484222325
+    assert fnv1a64(b"a") == 0xAF63DC4C8601EC8C
+    assert fnv1a64(b"foobar") == 0x85944171F73967E8
+
+
+def test_ten_requests_share_one_copy_of_the_system_prompt(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "prefix_sharing_example.json")))
+    B, n = g["block_size"], g["requests"]
+    rng = np.random.default_rng(0)
+    system = rng.integers(0, 32000, size=g["system_prompt_tokens"]).tolist()
+    m = oracle.OracleBlockManager(4096, B)
+    seqs, cached, own = [], [], 0
+    for i in range(n):
+        suffix = rng.integers(0, 32000, size=int(rng.integers(1, 100))).tolist()
+        s, c = m.new_sequence_cached(system + suffix)
+        seqs.append(s)
+        cached.append(c)
+        own += m.blocks_needed(len(system) + len(suffix)) - g["system_prompt_blocks"]
+    assert cached == [0] + [g["system_prompt_tokens"]] * (n - 1)
+    assert all(m.tables[s][:125] == m.tables[seqs[0]][:125] for s in seqs)
+    assert all(m.ref[b] == n for b in m.tables[seqs[0]][:g["system_prompt_blocks"]])
+    assert m.stats()[1] == g["system_prompt_blocks"] + own  # one copy, not ten
+    _check_invariants(m)
+
+
+def test_prefix_match_is_chained_and_stops_at_the_first_miss():
+    B = 4
+    m = oracle.OracleBlockManager(64, B)
+    a = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13]
+    s0, c0 = m.new_sequence_cached(a)
+    assert c0 == 0
+    # same first and third block, different second block: only block 0 is reused
+    b = [1, 2, 3, 4, 99, 6, 7, 8, 9, 10, 11, 12]
+    s1, c1 = m.new_sequence_cached(b)
+    assert c1 == 4 and m.tables[s1][0] == m.tables[s0][0] and m.tables[s1][2] != m.tables[s0][2]
+    # block 1 of `a` after a different block 0: no hit (the key covers the prefix)
+    s2, c2 = m.new_sequence_cached([0, 0, 0, 0, 5, 6, 7, 8])
+    assert c2 == 0
+    # the partial last block (token 13) was not registered
+    s3, c3 = m.new_sequence_cached(a)
+    assert c3 == 12 and m.tables[s3][3] != m.tables[s0][3]
+    _check_invariants(m)
+
+
+def test_cached_blocks_leave_the_map_when_their_last_user_frees_them():
+    m = oracle.OracleBlockManager(32, 4)
+    p = list(range(8))
+    s0, _ = m.new_sequence_cached(p)
+    s1, c1 = m.new_sequence_cached(p)
+    assert c1 == 8
+    m.free_seq(s0)
+    assert len(m.cached) == 2  # still held by s1
+    m.free_seq(s1)
+    assert len(m.cached) == 0
+    s2, c2 = m.new_sequence_cached(p)
+    assert c2 == 0
+    _check_invariants(m)
+
+
+def test_prefix_cached_failure_changes_nothing():
+    m = oracle.OracleBlockManager(3, 4)
+    m.new_sequence_cached(list(range(8)))
+    before = _state(m), dict(m.cached), m.hits, m.lookups
+    assert m.new_sequence_cached(list(range(8)) + [5] * 8) is None  # needs 2 fresh, 1 free
+    assert (_state(m), dict(m.cached), m.hits, m.lookups) == before
+
+
+@pytest.mark.parametrize("small", [True, False])
+def test_prefix_workload_never_writes_a_shared_block(small):
+    wl = inputs.workload("prefix", small=small)
+    r = oracle.run_script(wl.num_blocks, wl.block_size, wl.free_order, wl.script)
+    assert all(ref == 1 for ref in r["written_refcounts"])
+    assert (r["slots"] == -1).sum() > 0  # some prompt positions were cached
+    np.testing.assert_array_equal(r["lens"], wl.seq_lens)
+    _check_invariants(r["manager"])
+
+
+# -------------------------------------------------------------- beam search
+@pytest.mark.parametrize("small", [True, False])
+def test_beam_search_keeps_copy_on_write_invariants(small):
+    wl = inputs.beam(small)
+    m = oracle.OracleBlockManager(wl.num_blocks, wl.block_size, wl.free_order)
+    B = wl.block_size
+    for st in wl.steps:
+        setup = [op for op in st["ops"] if op[0] != "append"]  # the first step creates the beams
+        appends = [op for op in st["ops"] if op[0] == "append"]
+        oracle.run_script(0, B, None, setup, manager=m)
+        # A shared partly filled block with refcount R written by n of its
+        # holders is copied min(n, R - 1) times (the last holder writes in place).
+        writers, refs = {}, {}
+        for op in appends:
+            if op[0] == "append" and op[1] in m.tables:
+                pos = m.lens[op[1]]
+                if pos % B:
+                    b = m.tables[op[1]][pos // B]
+                    if m.ref[b] > 1:
+                        writers[b] = writers.get(b, 0) + 1
+                        refs[b] = m.ref[b]
+        r = oracle.run_script(0, B, None, appends, manager=m)
+        assert len(r["pairs"]) == sum(min(n, refs[b] - 1) for b, n in writers.items())
+        assert all(ref == 1 for ref in r["written_refcounts"])
+        oracle.run_script(0, B, None, st["select"], manager=m)
+        _check_invariants(m)
