@@ -364,6 +364,26 @@ def oracle_baseline(step, max_groups, threads):
     return ref, pairs, dt, bytes_, len(groups)
 
 
+def allocation_simulator():
+    """Host-side context (not the metric): contiguous max-length reservation
+    against paging with a block-size sweep, on one synthetic stream of 2000
+    requests (Poisson arrivals, lognormal lengths), 200k token slots."""
+    import paged_kv_cache_150_gb300 as pa
+    from paged_kv_cache_150_gb300 import inputs
+
+    a, p, o = inputs.request_stream(7, 2000, 1.0, prompt_median=256, output_median=128, max_prompt=2048,
+                                    max_new_tokens=2048)
+    out = {}
+    runs = [("contiguous", 16)] + [("paged", b) for b in (1, 8, 16, 32, 64, 128)]
+    for policy, b in runs:
+        r = pa.simulate(policy, a, p, o, 200000, block_size=b, max_new_tokens=2048)
+        key = policy if policy == "contiguous" else "paged_b%d" % b
+        out[key] = {"kv_utilization": round(r["utilization"], 4), "peak_running": r["peak_running"],
+                    "steps_to_drain": r["steps"], "preemptions": r["preemptions"],
+                    "waste_tokens_per_seq": round((r["sum_held"] - r["sum_used"]) / max(r["sum_running"], 1), 2)}
+    return out
+
+
 def parity_check(step, ref, pairs):
     import numpy as np
 
@@ -470,6 +490,7 @@ def run_ours(args, rank, world):
             torch.cuda.empty_cache()
         line["workloads"] = extra
     if rank == 0:
+        line["allocation_simulator"] = allocation_simulator()
         print(json.dumps(line), flush=True)
 
 

@@ -325,6 +325,41 @@ pa_status_t pa_bm_cache_stats(const pa_bm_t *bm, int32_t *cached_blocks_out, int
 pa_status_t pa_bm_export(const pa_bm_t *bm, const int32_t *seqs, int32_t n, int32_t max_blocks,
                          int32_t *tables_out, int32_t *lens_out);
 
+/* ------------------------------------------------------------------------
+ * Allocation simulator (host only): contiguous max-length reservation
+ * against paged blocks under one request stream ([PidokuInfra 10] section 10,
+ * exercises B and C; the utilisation contrast of section 2).  One decode step
+ * at a time: arrivals join a FIFO queue; the queue head is admitted while it
+ * fits (contiguous: prompt + max_new_tokens slots in one interval, first fit;
+ * paged: ceil(prompt / B) blocks of the host block manager); every running
+ * request (oldest admission first) generates one token, a paged request
+ * taking a block when its new token starts one, or, if none is free, being
+ * preempted (blocks freed, progress lost, back to the queue front); finished
+ * requests free their memory; the step adds held slots (reservations, or
+ * blocks x B), used slots (tokens stored) and running requests to the totals.
+ * utilization = sum_used / sum_held.
+ * arrival_step must be non-decreasing; lengths >= 1; for the contiguous
+ * policy output_len <= max_new_tokens.
+ * ---------------------------------------------------------------------- */
+typedef enum pa_sim_policy { PA_SIM_CONTIGUOUS = 0, PA_SIM_PAGED = 1 } pa_sim_policy_t;
+
+typedef struct pa_sim_config {
+    int32_t policy;          /* pa_sim_policy_t */
+    int32_t block_size;      /* paged: tokens per block */
+    int32_t max_new_tokens;  /* contiguous: reservation = prompt + max_new_tokens */
+    int32_t max_steps;       /* step limit */
+    int64_t total_slots;     /* token capacity of the pool */
+} pa_sim_config_t;
+
+typedef struct pa_sim_result {
+    int64_t steps, admitted, completed, preemptions, blocked_steps, peak_running;
+    int64_t sum_used, sum_held, sum_running;
+    double utilization;      /* sum_used / sum_held */
+} pa_sim_result_t;
+
+pa_status_t pa_sim_run(const pa_sim_config_t *cfg, const int32_t *arrival_step, const int32_t *prompt_len,
+                       const int32_t *output_len, int32_t num_requests, pa_sim_result_t *out);
+
 #ifdef __cplusplus
 }
 #endif

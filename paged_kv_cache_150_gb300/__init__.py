@@ -369,6 +369,21 @@ class BlockManager:
         return slots, np.asarray(pairs, dtype=np.int32).reshape(-1, 2)
 
 
+def simulate(policy, arrival_step, prompt_len, output_len, total_slots, block_size=16, max_new_tokens=2048,
+             max_steps=10 ** 7):
+    """Run the host allocation simulator (pa_sim_run): policy "contiguous"
+    (max-length reservation) or "paged".  Returns a dict of its totals."""
+    a = np.ascontiguousarray(np.asarray(arrival_step, dtype=np.int32))
+    p = np.ascontiguousarray(np.asarray(prompt_len, dtype=np.int32))
+    o = np.ascontiguousarray(np.asarray(output_len, dtype=np.int32))
+    cfg = _lib.SimConfig(1 if policy == "paged" else 0, int(block_size), int(max_new_tokens), int(max_steps),
+                         int(total_slots))
+    res = _lib.SimResult()
+    _lib.check("pa_sim_run", _lib.load().pa_sim_run(ctypes.byref(cfg), _i32p(a), _i32p(p), _i32p(o), a.shape[0],
+                                                    ctypes.byref(res)))
+    return {name: getattr(res, name) for name, _ in _lib.SimResult._fields_}
+
+
 def version():
     return _lib.load().pa_version().decode()
 
@@ -377,5 +392,5 @@ __all__ = [
     "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_workspace_bytes", "pa_decode_no_alloc",
     "pa_decode_default_splits", "pa_get_device_error", "pa_selftest_wait_timeout", "pa_split_range",
     "pa_split_owner",
-    "BlockManager", "PagedAttentionError", "version",
+    "BlockManager", "PagedAttentionError", "simulate", "version",
 ]

@@ -37,6 +37,18 @@ class CacheDesc(ctypes.Structure):
                 ("dtype", ctypes.c_int32), ("layout", ctypes.c_int32)]
 
 
+class SimConfig(ctypes.Structure):
+    _fields_ = [("policy", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("max_new_tokens", ctypes.c_int32), ("max_steps", ctypes.c_int32),
+                ("total_slots", ctypes.c_int64)]
+
+
+class SimResult(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("steps", "admitted", "completed", "preemptions", "blocked_steps",
+                                              "peak_running", "sum_used", "sum_held", "sum_running")] + \
+               [("utilization", ctypes.c_double)]
+
+
 class DecodeOpts(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int32), ("kernel", ctypes.c_int32),
                 ("ev_partial_begin", ctypes.c_void_p), ("ev_partial_end", ctypes.c_void_p)]
@@ -81,6 +93,7 @@ SIGNATURES = {
     "pa_bm_new_seq_cached": (_I32, [_P, _PI32, _I32, _PI32, _PI32]),
     "pa_bm_slots": (_I32, [_P, _I32, _I32, _I32, _PI32]),
     "pa_bm_cache_stats": (_I32, [_P, _PI32, _PI64, _PI64]),
+    "pa_sim_run": (_I32, [ctypes.POINTER(SimConfig), _PI32, _PI32, _PI32, _I32, ctypes.POINTER(SimResult)]),
 }
 
 _lib = None

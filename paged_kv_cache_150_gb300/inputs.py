@@ -413,3 +413,19 @@ def to_split_layout(k_cache, v_cache):
     k = k_cache.view(nb, bs, hk, d // x, x).permute(0, 2, 3, 1, 4).contiguous()
     v = v_cache.permute(0, 2, 3, 1).contiguous()
     return k, v
+
+
+def request_stream(seed: int, num_requests: int, rate: float, prompt_median: float = 256.0,
+                   output_median: float = 128.0, sigma: float = 1.0, max_prompt: int = 2048,
+                   max_new_tokens: int = 2048):
+    """A synthetic serving stream: Poisson arrivals (``rate`` requests per
+    decode step), lognormal prompt and output lengths (given medians, shape
+    sigma), clipped to [1, max_prompt] and [1, max_new_tokens].  Returns
+    int32 arrays (arrival_step non-decreasing, prompt_len, output_len)."""
+    rng = np.random.default_rng(seed)
+    gaps = rng.exponential(1.0 / rate, size=num_requests)
+    arrival = np.floor(np.cumsum(gaps)).astype(np.int32)
+    prompt = np.clip(np.rint(np.exp(rng.normal(math.log(prompt_median), sigma, size=num_requests))), 1, max_prompt)
+    output = np.clip(np.rint(np.exp(rng.normal(math.log(output_median), sigma, size=num_requests))), 1,
+                     max_new_tokens)
+    return arrival, prompt.astype(np.int32), output.astype(np.int32)
