@@ -45,13 +45,18 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
                                                            int32_t *__restrict__ cu,
                                                            unsigned int *__restrict__ counters,
                                                            int32_t num_counters, T *__restrict__ out,
+                                                           int32_t NG, int32_t C,
+                                                           int32_t *__restrict__ start_seq,
                                                            unsigned int *__restrict__ err) {
     grid_dependency_wait();     // inputs written by earlier work on the stream
     grid_launch_dependents();   // the attention kernel may become resident now
+    constexpr int32_t kSmemCu = 8192;  // prefix sums kept in shared memory for the start search
     __shared__ int32_t warp_incl[32];
     __shared__ int32_t carry;
     __shared__ int32_t n_empty;
     __shared__ int32_t empty_ids[1024];
+    __shared__ int32_t cu_s[kSmemCu];
+    const bool cu_in_smem = N + 1 <= kSmemCu;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
     if (threadIdx.x == 0) carry = 0;
@@ -90,7 +95,10 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
         }
         __syncthreads();
         const int32_t incl = x + (w > 0 ? warp_incl[w - 1] : 0) + carry;
-        if (i < N) cu[i] = incl - nb;
+        if (i < N) {
+            cu[i] = incl - nb;
+            if (cu_in_smem) cu_s[i] = incl - nb;
+        }
         // empty sequences of this pass: their output is zero
         for (int32_t k = 0; k < n_empty; ++k) {
             T *o = out + (int64_t)empty_ids[k] * HD;
@@ -100,56 +108,95 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
         if (threadIdx.x == blockDim.x - 1) carry = incl;
         __syncthreads();
     }
-    if (threadIdx.x == 0) cu[N] = carry;
+    if (threadIdx.x == 0) {
+        cu[N] = carry;
+        if (cu_in_smem) cu_s[N] = carry;
+    }
+    __syncthreads();
+    // Sequence holding the first block of each attention CTA's range, so the
+    // CTA starts without searching cu[].
+    const int32_t *cus = cu_in_smem ? cu_s : cu;
+    const int32_t Wg = cus[N];
+    const int64_t W = (int64_t)NG * Wg;
+    const int32_t Ce = (int32_t)(W < (int64_t)C ? W : (int64_t)C);
+    for (int32_t c = threadIdx.x; c < Ce; c += blockDim.x) {
+        const int32_t r = (int32_t)(split_begin(c, W, Ce) % Wg);
+        int32_t lo = 0, hi = N - 1;  // largest seq with cu[seq] <= r
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            if (cus[mid] <= r)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        start_seq[c] = lo;
+    }
 }
 
 // ------------------------------------------------------------ piece merge
 // Run by the warp that finished the last piece of one (sequence, KV head):
 // merges the pieces held by CTAs c0..c1 for its G query heads.  Lanes split
-// the G heads x D outputs (lane -> head lane / LPH, a contiguous slice of
-// D / LPH elements); one pass over the pieces with a running max, so every
-// load is independent of the previous piece's arithmetic.
-template <typename T, int D>
-__device__ __forceinline__ void merge_pieces(T *__restrict__ out_base, const float2 *__restrict__ ml_ws,
-                                             const float *__restrict__ acc_ws, int32_t c0, int32_t c1,
-                                             int32_t sp, int32_t HPG, int32_t hoff, int32_t G, int lane) {
-    // lanes per head: 32 / (G rounded up to a power of two), at least D/32 elements per lane
-    const int g2 = G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : 8));
-    const int lph = min(32 / g2, D / 4);  // slices of >= 4 elements (float4 loads)
-    const int h = lane / lph;
-    const int part = lane - h * lph;
-    constexpr int EMAX = D / 4;  // elements per lane when lph == 4
-    const int E = D / lph;
+// the G heads x D outputs: LPH lanes per head, each a contiguous slice of
+// E = D / LPH elements.  With LPH a compile-time constant every load of a
+// piece is issued back to back (the merge runs at the end of the kernel, so
+// its L2 latency is on the kernel's critical path); two passes, the maximum
+// over all pieces first, then the weighted sums.
+template <typename T, int D, int LPH>
+__device__ __forceinline__ void merge_pieces_lph(T *__restrict__ out_base, const float2 *__restrict__ ml_ws,
+                                                 const float *__restrict__ acc_ws, int32_t c0, int32_t c1,
+                                                 int32_t sp, int32_t HPG, int32_t hoff, int32_t G, int lane) {
+    constexpr int E = D / LPH;
+    static_assert(E % 4 == 0, "slices are whole float4s");
+    const int h = lane / LPH;
+    const int part = lane % LPH;
     if (h >= G) return;
-    float a[EMAX];
+    const int64_t base = partial_slot(0, sp) * HPG + hoff + h;  // piece c is at base + c * HPG
+    float M = -INFINITY;
+#pragma unroll 8
+    for (int32_t c = c0; c <= c1; ++c) M = fmaxf(M, __ldcg(&ml_ws[base + (int64_t)c * HPG]).x);
+    float a[E];
 #pragma unroll
-    for (int j = 0; j < EMAX; ++j) a[j] = 0.f;
-    float M = -INFINITY, Ls = 0.f;
+    for (int j = 0; j < E; ++j) a[j] = 0.f;
+    float Ls = 0.f;
+#pragma unroll 1
     for (int32_t c = c0; c <= c1; ++c) {
-        const int64_t idx = partial_slot(c, sp) * HPG + hoff + h;
-        const float2 v = __ldcg(&ml_ws[idx]);
+        const int64_t idx = base + (int64_t)c * HPG;
         const float4 *ap = reinterpret_cast<const float4 *>(acc_ws + idx * D + part * E);
-        const float Mn = fmaxf(M, v.x);
-        const float s_old = ex2_approx(M - Mn), s_new = ex2_approx(v.x - Mn);
-        Ls = Ls * s_old + v.y * s_new;
+        float4 x[E / 4];
 #pragma unroll
-        for (int j4 = 0; j4 < EMAX / 4; ++j4) {
-            if (j4 * 4 >= E) break;
-            const float4 x = __ldcg(ap + j4);
-            a[4 * j4 + 0] = fmaf(a[4 * j4 + 0], s_old, s_new * x.x);
-            a[4 * j4 + 1] = fmaf(a[4 * j4 + 1], s_old, s_new * x.y);
-            a[4 * j4 + 2] = fmaf(a[4 * j4 + 2], s_old, s_new * x.z);
-            a[4 * j4 + 3] = fmaf(a[4 * j4 + 3], s_old, s_new * x.w);
+        for (int j4 = 0; j4 < E / 4; ++j4) x[j4] = __ldcg(ap + j4);
+        const float2 v = __ldcg(&ml_ws[idx]);
+        const float wgt = ex2_approx(v.x - M);
+        Ls = fmaf(wgt, v.y, Ls);
+#pragma unroll
+        for (int j4 = 0; j4 < E / 4; ++j4) {
+            a[4 * j4 + 0] = fmaf(wgt, x[j4].x, a[4 * j4 + 0]);
+            a[4 * j4 + 1] = fmaf(wgt, x[j4].y, a[4 * j4 + 1]);
+            a[4 * j4 + 2] = fmaf(wgt, x[j4].z, a[4 * j4 + 2]);
+            a[4 * j4 + 3] = fmaf(wgt, x[j4].w, a[4 * j4 + 3]);
         }
-        M = Mn;
     }
     const float inv = 1.f / Ls;
     T *o = out_base + (int64_t)h * D + part * E;
 #pragma unroll
-    for (int j = 0; j < EMAX; ++j) {
-        if (j >= E) break;
-        store_out(o + j, a[j] * inv);
-    }
+    for (int j = 0; j < E; ++j) store_out(o + j, a[j] * inv);
+}
+
+// Lanes per head: 32 / (G rounded up to a power of two), with slices of at
+// least 4 elements.
+template <typename T, int D>
+__device__ __forceinline__ void merge_pieces(T *__restrict__ out_base, const float2 *__restrict__ ml_ws,
+                                             const float *__restrict__ acc_ws, int32_t c0, int32_t c1,
+                                             int32_t sp, int32_t HPG, int32_t hoff, int32_t G, int lane) {
+    constexpr int kMaxLph = D / 4 < 32 ? D / 4 : 32;
+    if (G > 4)
+        merge_pieces_lph<T, D, 4>(out_base, ml_ws, acc_ws, c0, c1, sp, HPG, hoff, G, lane);
+    else if (G > 2)
+        merge_pieces_lph<T, D, (8 < kMaxLph ? 8 : kMaxLph)>(out_base, ml_ws, acc_ws, c0, c1, sp, HPG, hoff, G, lane);
+    else if (G > 1)
+        merge_pieces_lph<T, D, (16 < kMaxLph ? 16 : kMaxLph)>(out_base, ml_ws, acc_ws, c0, c1, sp, HPG, hoff, G, lane);
+    else
+        merge_pieces_lph<T, D, kMaxLph>(out_base, ml_ws, acc_ws, c0, c1, sp, HPG, hoff, G, lane);
 }
 
 // After a warp wrote its partial for (sequence seq of group g, KV head kvh):
@@ -199,7 +246,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(
     const int32_t *__restrict__ lens, const int32_t *__restrict__ cu, int32_t N, int32_t H,
     int32_t Hk, int32_t G, int32_t B, int32_t NB, int32_t NH, float scale_log2, int32_t C,
     float2 *__restrict__ ml_ws, float *__restrict__ acc_ws, unsigned int *__restrict__ counters,
-    unsigned int *__restrict__ err) {
+    const int32_t *__restrict__ start_seq, unsigned int *__restrict__ err) {
     constexpr int VPL = D / 32;
     grid_dependency_wait();  // the plan kernel's cu[] / lens (programmatic launch)
     const int32_t NG = Hk / NH;
@@ -212,7 +259,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     BlockCursor cur;
-    cur.init(lo, cu, N);
+    cur.init_at(lo, start_seq[c], cu, N);
     float qv[GMAX][VPL], acc[GMAX][VPL], m[GMAX], l[GMAX];
     bool seg_start = true, seg_from_first = false;
     int32_t L = 0;
@@ -334,7 +381,7 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
     const int32_t *__restrict__ tables, int32_t max_blocks, const int32_t *__restrict__ lens,
     const int32_t *__restrict__ cu, int32_t N, int32_t H, int32_t Hk, int32_t G, int32_t NB,
     int32_t NH, float scale_log2, int32_t C, float2 *__restrict__ ml_ws, float *__restrict__ acc_ws,
-    unsigned int *__restrict__ counters, unsigned int *__restrict__ err) {
+    unsigned int *__restrict__ counters, const int32_t *__restrict__ start_seq, unsigned int *__restrict__ err) {
     using Tile = MmaTile<D, B>;
     constexpr int S = Tile::kStages;
     constexpr int KT = D / 16;  // k-steps of q.k and m-tiles of O^T
@@ -372,8 +419,8 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
             prefetch_tmap(&tmk);
             prefetch_tmap(&tmv);
             BlockCursor cur, ahead;
-            cur.init(lo, cu, N);
-            ahead.init(lo, cu, N);
+            cur.init_at(lo, start_seq[c], cu, N);
+            ahead.init_at(lo, start_seq[c], cu, N);
             // Block-table entries are loaded kTablePrefetch blocks ahead of their
             // TMA issue (a register shift ring), so the L2 latency of the table
             // read is off the issue path.
@@ -429,7 +476,7 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
     float o[KT][4];
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     BlockCursor cur;
-    cur.init(lo, cu, N);
+    cur.init_at(lo, start_seq[c], cu, N);
     bool seg_start = true, seg_from_first = false, have_next_q = false;
     // B operand of S^T = K Q^T: column n = query head r of this KV head.
     auto load_q = [&](uint32_t (&dst)[KT][2], int32_t seq, int32_t grp) {
@@ -645,7 +692,7 @@ struct DecodePlan {
     int C;         // persistent CTAs
     size_t smem;   // dynamic shared memory of the attention kernel
     // workspace layout (byte offsets)
-    size_t off_lens, off_cu, off_cnt, off_ml, off_acc, total;
+    size_t off_lens, off_cu, off_cnt, off_start, off_ml, off_acc, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -770,6 +817,8 @@ pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_d
     off = align256(off + sizeof(int32_t) * ((size_t)N + 1));
     p->off_cnt = off;
     off = align256(off + sizeof(uint32_t) * (size_t)std::max(N, 1) * c->num_kv_heads);
+    p->off_start = off;
+    off = align256(off + sizeof(int32_t) * (size_t)C);
     p->off_ml = off;
     off = align256(off + sizeof(float2) * slots * p->HPG);
     p->off_acc = off;
@@ -898,6 +947,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
     int32_t *lens_ws = (int32_t *)(ws + p.off_lens);
     int32_t *cu = (int32_t *)(ws + p.off_cu);
     unsigned int *cnt = (unsigned int *)(ws + p.off_cnt);
+    int32_t *start_seq = (int32_t *)(ws + p.off_start);
     float2 *ml = (float2 *)(ws + p.off_ml);
     float *acc = (float *)(ws + p.off_acc);
     const int G = num_heads / cache->num_kv_heads;
@@ -909,9 +959,9 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
     const int32_t HD = num_heads * cache->head_dim;
     const int32_t ncnt = num_seqs * cache->num_kv_heads;
     {
-        int32_t Nv = num_seqs, Bv = cache->block_size, ml_v = max_len, HDv = HD, nc = ncnt;
+        int32_t Nv = num_seqs, Bv = cache->block_size, ml_v = max_len, HDv = HD, nc = ncnt, NGv = p.NG, Cv = p.C;
         void *outp = out;
-        void *pargs[] = {&seq_lens, &Nv, &Bv, &ml_v, &HDv, &lens_ws, &cu, &cnt, &nc, &outp, &err};
+        void *pargs[] = {&seq_lens, &Nv, &Bv, &ml_v, &HDv, &lens_ws, &cu, &cnt, &nc, &outp, &NGv, &Cv, &start_seq, &err};
         const void *pfn = cache->dtype == PA_BF16 ? (const void *)decode_plan_kernel<__nv_bfloat16>
                                                   : (const void *)decode_plan_kernel<float>;
         if (launch_pdl(pfn, dim3(1), dim3(1024), pargs, 0, s) != cudaSuccess) return PA_ERR_CUDA;
@@ -934,7 +984,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         int32_t Nv = num_seqs, Hv = num_heads, Gv = G, mb = max_blocks_per_seq;
         float sl = scale_log2;
         void *args[] = {&tmk, &tmv, &qb, &ob, &block_tables, &mb, &lens_ws, &cu, &Nv, &Hv, &Hk, &Gv,
-                        &NB, &NHv, &sl, &Cv, &ml, &acc, &cnt, &err};
+                        &NB, &NHv, &sl, &Cv, &ml, &acc, &cnt, &start_seq, &err};
         if (launch_pdl(fn, grid, block, args, p.smem, s) != cudaSuccess) return PA_ERR_CUDA;
     } else {
         const void *fn = simt_kernel_ptr(cache->dtype, cache->head_dim, G, cache->layout);
@@ -944,7 +994,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         int32_t Nv = num_seqs, Hv = num_heads, Gv = G, mb = max_blocks_per_seq, Bv = cache->block_size;
         float sl = scale_log2;
         void *args[] = {&q, &out, &k_cache, &v_cache, &block_tables, &mb, &lens_ws, &cu, &Nv, &Hv, &Hk,
-                        &Gv, &Bv, &NB, &NHv, &sl, &Cv, &ml, &acc, &cnt, &err};
+                        &Gv, &Bv, &NB, &NHv, &sl, &Cv, &ml, &acc, &cnt, &start_seq, &err};
         if (launch_pdl(fn, grid, block, args, 0, s) != cudaSuccess) return PA_ERR_CUDA;
     }
     if (opts && opts->ev_partial_end && cudaEventRecord((cudaEvent_t)opts->ev_partial_end, s) != cudaSuccess)

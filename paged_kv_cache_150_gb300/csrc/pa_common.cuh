@@ -207,6 +207,16 @@ struct BlockCursor {
         nb = cu[seq + 1] - cu[seq];
     }
 
+    // Position at flattened block x when the sequence holding it is known
+    // (from the plan kernel's per-CTA start table): no search.
+    __device__ __forceinline__ void init_at(int64_t x, int32_t s, const int32_t *__restrict__ cu, int32_t N) {
+        const int32_t Wg = cu[N];
+        g = (int32_t)(x / Wg);
+        seq = s;
+        blk = (int32_t)(x - (int64_t)g * Wg) - cu[s];
+        nb = cu[s + 1] - cu[s];
+    }
+
     __device__ __forceinline__ void advance(const int32_t *__restrict__ cu, int32_t N) {
         if (++blk < nb) return;
         blk = 0;
