@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
                                                            unsigned int *__restrict__ err) {
     grid_dependency_wait();     // inputs written by earlier work on the stream
     grid_launch_dependents();   // the attention kernel may become resident now
-    constexpr int32_t kSmemCu = 8192;  // prefix sums kept in shared memory for the start search
+    constexpr int32_t kSmemCu = 2048;  // prefix sums kept in shared memory for the start search
     __shared__ int32_t warp_incl[32];
     __shared__ int32_t carry;
     __shared__ int32_t n_empty;
@@ -418,6 +418,9 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
         if (lane == 0) {
             prefetch_tmap(&tmk);
             prefetch_tmap(&tmv);
+            // KV tiles stream through once: evict them first, so that L2 keeps
+            // the partials, q and tables that are read again.
+            const uint64_t kv_policy = l2_policy_evict_first();
             BlockCursor cur, ahead;
             cur.init_at(lo, start_seq[c], cu, N);
             ahead.init_at(lo, start_seq[c], cu, N);
@@ -454,11 +457,11 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
                 const uint32_t dst = smem_u32(smem + (size_t)s * stage_bytes);
                 mbar_arrive_expect_tx(fb, stage_bytes);
                 if (LAYOUT == PA_LAYOUT_ROW) {
-                    tma_load_4d(dst, &tmk, fb, 0, phys * B, 0, cur.g * NH);
-                    tma_load_4d(dst + tile_bytes, &tmv, fb, 0, phys * B, 0, cur.g * NH);
+                    tma_load_4d_hint(dst, &tmk, fb, 0, phys * B, 0, cur.g * NH, kv_policy);
+                    tma_load_4d_hint(dst + tile_bytes, &tmv, fb, 0, phys * B, 0, cur.g * NH, kv_policy);
                 } else {
-                    tma_load_4d(dst, &tmk, fb, 0, 0, cur.g * NH, phys);
-                    tma_load_4d(dst + tile_bytes, &tmv, fb, 0, 0, cur.g * NH, phys);
+                    tma_load_4d_hint(dst, &tmk, fb, 0, 0, cur.g * NH, phys, kv_policy);
+                    tma_load_4d_hint(dst + tile_bytes, &tmv, fb, 0, 0, cur.g * NH, phys, kv_policy);
                 }
                 cur.advance(cu, N);
             }

@@ -147,6 +147,23 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// Same load with an L2 cache policy (e.g. evict-first for streamed data).
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void *tmap, uint32_t bar, int32_t c0,
+                                                 int32_t c1, int32_t c2, int32_t c3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+        : "memory");
+}
+
+// L2 policy that evicts these lines first: KV tiles are read once per step.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
