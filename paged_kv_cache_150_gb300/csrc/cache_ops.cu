@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     const V *__restrict__ k, const V *__restrict__ v, const int32_t *__restrict__ slots,
     int32_t num_tokens, V *__restrict__ k_cache, V *__restrict__ v_cache, int64_t num_slots,
     int32_t row_vecs, unsigned int *__restrict__ err) {
+    grid_dependency_wait();    // launched programmatically: the previous grid's writes first
     grid_launch_dependents();  // a programmatically launched successor may get resident early
     const int64_t total = (int64_t)num_tokens * row_vecs;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -45,6 +46,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_split_kernel(
     const T *__restrict__ k, const T *__restrict__ v, const int32_t *__restrict__ slots, int32_t num_tokens,
     T *__restrict__ k_cache, T *__restrict__ v_cache, int64_t num_slots, int32_t B, int32_t Hk, int32_t D,
     unsigned int *__restrict__ err) {
+    grid_dependency_wait();
     grid_launch_dependents();
     constexpr int X = 16 / (int)sizeof(T);
     const int64_t per_tok = (int64_t)Hk * D;
@@ -76,6 +78,7 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(V *__restrict__ k_cach
                                                           int32_t num_pairs, int32_t num_blocks,
                                                           int64_t block_vecs, int32_t chunks_per_pair,
                                                           unsigned int *__restrict__ err) {
+    grid_dependency_wait();    // launched programmatically: the previous grid's writes first
     grid_launch_dependents();  // a programmatically launched successor may get resident early
     const int32_t p = blockIdx.x / chunks_per_pair;
     const int32_t chunk = blockIdx.x - p * chunks_per_pair;
@@ -97,6 +100,23 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(V *__restrict__ k_cach
         kd[i] = ks[i];
         vd[i] = vs[i];
     }
+}
+
+// Launch with programmatic stream serialization; the kernels wait for the
+// previous grid (griddepcontrol.wait) before their first memory access, so
+// only the launch and scheduling latency overlaps the previous kernel.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 static int vec_bytes_for(int64_t row_bytes, const void *a, const void *b, const void *c, const void *d) {
@@ -129,14 +149,14 @@ extern "C" pa_status_t pa_reshape_and_cache(const void *k, const void *v, const 
         const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256,
                                                                       (int64_t)std::max(num_sms(), 1) * 16));
         if (cache->dtype == PA_BF16)
-            reshape_and_cache_split_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-                (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, slot_mapping, num_tokens,
-                (__nv_bfloat16 *)k_cache, (__nv_bfloat16 *)v_cache, num_slots, cache->block_size,
-                cache->num_kv_heads, cache->head_dim, err);
+            launch_pdl(reshape_and_cache_split_kernel<__nv_bfloat16>, grid, 256, s, (const __nv_bfloat16 *)k,
+                       (const __nv_bfloat16 *)v, slot_mapping, num_tokens, (__nv_bfloat16 *)k_cache,
+                       (__nv_bfloat16 *)v_cache, num_slots, cache->block_size, cache->num_kv_heads,
+                       cache->head_dim, err);
         else
-            reshape_and_cache_split_kernel<float><<<grid, 256, 0, s>>>(
-                (const float *)k, (const float *)v, slot_mapping, num_tokens, (float *)k_cache, (float *)v_cache,
-                num_slots, cache->block_size, cache->num_kv_heads, cache->head_dim, err);
+            launch_pdl(reshape_and_cache_split_kernel<float>, grid, 256, s, (const float *)k, (const float *)v,
+                       slot_mapping, num_tokens, (float *)k_cache, (float *)v_cache, num_slots, cache->block_size,
+                       cache->num_kv_heads, cache->head_dim, err);
         return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     }
     const int64_t row_bytes = (int64_t)cache->num_kv_heads * cache->head_dim * dtype_bytes(cache->dtype);
@@ -148,24 +168,20 @@ extern "C" pa_status_t pa_reshape_and_cache(const void *k, const void *v, const 
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)std::max(num_sms(), 1) * 16));
     switch (vb) {
         case 16:
-            reshape_and_cache_kernel<uint4><<<grid, threads, 0, s>>>(
-                (const uint4 *)k, (const uint4 *)v, slot_mapping, num_tokens, (uint4 *)k_cache,
-                (uint4 *)v_cache, num_slots, row_vecs, err);
+            launch_pdl(reshape_and_cache_kernel<uint4>, grid, threads, s, (const uint4 *)k, (const uint4 *)v,
+                       slot_mapping, num_tokens, (uint4 *)k_cache, (uint4 *)v_cache, num_slots, row_vecs, err);
             break;
         case 8:
-            reshape_and_cache_kernel<uint2><<<grid, threads, 0, s>>>(
-                (const uint2 *)k, (const uint2 *)v, slot_mapping, num_tokens, (uint2 *)k_cache,
-                (uint2 *)v_cache, num_slots, row_vecs, err);
+            launch_pdl(reshape_and_cache_kernel<uint2>, grid, threads, s, (const uint2 *)k, (const uint2 *)v,
+                       slot_mapping, num_tokens, (uint2 *)k_cache, (uint2 *)v_cache, num_slots, row_vecs, err);
             break;
         case 4:
-            reshape_and_cache_kernel<uint32_t><<<grid, threads, 0, s>>>(
-                (const uint32_t *)k, (const uint32_t *)v, slot_mapping, num_tokens,
-                (uint32_t *)k_cache, (uint32_t *)v_cache, num_slots, row_vecs, err);
+            launch_pdl(reshape_and_cache_kernel<uint32_t>, grid, threads, s, (const uint32_t *)k, (const uint32_t *)v,
+                       slot_mapping, num_tokens, (uint32_t *)k_cache, (uint32_t *)v_cache, num_slots, row_vecs, err);
             break;
         default:
-            reshape_and_cache_kernel<uint16_t><<<grid, threads, 0, s>>>(
-                (const uint16_t *)k, (const uint16_t *)v, slot_mapping, num_tokens,
-                (uint16_t *)k_cache, (uint16_t *)v_cache, num_slots, row_vecs, err);
+            launch_pdl(reshape_and_cache_kernel<uint16_t>, grid, threads, s, (const uint16_t *)k, (const uint16_t *)v,
+                       slot_mapping, num_tokens, (uint16_t *)k_cache, (uint16_t *)v_cache, num_slots, row_vecs, err);
             break;
     }
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -193,24 +209,20 @@ extern "C" pa_status_t pa_copy_blocks(void *k_cache, void *v_cache, const pa_cac
     cudaStream_t s = (cudaStream_t)stream;
     switch (vb) {
         case 16:
-            copy_blocks_kernel<uint4><<<grid, threads, 0, s>>>((uint4 *)k_cache, (uint4 *)v_cache,
-                                                               src_dst_pairs, num_pairs,
-                                                               cache->num_blocks, block_vecs, chunks, err);
+            launch_pdl(copy_blocks_kernel<uint4>, grid, threads, s, (uint4 *)k_cache, (uint4 *)v_cache,
+                       src_dst_pairs, num_pairs, cache->num_blocks, block_vecs, chunks, err);
             break;
         case 8:
-            copy_blocks_kernel<uint2><<<grid, threads, 0, s>>>((uint2 *)k_cache, (uint2 *)v_cache,
-                                                               src_dst_pairs, num_pairs,
-                                                               cache->num_blocks, block_vecs, chunks, err);
+            launch_pdl(copy_blocks_kernel<uint2>, grid, threads, s, (uint2 *)k_cache, (uint2 *)v_cache,
+                       src_dst_pairs, num_pairs, cache->num_blocks, block_vecs, chunks, err);
             break;
         case 4:
-            copy_blocks_kernel<uint32_t><<<grid, threads, 0, s>>>(
-                (uint32_t *)k_cache, (uint32_t *)v_cache, src_dst_pairs, num_pairs, cache->num_blocks,
-                block_vecs, chunks, err);
+            launch_pdl(copy_blocks_kernel<uint32_t>, grid, threads, s, (uint32_t *)k_cache, (uint32_t *)v_cache,
+                       src_dst_pairs, num_pairs, cache->num_blocks, block_vecs, chunks, err);
             break;
         default:
-            copy_blocks_kernel<uint16_t><<<grid, threads, 0, s>>>(
-                (uint16_t *)k_cache, (uint16_t *)v_cache, src_dst_pairs, num_pairs, cache->num_blocks,
-                block_vecs, chunks, err);
+            launch_pdl(copy_blocks_kernel<uint16_t>, grid, threads, s, (uint16_t *)k_cache, (uint16_t *)v_cache,
+                       src_dst_pairs, num_pairs, cache->num_blocks, block_vecs, chunks, err);
             break;
     }
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
