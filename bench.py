@@ -340,6 +340,44 @@ def time_e2e(step, steps):
     return statistics.mean(times), h2d, d2h
 
 
+def time_write_copy(step, iters, peak):
+    """The cache write and the block copy timed on their own (CUDA events
+    around each call, median), reported as GB/s of bytes read + written.  A
+    512 MiB buffer is READ before each timed call, so the call's source rows
+    are not in L2 and no dirty line of the flush is written back inside it."""
+    import torch
+
+    pa, v, wl = step.pa, step.vals, step.wl
+    row = wl.num_kv_heads * wl.head_dim * wl.elem_bytes
+    rows = int((step.host["slots"] >= 0).sum())
+    npairs = int(step.host["pairs"].shape[0])
+    flush = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    calls = {"cache_write": (lambda: pa.pa_reshape_and_cache(v["k"], v["v"], step.slots, v["k_cache"], v["v_cache"]),
+                             2 * 2 * rows * row + 4 * int(step.slots.numel()), rows)}
+    if npairs:
+        calls["block_copy"] = (lambda: pa.pa_copy_blocks(v["k_cache"], v["v_cache"], step.pairs),
+                               2 * 2 * npairs * wl.block_size * row + 8 * npairs, npairs)
+    out = {}
+    for name, (fn, nbytes, units) in calls.items():
+        for _ in range(3):
+            fn()
+        ev = _events(iters)
+        for i in range(iters):
+            flush.sum()
+            ev[i][0].record()
+            fn()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        pa.pa_get_device_error()
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"us": round(ms * 1e3, 2), "bytes_read_written": nbytes,
+                     ("rows" if name == "cache_write" else "pairs"): units,
+                     "gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4)}
+    del flush
+    return out
+
+
 def oracle_baseline(step, max_groups, threads):
     """The CPU oracle, as it stands, on a bounded sample of the workload:
     whole (sequence, KV head) groups, all G query heads of each."""
@@ -424,6 +462,7 @@ def run_ours(args, rank, world):
     achieved = step.kernel_bytes / (kern_avg_ms / 1e3) / 1e9
     traffic, _ = profiled_traffic(workload_name(step))
 
+    write_copy = time_write_copy(step, 50, peak)
     if args.no_e2e:
         e2e = None
     else:
@@ -452,6 +491,7 @@ def run_ours(args, rank, world):
         "gpu_launches": step.kernel_launches * args.steps,
         "clocks": clocks,
         "block_manager_ms": round(step.bm_ms, 3),
+        "write_copy": write_copy,
     }
     if do_cpu:
         import oracle
@@ -485,7 +525,8 @@ def run_ours(args, rank, world):
                                  "cow_pairs": int(st.host["pairs"].shape[0]), "new_tokens": st.wl.num_new_tokens,
                                  "unique_block_bytes": st.unique_block_bytes,
                                  "written_rows": int((st.host["slots"] >= 0).sum()),
-                                 "cache_layout": st.layout}
+                                 "cache_layout": st.layout,
+                                 "write_copy": time_write_copy(st, 50, peak)}
             del st
             torch.cuda.empty_cache()
         line["workloads"] = extra

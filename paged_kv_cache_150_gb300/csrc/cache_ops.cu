@@ -13,28 +13,70 @@
 
 namespace pa {
 
+// Row copy by one warp: every lane issues its loads of the K and V rows
+// (kUnroll vectors of each) before its stores, so a row is one memory round
+// trip.
+constexpr int kUnroll = 4;
+
 template <typename V>
-__global__ void __launch_bounds__(256) reshape_and_cache_kernel(
+__device__ __forceinline__ void warp_copy_rows(V *__restrict__ kd, V *__restrict__ vd, const V *__restrict__ ks,
+                                               const V *__restrict__ vs, int64_t n, int lane, bool streaming) {
+    for (int64_t j0 = 0; j0 < n; j0 += 32 * kUnroll) {
+        V kx[kUnroll], vx[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t j = j0 + u * 32 + lane;
+            if (j < n) {
+                kx[u] = streaming ? __ldcs(ks + j) : ks[j];
+                vx[u] = streaming ? __ldcs(vs + j) : vs[j];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t j = j0 + u * 32 + lane;
+            if (j < n) {
+                kd[j] = kx[u];
+                vd[j] = vx[u];
+            }
+        }
+    }
+}
+
+// A row is cut into NC chunks of 32 * kUnroll vectors; warp w copies chunk
+// w % NC of the tokens w / NC, w / NC + NWt, w / NC + 2 NWt, ... (NWt = warps
+// per chunk), 32 tokens at a time.  The 32 slots come in one load, and padding
+// tokens (slot < 0, e.g. prompt positions already in the prefix cache) are
+// dropped by a ballot without touching their rows.
+template <typename V>
+__global__ void __launch_bounds__(256, 4) reshape_and_cache_kernel(
     const V *__restrict__ k, const V *__restrict__ v, const int32_t *__restrict__ slots,
     int32_t num_tokens, V *__restrict__ k_cache, V *__restrict__ v_cache, int64_t num_slots,
     int32_t row_vecs, unsigned int *__restrict__ err) {
     grid_dependency_wait();    // launched programmatically: the previous grid's writes first
     grid_launch_dependents();  // a programmatically launched successor may get resident early
-    const int64_t total = (int64_t)num_tokens * row_vecs;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const int32_t t = (int32_t)(i / row_vecs);
-        const int32_t j = (int32_t)(i - (int64_t)t * row_vecs);
-        const int32_t s = __ldg(slots + t);
-        if (s < 0) continue;  // padding token
-        if ((int64_t)s >= num_slots) {
-            if (j == 0) atomicOr(err, kErrBounds);
-            continue;
+    constexpr int kChunk = 32 * kUnroll;
+    const int lane = threadIdx.x & 31;
+    const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int32_t NC = (row_vecs + kChunk - 1) / kChunk;
+    const int64_t NWt = (((int64_t)gridDim.x * blockDim.x) >> 5) / NC;
+    const int64_t wt = w / NC;
+    if (wt >= NWt) return;
+    const int64_t j0 = (w - wt * NC) * kChunk;
+    const int64_t n = min((int64_t)kChunk, (int64_t)row_vecs - j0);
+    for (int64_t t0 = wt; t0 < num_tokens; t0 += 32 * NWt) {
+        const int64_t tl = t0 + (int64_t)lane * NWt;
+        const int32_t sl = tl < num_tokens ? __ldg(slots + tl) : -1;
+        const bool bad = (int64_t)sl >= num_slots;
+        if (__any_sync(0xffffffffu, bad) && lane == 0 && j0 == 0) atomicOr(err, kErrBounds);
+        unsigned int todo = __ballot_sync(0xffffffffu, sl >= 0 && !bad);
+        while (todo) {
+            const int b = __ffs(todo) - 1;
+            todo &= todo - 1;
+            const int64_t s = __shfl_sync(0xffffffffu, sl, b);
+            const int64_t t = t0 + (int64_t)b * NWt;
+            warp_copy_rows(k_cache + s * row_vecs + j0, v_cache + s * row_vecs + j0, k + t * row_vecs + j0,
+                           v + t * row_vecs + j0, n, lane, true);
         }
-        const int64_t dst = (int64_t)s * row_vecs + j;
-        const int64_t src = (int64_t)t * row_vecs + j;
-        k_cache[dst] = __ldcs(k + src);
-        v_cache[dst] = __ldcs(v + src);
     }
 }
 
@@ -92,14 +134,12 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(V *__restrict__ k_cach
     const int64_t per_chunk = (block_vecs + chunks_per_pair - 1) / chunks_per_pair;
     const int64_t lo = chunk * per_chunk;
     const int64_t hi = min(block_vecs, lo + per_chunk);
-    const V *ks = k_cache + (int64_t)src * block_vecs;
-    const V *vs = v_cache + (int64_t)src * block_vecs;
-    V *kd = k_cache + (int64_t)dst * block_vecs;
-    V *vd = v_cache + (int64_t)dst * block_vecs;
-    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
-        kd[i] = ks[i];
-        vd[i] = vs[i];
-    }
+    const int64_t ks = (int64_t)src * block_vecs, kd = (int64_t)dst * block_vecs;
+    // The CTA's warps take consecutive 32 * kUnroll-vector pieces of the chunk.
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    for (int64_t j = lo + (int64_t)warp * 32 * kUnroll; j < hi; j += (int64_t)nwarps * 32 * kUnroll)
+        warp_copy_rows(k_cache + kd + j, v_cache + kd + j, k_cache + ks + j, v_cache + ks + j,
+                       min((int64_t)32 * kUnroll, hi - j), lane, false);
 }
 
 // Launch with programmatic stream serialization; the kernels wait for the
@@ -162,10 +202,13 @@ extern "C" pa_status_t pa_reshape_and_cache(const void *k, const void *v, const 
     const int64_t row_bytes = (int64_t)cache->num_kv_heads * cache->head_dim * dtype_bytes(cache->dtype);
     const int vb = vec_bytes_for(row_bytes, k, v, k_cache, v_cache);
     const int32_t row_vecs = (int32_t)(row_bytes / vb);
-    const int64_t total = (int64_t)num_tokens * row_vecs;
+    // One warp per (token, row chunk) up to 32 warps (4 resident CTAs of 256
+    // threads) per SM.
     const int threads = 256;
-    const int64_t want = (total + threads - 1) / threads;
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)std::max(num_sms(), 1) * 16));
+    const int64_t chunks = (row_vecs + 32 * kUnroll - 1) / (32 * kUnroll);
+    const int64_t token_warps =
+        std::min<int64_t>(num_tokens, std::max<int64_t>(1, (int64_t)std::max(num_sms(), 1) * 32 / chunks));
+    const int grid = (int)std::max<int64_t>(1, (token_warps * chunks + 7) / 8);
     switch (vb) {
         case 16:
             launch_pdl(reshape_and_cache_kernel<uint4>, grid, threads, s, (const uint4 *)k, (const uint4 *)v,
@@ -202,8 +245,9 @@ extern "C" pa_status_t pa_copy_blocks(void *k_cache, void *v_cache, const pa_cac
     const int vb = vec_bytes_for(block_bytes, k_cache, v_cache, k_cache, v_cache);
     const int64_t block_vecs = block_bytes / vb;
     const int threads = 256;
-    // ~8 KiB of each tensor per CTA, at least one CTA per pair
-    int32_t chunks = (int32_t)std::max<int64_t>(1, (block_vecs * vb + 8191) / 8192);
+    // 16 KiB of each tensor per CTA (8 warps x 32 lanes x kUnroll 16-byte
+    // vectors: one round trip), at least one CTA per pair
+    int32_t chunks = (int32_t)std::max<int64_t>(1, (block_vecs * vb + 16383) / 16384);
     if ((int64_t)num_pairs * chunks > INT32_MAX) chunks = INT32_MAX / num_pairs;
     const int grid = num_pairs * chunks;
     cudaStream_t s = (cudaStream_t)stream;

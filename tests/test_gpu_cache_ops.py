@@ -48,8 +48,9 @@ def _cache(nb, bs, hk, d, dtype, seed):
             torch.randn(nb, bs, hk, d, generator=g, device="cuda").to(dtype))
 
 
-@pytest.mark.parametrize("hk,d,dtype", [(2, 3, torch.bfloat16), (1, 6, torch.float32), (8, 128, torch.bfloat16), (1, 3, torch.bfloat16),
-                                        (3, 4, torch.bfloat16)])
+@pytest.mark.parametrize("hk,d,dtype", [(2, 3, torch.bfloat16), (1, 6, torch.float32), (8, 128, torch.bfloat16),
+                                        (1, 3, torch.bfloat16), (3, 4, torch.bfloat16), (8, 256, torch.bfloat16),
+                                        (8, 128, torch.float32), (5, 104, torch.bfloat16)])
 def test_write_any_row_width_and_padding_slots(hk, d, dtype):
     nb, bs = 5, 4
     kc, vc = _cache(nb, bs, hk, d, dtype, 1)
@@ -95,3 +96,25 @@ def test_copy_of_many_pairs():
     pa.pa_copy_blocks(kc, vc, torch.stack([src, dst], 1).cuda())
     assert pa.pa_get_device_error(raise_on_error=False) == 0
     assert torch.equal(kc, ref_k) and torch.equal(vc, ref_v)
+
+
+def test_write_many_tokens_several_grid_passes():
+    """More tokens than one pass of the write's grid covers (32 tokens per warp
+    per pass), a third of them padding, each row one 16-byte vector."""
+    T, nslots, hk, d = 400_000, 500_000, 1, 8
+    bs = 16
+    kc, vc = _cache(nslots // bs, bs, hk, d, torch.bfloat16, 5)
+    g = torch.Generator(device="cuda").manual_seed(6)
+    k = torch.randn(T, hk, d, generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn(T, hk, d, generator=g, device="cuda").to(torch.bfloat16)
+    rng = np.random.default_rng(7)
+    slots = rng.permutation(nslots)[:T].astype(np.int32)
+    slots[rng.random(T) < 1 / 3] = -1
+    slots_d = torch.from_numpy(slots).cuda()
+    ref_k, ref_v = kc.clone().view(-1, hk, d), vc.clone().view(-1, hk, d)
+    keep = slots_d >= 0
+    ref_k[slots_d[keep].long()] = k[keep]
+    ref_v[slots_d[keep].long()] = v[keep]
+    pa.pa_reshape_and_cache(k, v, slots_d, kc, vc)
+    assert pa.pa_get_device_error(raise_on_error=False) == 0
+    assert torch.equal(kc.view(-1, hk, d), ref_k) and torch.equal(vc.view(-1, hk, d), ref_v)

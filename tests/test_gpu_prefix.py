@@ -28,5 +28,8 @@ def test_prefix_cached_full_size_sampled():
     r = oracle_step(wl, host)
     g = gpu_step(wl, dev)
     assert (g["host_slots"] == -1).sum() == 144000  # 9000 cached blocks of 16 positions
+    np.testing.assert_array_equal(g["host_slots"], r["slots"])
+    assert np.array_equal(inputs.to_numpy_elems(g["k_cache"]), r["k_cache"])
+    assert np.array_equal(inputs.to_numpy_elems(g["v_cache"]), r["v_cache"])
     pairs = sample_pairs(wl, 64)
     assert max_abs_err(g["out"], oracle_decode(wl, host, r, pairs=pairs), pairs) <= TOL["bf16"]
