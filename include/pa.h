@@ -51,7 +51,8 @@ typedef enum pa_status {
     PA_ERR_NO_BLOCKS = -4,      /* block manager: the free list cannot satisfy the request */
     PA_ERR_DEVICE_BOUNDS = -5,  /* a kernel met an index outside the pool or the table */
     PA_ERR_DEVICE_TIMEOUT = -6, /* a kernel's bounded wait on an mbarrier ran out */
-    PA_ERR_WORKSPACE = -7       /* the decode workspace is smaller than required */
+    PA_ERR_WORKSPACE = -7,      /* the decode workspace is smaller than required */
+    PA_ERR_DEVICE_PLAN = -8     /* a shared-prefix plan does not match its decode call */
 } pa_status_t;
 
 typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1 } pa_dtype_t;
@@ -169,6 +170,7 @@ typedef struct pa_decode_opts {
     int32_t kernel;     /* pa_kernel_t */
     pa_event_t ev_partial_begin; /* optional: recorded just before the attention kernel */
     pa_event_t ev_partial_end;   /* optional: recorded just after the attention kernel */
+    const int32_t *shared_plan;  /* optional device copy of a pa_shared_plan_build plan (NULL = none) */
 } pa_decode_opts_t;
 
 size_t pa_decode_workspace_bytes(const pa_cache_desc_t *cache, int32_t num_seqs, int32_t num_heads,
@@ -214,6 +216,60 @@ pa_status_t pa_decode_no_alloc(void *out, const void *q, const void *k_cache, co
                                int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
                                int32_t num_heads, float scale, const pa_decode_opts_t *opts,
                                pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Shared-prefix decode plan.
+ *
+ * Sequences forked from one prompt (parallel sampling, beam search) or
+ * matched in the prefix cache point at the same physical blocks
+ * ([PidokuInfra 10] section 5 "Copy-on-write sharing": one copy of the
+ * prompt's blocks with refcount n, and "The relationship to prefix caching";
+ * [tokentrails] step 4: shared blocks with reference counts).  Attention over a shared block is the same K and V for every
+ * sharer, only the queries differ.  With a plan, pa_decode reads each shared
+ * block once and applies it to the query heads of all sharers; each
+ * sequence's own blocks are read as before, and the two kinds of partial
+ * result are merged by the same rescaling reduce.  The output is the same
+ * attention (within the tolerance of a different summation order).
+ *
+ * pa_shared_plan_build works on the HOST copies of one batch's block tables
+ * and lengths (the ones that will be passed to pa_decode).  A group is two or
+ * more sequences whose tables start with the same physical block; its shared
+ * prefix is the longest run of leading blocks that every member has in
+ * common, cut so that every member keeps at least one position of its own
+ * after it (P * B < seq_lens[i]).  Groups with P < min_shared_blocks are
+ * dropped.  Sharing needs H / Hk in {1, 2, 4, 8}; for other ratios the plan
+ * holds no group (info->num_groups = 0) and pa_decode runs as without one.
+ *
+ * plan       host int32 buffer of at least pa_shared_plan_ints(num_seqs)
+ *            elements (written).  Copy it to the device unchanged and pass
+ *            its device address in pa_decode_opts_t.shared_plan, with the
+ *            same tables, lengths and head counts.  The device checks the
+ *            plan's header (sizes, heads per KV head, block size) and that
+ *            every member keeps a position of its own; a mismatch records
+ *            PA_ERR_DEVICE_PLAN and the affected sequences (or, for a bad
+ *            header, all of them) are computed without sharing.  Whether the
+ *            members' table entries really are equal is NOT re-checked on the
+ *            device: a plan built from other tables gives wrong results.
+ * info       optional (NULL allowed): groups, member sequences, shared blocks.
+ * Returns PA_ERR_INVALID_ARG for bad sizes or null pointers, or when a
+ * length is outside [0, max_blocks_per_seq * B].
+ * The tensor-core kernel uses the plan when Hk is a multiple of 4, the launch
+ * has at least 2 CTAs and q is 16-byte aligned; otherwise (and in the
+ * CUDA-core kernel) the plan is ignored and the call runs without sharing.
+ * ---------------------------------------------------------------------- */
+typedef struct pa_shared_plan_info {
+    int32_t num_groups;    /* groups of >= 2 sequences sharing a prefix */
+    int32_t num_members;   /* sequences in groups */
+    int64_t shared_blocks; /* sum over groups of their shared prefix blocks */
+    int64_t saved_blocks;  /* block reads (per KV head) saved per decode: sum of (members - passes) * P */
+} pa_shared_plan_info_t;
+
+size_t pa_shared_plan_ints(int32_t num_seqs);
+
+pa_status_t pa_shared_plan_build(const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *seq_lens, int32_t num_seqs, int32_t block_size,
+                                 int32_t num_heads, int32_t num_kv_heads, int32_t min_shared_blocks,
+                                 int32_t *plan, size_t plan_ints, pa_shared_plan_info_t *info);
 
 /* Number of CTAs a default (num_splits = 0) decode launch uses on the current
  * device for this shape, or a negative pa_status_t. */

@@ -103,8 +103,10 @@ def pa_copy_blocks(k_cache, v_cache, src_dst_pairs):
     _lib.check("pa_copy_blocks", st)
 
 
-def _opts(num_splits, kernel, events):
-    o = _lib.DecodeOpts(int(num_splits), _KERNELS[kernel], None, None)
+def _opts(num_splits, kernel, events, shared_plan=None):
+    o = _lib.DecodeOpts(int(num_splits), _KERNELS[kernel], None, None, None)
+    if shared_plan is not None:
+        o.shared_plan = _dev(shared_plan, "shared_plan", _torch().int32).value
     if events is not None:
         for e in events:
             if not e.cuda_event:  # torch creates the CUDA event on its first record
@@ -122,9 +124,13 @@ def _cache_desc_from_k(k_cache):
     return _cache_desc(k_cache, k_cache)
 
 
-def pa_decode_workspace_bytes(k_cache, num_seqs, num_heads, num_splits=0, kernel="auto"):
+def pa_decode_workspace_bytes(k_cache, num_seqs, num_heads, num_splits=0, kernel="auto", shared=False):
+    """Workspace bytes of pa_decode; ``shared`` sizes it for a call with a
+    shared-prefix plan."""
     desc = _cache_desc_from_k(k_cache)
     o = _opts(num_splits, kernel, None)
+    if shared:
+        o.shared_plan = ctypes.c_void_p(1)  # only tested for NULL when sizing
     n = _lib.load().pa_decode_workspace_bytes(ctypes.byref(desc), int(num_seqs), int(num_heads),
                                               ctypes.byref(o))
     if n == 0:
@@ -142,11 +148,13 @@ def pa_decode_default_splits(k_cache, num_heads, kernel="auto"):
 
 
 def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None, workspace=None,
-              num_splits=0, kernel="auto", events=None):
+              num_splits=0, kernel="auto", events=None, shared_plan=None):
     """Decode attention through block tables; returns ``out`` [N, H, D].
 
     ``events``: optional (begin, end) torch.cuda.Event pair recorded around the
-    attention kernel on the current stream."""
+    attention kernel on the current stream.  ``shared_plan``: optional device
+    int32 tensor from shared_prefix_plan (built from the same tables and
+    lengths), so that blocks shared by several sequences are read once."""
     torch = _torch()
     desc = _cache_desc(k_cache, v_cache)
     N, H, D = q.shape
@@ -158,7 +166,7 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None, work
         out = torch.empty_like(q)
     elif out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("out must match q")
-    o = _opts(num_splits, kernel, events)
+    o = _opts(num_splits, kernel, events, shared_plan)
     lib = _lib.load()
     need = lib.pa_decode_workspace_bytes(ctypes.byref(desc), N, H, ctypes.byref(o))
     if need == 0:
@@ -172,6 +180,29 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None, work
                        ctypes.byref(o), _stream())
     _lib.check("pa_decode", st)
     return out
+
+
+def shared_prefix_plan(block_tables, seq_lens, block_size, num_heads, num_kv_heads, min_shared_blocks=1):
+    """Shared-prefix plan of one batch from HOST tables [N, max_blocks] and
+    lengths [N] (numpy or CPU tensors): sequences whose tables start with the
+    same physical blocks, and their common prefix.  Returns (plan, info):
+    plan is a CPU int32 tensor to copy to the device and pass to pa_decode
+    as ``shared_plan``; info is a dict (num_groups, num_members,
+    shared_blocks, saved_blocks)."""
+    torch = _torch()
+    t = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    L = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    if t.ndim != 2 or L.shape != (t.shape[0],):
+        raise ValueError("block_tables must be [num_seqs, max_blocks] and seq_lens [num_seqs]")
+    lib = _lib.load()
+    n = int(lib.pa_shared_plan_ints(t.shape[0]))
+    plan = np.zeros(n, dtype=np.int32)
+    info = _lib.SharedPlanInfo()
+    st = lib.pa_shared_plan_build(_i32p(t), t.shape[1], _i32p(L), t.shape[0], int(block_size), int(num_heads),
+                                  int(num_kv_heads), int(min_shared_blocks), _i32p(plan), n, ctypes.byref(info))
+    _lib.check("pa_shared_plan_build", st)
+    return torch.from_numpy(plan), {"num_groups": info.num_groups, "num_members": info.num_members,
+                                    "shared_blocks": info.shared_blocks, "saved_blocks": info.saved_blocks}
 
 
 def pa_decode_no_alloc(q, k_cache, v_cache, block_tables, seq_lens, scale, out, num_splits=0, kernel="auto"):

@@ -16,6 +16,7 @@ PA_ERR_NO_BLOCKS = -4
 PA_ERR_DEVICE_BOUNDS = -5
 PA_ERR_DEVICE_TIMEOUT = -6
 PA_ERR_WORKSPACE = -7
+PA_ERR_DEVICE_PLAN = -8
 
 PA_F32 = 0
 PA_BF16 = 1
@@ -51,7 +52,13 @@ class SimResult(ctypes.Structure):
 
 class DecodeOpts(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int32), ("kernel", ctypes.c_int32),
-                ("ev_partial_begin", ctypes.c_void_p), ("ev_partial_end", ctypes.c_void_p)]
+                ("ev_partial_begin", ctypes.c_void_p), ("ev_partial_end", ctypes.c_void_p),
+                ("shared_plan", ctypes.c_void_p)]
+
+
+class SharedPlanInfo(ctypes.Structure):
+    _fields_ = [("num_groups", ctypes.c_int32), ("num_members", ctypes.c_int32),
+                ("shared_blocks", ctypes.c_int64), ("saved_blocks", ctypes.c_int64)]
 
 
 # symbol -> (restype, argtypes)
@@ -65,6 +72,9 @@ _OPTS = ctypes.POINTER(DecodeOpts)
 
 SIGNATURES = {
     "pa_status_string": (ctypes.c_char_p, [_I32]),
+    "pa_shared_plan_ints": (ctypes.c_size_t, [_I32]),
+    "pa_shared_plan_build": (_I32, [_PI32, _I32, _PI32, _I32, _I32, _I32, _I32, _I32, _PI32, ctypes.c_size_t,
+                                    ctypes.POINTER(SharedPlanInfo)]),
     "pa_version": (ctypes.c_char_p, []),
     "pa_reshape_and_cache": (_I32, [_P, _P, _P, _I32, _P, _P, _DESC, _P]),
     "pa_copy_blocks": (_I32, [_P, _P, _DESC, _P, _I32, _P]),

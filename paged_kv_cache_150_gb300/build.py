@@ -14,7 +14,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBRARY = os.path.join(HERE, "libpa.so")
-SOURCES = ["pa_api.cu", "cache_ops.cu", "decode.cu", "block_manager.cpp", "simulator.cpp"]
+SOURCES = ["pa_api.cu", "cache_ops.cu", "decode.cu", "block_manager.cpp", "simulator.cpp", "shared_plan.cpp"]
 HEADERS = ["pa_common.cuh", "pa_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

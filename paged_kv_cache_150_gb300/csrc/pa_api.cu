@@ -65,6 +65,7 @@ extern "C" const char *pa_status_string(pa_status_t status) {
         case PA_ERR_DEVICE_BOUNDS: return "kernel met an index outside the pool or table";
         case PA_ERR_DEVICE_TIMEOUT: return "kernel wait timed out";
         case PA_ERR_WORKSPACE: return "workspace too small";
+        case PA_ERR_DEVICE_PLAN: return "shared-prefix plan does not match the decode call";
     }
     return "unknown status";
 }
@@ -82,6 +83,7 @@ extern "C" pa_status_t pa_get_device_error(pa_stream_t stream) {
     if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
     if (word & kErrTimeout) return PA_ERR_DEVICE_TIMEOUT;
     if (word & (kErrBounds | kErrLength)) return PA_ERR_DEVICE_BOUNDS;
+    if (word & kErrPlan) return PA_ERR_DEVICE_PLAN;
     return PA_OK;
 }
 

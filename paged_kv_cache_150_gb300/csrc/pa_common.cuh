@@ -18,6 +18,7 @@ enum : unsigned int {
     kErrBounds = 1u,   // slot / table entry / block id outside the pool
     kErrLength = 2u,   // sequence length outside [0, max_blocks * B]
     kErrTimeout = 4u,  // a bounded mbarrier wait ran out
+    kErrPlan = 8u,     // a shared-prefix plan that does not match its decode call
 };
 
 // Bound on any single mbarrier wait (nanoseconds of %globaltimer).
@@ -52,6 +53,62 @@ __host__ __device__ __forceinline__ int32_t split_owner(int64_t x, int64_t W, in
 __host__ __device__ __forceinline__ int64_t partial_slot(int32_t c, int32_t sp) {
     return (int64_t)c + sp;
 }
+
+// ------------------------------------------------------- shared-prefix plan
+// Packed int32 words written by pa_shared_plan_build, read by the decode
+// plan and attention kernels:
+//   header[kPlanHeader] = {magic, N, G, B, groups, members, V, R}
+//   seq_group[N]  seq_member[N]  group_prefix[groups]  group_vbase[groups + 1]
+//   group_begin[groups + 1]  members[members]  vgroup[V]  cu_s[V + 1]
+// A group's sharers contribute G query rows each (member m: rows m*G ..
+// m*G + G - 1); the rows are cut into passes of R = kPlanRows, and each pass
+// is one "virtual sequence" v over the group's P shared blocks (cu_s = prefix
+// sums of P over virtual sequences).  A stage of a shared-prefix CTA holds
+// kPlanHeads KV heads, one per consumer warp, and each warp applies it to the
+// pass's 16 rows of its head (two 8-column MMA tiles).  G divides 8, so a
+// member's rows never straddle an MMA tile or a pass.
+constexpr int32_t kPlanMagic = 0x50415350;
+constexpr int kPlanHeader = 8;
+constexpr int kPlanRows = 16;                            // query rows per pass
+constexpr int kPlanHeads = 4;                            // KV heads per shared-prefix stage
+constexpr int kPlanSlotRows = kPlanHeads * kPlanRows;    // rows of one shared-prefix partial slot
+
+struct PlanView {
+    const int32_t *seq_group, *seq_member, *group_prefix, *group_vbase, *group_begin, *members, *vgroup, *cu_s;
+    int32_t N, G, B, groups, M, V, R;
+
+    __host__ __device__ __forceinline__ static int64_t words(int32_t N, int32_t groups, int32_t M, int32_t V) {
+        return (int64_t)kPlanHeader + 2 * (int64_t)N + 3 * (int64_t)groups + 2 + M + 2 * (int64_t)V + 1;
+    }
+    // Pointers into the words; the header's counts must be validated first.
+    __host__ __device__ __forceinline__ static PlanView at(const int32_t *w) {
+        PlanView p;
+        p.N = w[1];
+        p.G = w[2];
+        p.B = w[3];
+        p.groups = w[4];
+        p.M = w[5];
+        p.V = w[6];
+        p.R = w[7];
+        const int32_t *x = w + kPlanHeader;
+        p.seq_group = x;
+        x += p.N;
+        p.seq_member = x;
+        x += p.N;
+        p.group_prefix = x;
+        x += p.groups;
+        p.group_vbase = x;
+        x += p.groups + 1;
+        p.group_begin = x;
+        x += p.groups + 1;
+        p.members = x;
+        x += p.M;
+        p.vgroup = x;
+        x += p.V;
+        p.cu_s = x;
+        return p;
+    }
+};
 
 // ------------------------------------------------------------- small helpers
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
@@ -205,8 +262,10 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 struct BlockCursor {
     int32_t g, seq, blk;
     int32_t nb;  // blocks of the current sequence
+    int32_t b0;  // blocks of the current sequence before the list's first (skip[seq]; 0 without skip)
 
-    __device__ __forceinline__ void init(int64_t x, const int32_t *__restrict__ cu, int32_t N) {
+    __device__ __forceinline__ void init(int64_t x, const int32_t *__restrict__ cu, int32_t N,
+                                         const int32_t *__restrict__ skip = nullptr) {
         const int32_t Wg = cu[N];
         g = (int32_t)(x / Wg);
         const int32_t r = (int32_t)(x - (int64_t)g * Wg);
@@ -222,19 +281,23 @@ struct BlockCursor {
         seq = lo;
         blk = r - cu[seq];
         nb = cu[seq + 1] - cu[seq];
+        b0 = skip ? skip[seq] : 0;
     }
 
     // Position at flattened block x when the sequence holding it is known
     // (from the plan kernel's per-CTA start table): no search.
-    __device__ __forceinline__ void init_at(int64_t x, int32_t s, const int32_t *__restrict__ cu, int32_t N) {
+    __device__ __forceinline__ void init_at(int64_t x, int32_t s, const int32_t *__restrict__ cu, int32_t N,
+                                            const int32_t *__restrict__ skip = nullptr) {
         const int32_t Wg = cu[N];
         g = (int32_t)(x / Wg);
         seq = s;
         blk = (int32_t)(x - (int64_t)g * Wg) - cu[s];
         nb = cu[s + 1] - cu[s];
+        b0 = skip ? skip[s] : 0;
     }
 
-    __device__ __forceinline__ void advance(const int32_t *__restrict__ cu, int32_t N) {
+    __device__ __forceinline__ void advance(const int32_t *__restrict__ cu, int32_t N,
+                                            const int32_t *__restrict__ skip = nullptr) {
         if (++blk < nb) return;
         blk = 0;
         do {
@@ -244,6 +307,7 @@ struct BlockCursor {
             }
             nb = cu[seq + 1] - cu[seq];
         } while (nb == 0);
+        b0 = skip ? skip[seq] : 0;
     }
 };
 

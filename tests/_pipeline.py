@@ -42,7 +42,8 @@ def oracle_decode(wl, host, r, pairs=None):
                          pairs=pairs, num_threads=oracle.available_threads())
 
 
-def gpu_step(wl, dev, kernel="auto", num_splits=0, decode=True):
+def gpu_step(wl, dev, kernel="auto", num_splits=0, decode=True, shared=False):
+    """``shared``: decode with a shared-prefix plan built from the host tables."""
     bm = pa.BlockManager(wl.num_blocks, wl.block_size, wl.free_order)
     slots, pairs = bm.apply_script(wl.script)
     tables, lens = bm.export(list(range(wl.num_seqs)), wl.max_blocks_per_seq)
@@ -53,9 +54,13 @@ def gpu_step(wl, dev, kernel="auto", num_splits=0, decode=True):
     g["pairs"] = torch.from_numpy(pairs).cuda()
     pa.pa_copy_blocks(g["k_cache"], g["v_cache"], g["pairs"])
     pa.pa_reshape_and_cache(g["k"], g["v"], g["slots"], g["k_cache"], g["v_cache"])
+    plan = None
+    if shared:
+        plan, g["plan_info"] = pa.shared_prefix_plan(tables, lens, wl.block_size, wl.num_q_heads, wl.num_kv_heads)
+        plan = plan.cuda()
     if decode:
         g["out"] = pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale,
-                                kernel=kernel, num_splits=num_splits)
+                                kernel=kernel, num_splits=num_splits, shared_plan=plan)
     assert pa.pa_get_device_error(raise_on_error=False) == 0
     g["host_tables"], g["host_slots"], g["host_pairs"] = tables, slots, pairs
     return g

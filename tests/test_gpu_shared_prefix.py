@@ -1,0 +1,197 @@
+"""GPU parity of decode with a shared-prefix plan: blocks shared by several
+sequences (parallel-sampling forks, prefix-cache hits, beams) are read once
+for all sharers.  The output is the same attention, so it must match the fp64
+oracle within the bf16 tolerance, for every head ratio, head size, block
+size, layout and split count the tensor-core kernel covers; a plan that does
+not match its call is reported and the affected sequences are computed
+without sharing, still correctly."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_150_gb300 as pa
+from paged_kv_cache_150_gb300 import inputs
+from _pipeline import TOL, gpu_step, host_values, max_abs_err, oracle_decode, oracle_step, sample_pairs
+
+pytestmark = pytest.mark.gpu
+
+# (name, prompts, prompt_len, samples, max_append, H, Hk, D, B)
+SAMPLING = [
+    ("g4-s4", 6, 200, 4, 40, 32, 8, 128, 16),     # the parallel-sampling shape, reduced
+    ("g8-s4", 4, 150, 4, 30, 64, 8, 128, 16),     # 8 query heads per KV head: one member per warp
+    ("g1-s40", 2, 90, 40, 20, 32, 32, 128, 16),   # one query head per KV head, 40 sharers: three passes of 16
+    ("g2-b32", 3, 300, 5, 70, 16, 8, 128, 32),    # block size 32
+    ("g4-d64", 3, 120, 6, 25, 32, 8, 64, 16),     # head_dim 64
+    ("g4-s9-b32", 3, 64, 9, 10, 16, 4, 64, 32),   # 36 rows: three passes, head_dim 64, block 32
+    ("g2-s4", 3, 80, 4, 12, 16, 8, 128, 16),      # 8 rows: one pass, the second MMA tile empty
+]
+
+
+def _sampling(name, prompts, prompt_len, samples, max_append, H, Hk, D, B, seed=4242):
+    return inputs.sampling_workload(name, prompts, prompt_len, samples, max_append, H, Hk, D, B, "bf16", seed)
+
+
+@pytest.mark.parametrize("spec", SAMPLING, ids=[s[0] for s in SAMPLING])
+def test_shared_prefix_decode_matches_oracle(spec):
+    wl = _sampling(*spec)
+    dev, host = host_values(wl, "cpu")
+    r = oracle_step(wl, host)
+    ref = oracle_decode(wl, host, r)
+    g = gpu_step(wl, {k: v.clone() for k, v in dev.items()}, shared=True)
+    assert g["plan_info"]["num_groups"] == spec[1]  # every prompt's samples share its blocks
+    assert max_abs_err(g["out"], ref) <= TOL["bf16"]
+    plain = gpu_step(wl, {k: v.clone() for k, v in dev.items()})
+    assert (g["out"].float() - plain["out"].float()).abs().max().item() <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("splits", [2, 3, 7, 64, 0])
+def test_shared_prefix_any_split_count(splits):
+    wl = _sampling(*SAMPLING[0])
+    dev, host = host_values(wl, "cpu")
+    r = oracle_step(wl, host)
+    ref = oracle_decode(wl, host, r)
+    g = gpu_step(wl, dev, shared=True, num_splits=splits)
+    assert max_abs_err(g["out"], ref) <= TOL["bf16"]
+
+
+def test_shared_prefix_split_layout():
+    wl = _sampling(*SAMPLING[0])
+    dev, host = host_values(wl, "cpu", layout="split")
+    r = oracle_step(wl, host)
+    g = gpu_step(wl, dev, shared=True)
+    assert max_abs_err(g["out"], oracle_decode(wl, host, r)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("cfg,kw", [("cfg3", {"small": True}), ("cfg3", {"small": True, "prompt_len": 200}),
+                                    ("prefix", {"small": True})])
+def test_shared_prefix_small_workloads(cfg, kw):
+    wl = inputs.workload(cfg, **kw)
+    dev, host = host_values(wl, "cpu")
+    r = oracle_step(wl, host)
+    g = gpu_step(wl, dev, shared=True)
+    assert g["plan_info"]["num_groups"] > 0
+    assert max_abs_err(g["out"], oracle_decode(wl, host, r)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("cfg,kw", [("cfg3", {"prompt_len": 2008}), ("cfg3", {}), ("prefix", {})])
+def test_shared_prefix_full_size_sampled(cfg, kw):
+    wl = inputs.workload(cfg, **kw)
+    dev, host = host_values(wl, "cuda")
+    r = oracle_step(wl, host)
+    g = gpu_step(wl, dev, shared=True)
+    assert g["plan_info"]["num_groups"] in (64, 8)
+    pairs = sample_pairs(wl, 64)
+    assert max_abs_err(g["out"], oracle_decode(wl, host, r, pairs=pairs), pairs) <= TOL["bf16"]
+    # every output against the decode without a plan
+    plain = pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale)
+    assert (g["out"].float() - plain.float()).abs().max().item() <= TOL["bf16"]
+
+
+def test_shared_prefix_beam_search_steps():
+    wl = inputs.beam(False)
+    vals = inputs.make_values(wl, "cuda")
+    dev = {k: v.cuda() for k, v in vals.items()}
+    host = {k: inputs.to_numpy_elems(v).copy() for k, v in vals.items()}
+    m = oracle.OracleBlockManager(wl.num_blocks, wl.block_size, wl.free_order)
+    bm = pa.BlockManager(wl.num_blocks, wl.block_size, wl.free_order)
+    row = qrow = grouped = 0
+    for st in wl.steps:
+        r = oracle.run_script(0, wl.block_size, None, st["ops"], manager=m)
+        slots, pairs = bm.apply_script(st["ops"])
+        T = len(slots)
+        oracle.copy_blocks(host["k_cache"], host["v_cache"], r["pairs"])
+        oracle.reshape_and_cache(host["k"][row:row + T], host["v"][row:row + T], r["slots"], host["k_cache"],
+                                 host["v_cache"])
+        pa.pa_copy_blocks(dev["k_cache"], dev["v_cache"], torch.from_numpy(pairs).cuda())
+        pa.pa_reshape_and_cache(dev["k"][row:row + T], dev["v"][row:row + T], torch.from_numpy(slots).cuda(),
+                                dev["k_cache"], dev["v_cache"])
+        seqs = st["decode"]
+        mb = max(len(m.tables[s]) for s in seqs)
+        tables, lens = bm.export(seqs, mb)
+        plan, info = pa.shared_prefix_plan(tables, lens, wl.block_size, wl.num_q_heads, wl.num_kv_heads)
+        grouped += info["num_groups"]
+        q = dev["q"][qrow:qrow + len(seqs)]
+        out = pa.pa_decode(q, dev["k_cache"], dev["v_cache"], torch.from_numpy(tables).cuda(),
+                           torch.from_numpy(lens).cuda(), wl.scale, shared_plan=plan.cuda())
+        ref = oracle.decode(host["q"][qrow:qrow + len(seqs)], host["k_cache"], host["v_cache"],
+                            oracle.pad_tables([m.tables[s] for s in seqs], mb), [m.lens[s] for s in seqs],
+                            wl.scale, num_threads=oracle.available_threads())
+        assert np.abs(out.double().cpu().numpy() - ref).max() <= TOL["bf16"]
+        oracle.run_script(0, wl.block_size, None, st["select"], manager=m)
+        bm.apply_script(st["select"])
+        row += T
+        qrow += len(seqs)
+    assert pa.pa_get_device_error(raise_on_error=False) == 0
+    assert grouped > 0
+
+
+def _plan_case():
+    wl = _sampling("mismatch", 3, 100, 4, 20, 32, 8, 128, 16, seed=77)
+    dev, host = host_values(wl, "cpu")
+    r = oracle_step(wl, host)
+    g = gpu_step(wl, dev, decode=False)
+    tables, lens = g["host_tables"], r["lens"].astype(np.int32)
+    plan, info = pa.shared_prefix_plan(tables, lens, wl.block_size, wl.num_q_heads, wl.num_kv_heads)
+    assert info["num_groups"] == 3
+    return wl, host, r, g, plan, lens
+
+
+def test_member_without_own_positions_is_computed_without_sharing():
+    wl, host, r, g, plan, lens = _plan_case()
+    P = 100 // 16  # 6 shared blocks
+    short = lens.copy()
+    short[5] = P * wl.block_size  # on the device this member now ends with the shared prefix
+    out = pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["tables"], torch.from_numpy(short).cuda(), wl.scale,
+                       shared_plan=plan.cuda())
+    assert pa.pa_get_device_error(raise_on_error=False) == pa._lib.PA_ERR_DEVICE_PLAN
+    ref = oracle.decode(host["q"], r["k_cache"], r["v_cache"], r["tables_padded"], short, wl.scale,
+                        num_threads=oracle.available_threads())
+    assert max_abs_err(out, ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("corrupt", ["magic", "num_seqs", "member", "prefix", "back_pointer", "pass_count",
+                                     "rows_per_pass"])
+def test_plan_that_does_not_match_is_reported_and_ignored(corrupt):
+    wl, host, r, g, plan, lens = _plan_case()
+    w = plan.clone()
+    N, ng, M = int(w[1]), int(w[4]), int(w[5])
+    o_prefix = 8 + 2 * N
+    o_vbase = o_prefix + ng
+    o_members = o_vbase + 2 * (ng + 1)
+    if corrupt == "magic":
+        w[0] = 0
+    elif corrupt == "num_seqs":
+        w[1] = N + 1
+    elif corrupt == "member":
+        w[o_members + 1] = N + 5
+    elif corrupt == "prefix":
+        w[o_prefix] = 10 ** 6
+    elif corrupt == "back_pointer":
+        w[8 + N + 0] = 3  # seq_member of sequence 0
+    elif corrupt == "pass_count":
+        w[o_vbase + 1] += 1
+    elif corrupt == "rows_per_pass":
+        w[7] = 24
+    out = pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale,
+                       shared_plan=w.cuda())
+    assert pa.pa_get_device_error(raise_on_error=False) == pa._lib.PA_ERR_DEVICE_PLAN
+    assert max_abs_err(out, oracle_decode(wl, host, r)) <= TOL["bf16"]
+
+
+def test_plan_with_one_cta_is_ignored_quietly():
+    wl, host, r, g, plan, lens = _plan_case()
+    out = pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale, num_splits=1,
+                       shared_plan=plan.cuda())
+    assert pa.pa_get_device_error(raise_on_error=False) == 0
+    assert max_abs_err(out, oracle_decode(wl, host, r)) <= TOL["bf16"]
+
+
+def test_plan_with_q_not_16_byte_aligned_is_ignored_quietly():
+    wl, host, r, g, plan, lens = _plan_case()
+    buf = torch.empty(g["q"].numel() + 8, dtype=g["q"].dtype, device="cuda")
+    q = buf[2:2 + g["q"].numel()].view(g["q"].shape)  # 4-byte aligned, not 16
+    q.copy_(g["q"])
+    out = pa.pa_decode(q, g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale, shared_plan=plan.cuda())
+    assert pa.pa_get_device_error(raise_on_error=False) == 0
+    assert max_abs_err(out, oracle_decode(wl, host, r)) <= TOL["bf16"]
