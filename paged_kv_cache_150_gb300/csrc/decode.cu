@@ -37,6 +37,28 @@ namespace pa {
 __device__ __forceinline__ void store_out(float *p, float v) { *p = v; }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
 
+// A lane's slice of E merged outputs, a[j] * inv: 16-byte stores where the
+// slice allows (bf16, E % 8 == 0, 16-byte aligned), else element by element.
+template <typename T, int E>
+__device__ __forceinline__ void store_slice(T *o, const float (&a)[E], float inv) {
+    if constexpr (sizeof(T) == 2 && E % 8 == 0) {
+        if (((uintptr_t)o & 15) == 0) {
+#pragma unroll
+            for (int j8 = 0; j8 < E / 8; ++j8) {
+                uint4 u;
+                u.x = pack_bf16x2(a[8 * j8 + 0] * inv, a[8 * j8 + 1] * inv);
+                u.y = pack_bf16x2(a[8 * j8 + 2] * inv, a[8 * j8 + 3] * inv);
+                u.z = pack_bf16x2(a[8 * j8 + 4] * inv, a[8 * j8 + 5] * inv);
+                u.w = pack_bf16x2(a[8 * j8 + 6] * inv, a[8 * j8 + 7] * inv);
+                *reinterpret_cast<uint4 *>(o + 8 * j8) = u;
+            }
+            return;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < E; ++j) store_out(o + j, a[j] * inv);
+}
+
 // ---------------------------------------------------------------- plan kernel
 // Checks a shared-prefix plan's words against the call (sizes, heads per KV
 // head, block size, and every index it holds), so that a bad plan can only
@@ -109,7 +131,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
                                                            const int32_t *__restrict__ plan, int32_t G,
                                                            int32_t Hk, int32_t NH, int32_t *__restrict__ skip,
                                                            int32_t *__restrict__ ctl,
-                                                           int32_t *__restrict__ start_s) {
+                                                           int32_t *__restrict__ start_s, int32_t plan_in_smem) {
     grid_dependency_wait();     // inputs written by earlier work on the stream
     grid_launch_dependents();   // the attention kernel may become resident now
     constexpr int32_t kSmemCu = 2048;  // prefix sums kept in shared memory for the start search
@@ -124,6 +146,16 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
     const int nwarps = blockDim.x >> 5;
     if (threadIdx.x == 0) carry = 0;
     for (int32_t i = threadIdx.x; i < num_counters; i += blockDim.x) counters[i] = 0u;
+    // The plan's words (the caller's buffer holds 7 N + 16 of them), copied to
+    // shared memory in one coalesced pass when they fit, so that its checks
+    // and lookups below are not chains of global loads.
+    extern __shared__ int32_t plan_sm[];
+    if (plan && plan_in_smem) {
+        const int32_t words = 7 * N + 16;
+        for (int32_t i = threadIdx.x; i < words; i += blockDim.x) plan_sm[i] = plan[i];
+        __syncthreads();
+        plan = plan_sm;
+    }
     // A shared-prefix plan that does not match the call switches sharing off.
     const bool plan_ok = plan && plan_valid(plan, N, G, B, max_len / B, &s_flag, &s_count);
     if (plan && !plan_ok && threadIdx.x == 0) atomicOr(err, kErrPlan);
@@ -265,7 +297,7 @@ struct PieceRange {
 // back to back (the merge runs at the end of the kernel, so its L2 latency is
 // on the kernel's critical path); two passes, the maximum over all pieces
 // first, then the weighted sums.
-template <typename T, int D, int LPH, int kBatch>
+template <typename T, int D, int LPH>
 __device__ __forceinline__ void merge_pieces_lph(T *__restrict__ out_base, const PieceRange (&rg)[2], int32_t G,
                                                  int lane) {
     constexpr int E = D / LPH;
@@ -285,88 +317,48 @@ __device__ __forceinline__ void merge_pieces_lph(T *__restrict__ out_base, const
 #pragma unroll
     for (int j = 0; j < E; ++j) a[j] = 0.f;
     float Ls = 0.f;
-    // kBatch pieces per L2 round trip (kBatch * E registers): 1 inside the
-    // attention kernel, where the block loop holds the registers; more in
-    // the merge kernel.  Pieces are added in the same order either way.
-    if constexpr (kBatch == 1) {
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const PieceRange &p = rg[k];
+    for (int k = 0; k < 2; ++k) {
+        const PieceRange &p = rg[k];
 #pragma unroll 1
-            for (int32_t c = p.c0; c <= p.c1; ++c) {
-                const int64_t idx = (c + p.base) * p.stride + p.col + h;
-                const float4 *ap = reinterpret_cast<const float4 *>(p.acc + idx * D + part * E);
-                float4 x[E / 4];
+        for (int32_t c = p.c0; c <= p.c1; ++c) {
+            const int64_t idx = (c + p.base) * p.stride + p.col + h;
+            const float4 *ap = reinterpret_cast<const float4 *>(p.acc + idx * D + part * E);
+            float4 x[E / 4];
 #pragma unroll
-                for (int j4 = 0; j4 < E / 4; ++j4) x[j4] = __ldcg(ap + j4);
-                const float2 v = __ldcg(&p.ml[idx]);
-                const float wgt = ex2_approx(v.x - M);
-                Ls = fmaf(wgt, v.y, Ls);
+            for (int j4 = 0; j4 < E / 4; ++j4) x[j4] = __ldcg(ap + j4);
+            const float2 v = __ldcg(&p.ml[idx]);
+            const float wgt = ex2_approx(v.x - M);
+            Ls = fmaf(wgt, v.y, Ls);
 #pragma unroll
-                for (int j4 = 0; j4 < E / 4; ++j4) {
-                    a[4 * j4 + 0] = fmaf(wgt, x[j4].x, a[4 * j4 + 0]);
-                    a[4 * j4 + 1] = fmaf(wgt, x[j4].y, a[4 * j4 + 1]);
-                    a[4 * j4 + 2] = fmaf(wgt, x[j4].z, a[4 * j4 + 2]);
-                    a[4 * j4 + 3] = fmaf(wgt, x[j4].w, a[4 * j4 + 3]);
-                }
-            }
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const PieceRange &p = rg[k];
-#pragma unroll 1
-            for (int32_t cb = p.c0; cb <= p.c1; cb += kBatch) {
-                float4 x[kBatch][E / 4];
-                float2 v[kBatch];
-#pragma unroll
-                for (int b = 0; b < kBatch; ++b) {
-                    if (cb + b <= p.c1) {
-                        const int64_t idx = (cb + b + p.base) * p.stride + p.col + h;
-                        const float4 *ap = reinterpret_cast<const float4 *>(p.acc + idx * D + part * E);
-#pragma unroll
-                        for (int j4 = 0; j4 < E / 4; ++j4) x[b][j4] = __ldcg(ap + j4);
-                        v[b] = __ldcg(&p.ml[idx]);
-                    }
-                }
-#pragma unroll
-                for (int b = 0; b < kBatch; ++b) {
-                    if (cb + b <= p.c1) {
-                        const float wgt = ex2_approx(v[b].x - M);
-                        Ls = fmaf(wgt, v[b].y, Ls);
-#pragma unroll
-                        for (int j4 = 0; j4 < E / 4; ++j4) {
-                            a[4 * j4 + 0] = fmaf(wgt, x[b][j4].x, a[4 * j4 + 0]);
-                            a[4 * j4 + 1] = fmaf(wgt, x[b][j4].y, a[4 * j4 + 1]);
-                            a[4 * j4 + 2] = fmaf(wgt, x[b][j4].z, a[4 * j4 + 2]);
-                            a[4 * j4 + 3] = fmaf(wgt, x[b][j4].w, a[4 * j4 + 3]);
-                        }
-                    }
-                }
+            for (int j4 = 0; j4 < E / 4; ++j4) {
+                a[4 * j4 + 0] = fmaf(wgt, x[j4].x, a[4 * j4 + 0]);
+                a[4 * j4 + 1] = fmaf(wgt, x[j4].y, a[4 * j4 + 1]);
+                a[4 * j4 + 2] = fmaf(wgt, x[j4].z, a[4 * j4 + 2]);
+                a[4 * j4 + 3] = fmaf(wgt, x[j4].w, a[4 * j4 + 3]);
             }
         }
     }
     const float inv = 1.f / Ls;
     T *o = out_base + (int64_t)h * D + part * E;
-#pragma unroll
-    for (int j = 0; j < E; ++j) store_out(o + j, a[j] * inv);
+    store_slice<T, E>(o, a, inv);
 }
 
 // Lanes per head: 32 / (G rounded up to a power of two), with slices of at
 // least 4 elements.
-template <typename T, int D, int kBatch = 1>
+template <typename T, int D>
 __device__ __forceinline__ void merge_pieces(T *__restrict__ out_base, const PieceRange (&rg)[2], int32_t G,
                                              int lane) {
     constexpr int kMaxLph = D / 4 < 32 ? D / 4 : 32;
     constexpr int kL8 = 8 < kMaxLph ? 8 : kMaxLph, kL16 = 16 < kMaxLph ? 16 : kMaxLph;
     if (G > 4)
-        merge_pieces_lph<T, D, 4, kBatch>(out_base, rg, G, lane);
+        merge_pieces_lph<T, D, 4>(out_base, rg, G, lane);
     else if (G > 2)
-        merge_pieces_lph<T, D, kL8, kBatch>(out_base, rg, G, lane);
+        merge_pieces_lph<T, D, kL8>(out_base, rg, G, lane);
     else if (G > 1)
-        merge_pieces_lph<T, D, kL16, kBatch>(out_base, rg, G, lane);
+        merge_pieces_lph<T, D, kL16>(out_base, rg, G, lane);
     else
-        merge_pieces_lph<T, D, kMaxLph, kBatch>(out_base, rg, G, lane);
+        merge_pieces_lph<T, D, kMaxLph>(out_base, rg, G, lane);
 }
 
 // Pieces of the sequence's own blocks: its range of the flattened (head
@@ -1253,6 +1245,9 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
 
     grid_dependency_wait();  // the plan kernel's cu[] / lens / split (programmatic launch)
+    // With a plan, the merge kernel may become resident as CTAs finish and
+    // work out its piece ranges from the plan while the last ones run.
+    if (kShared) grid_launch_dependents();
     const int32_t Cs = kShared ? sh.ctl[0] : 0;
     if (kShared && (int32_t)blockIdx.x < Cs)
         shared_prefix_cta<D, B, LAYOUT>(smem, &tmk, &tmv, q, out, tables, max_blocks, H, G, NB, scale_log2,
@@ -1263,14 +1258,75 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
                                              err);
 }
 
+// Single-pass merge for the merge kernel: pieces are loaded kBatch at a
+// time and folded in with a running maximum, so a merge costs one dependent
+// load per batch.  Lanes as in merge_pieces_lph.
+template <typename T, int D, int LPH>
+__device__ __forceinline__ void merge_online_lph(T *__restrict__ out_base, const PieceRange (&rg)[2], int32_t G,
+                                                 int lane) {
+    constexpr int E = D / LPH, kBatch = E >= 32 ? 2 : 4;  // kBatch * E floats of pieces in flight
+    static_assert(E % 4 == 0, "slices are whole float4s");
+    const int h = lane / LPH, part = lane % LPH;
+    if (h >= G) return;
+    float a[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) a[j] = 0.f;
+    float M = -INFINITY, Ls = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const PieceRange &p = rg[k];
+#pragma unroll 1
+        for (int32_t cb = p.c0; cb <= p.c1; cb += kBatch) {
+            float4 x[kBatch][E / 4];
+            float2 v[kBatch];
+            float mb = -INFINITY;
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                if (cb + b <= p.c1) {
+                    const int64_t idx = (cb + b + p.base) * p.stride + p.col + h;
+                    const float4 *ap = reinterpret_cast<const float4 *>(p.acc + idx * D + part * E);
+#pragma unroll
+                    for (int j4 = 0; j4 < E / 4; ++j4) x[b][j4] = __ldcg(ap + j4);
+                    v[b] = __ldcg(&p.ml[idx]);
+                    mb = fmaxf(mb, v[b].x);
+                }
+            }
+            const float Mn = fmaxf(M, mb);
+            const float sc = M == -INFINITY ? 0.f : ex2_approx(M - Mn);  // every piece has a finite max
+            Ls *= sc;
+#pragma unroll
+            for (int j = 0; j < E; ++j) a[j] *= sc;
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                if (cb + b <= p.c1) {
+                    const float wgt = ex2_approx(v[b].x - Mn);
+                    Ls = fmaf(wgt, v[b].y, Ls);
+#pragma unroll
+                    for (int j4 = 0; j4 < E / 4; ++j4) {
+                        a[4 * j4 + 0] = fmaf(wgt, x[b][j4].x, a[4 * j4 + 0]);
+                        a[4 * j4 + 1] = fmaf(wgt, x[b][j4].y, a[4 * j4 + 1]);
+                        a[4 * j4 + 2] = fmaf(wgt, x[b][j4].z, a[4 * j4 + 2]);
+                        a[4 * j4 + 3] = fmaf(wgt, x[b][j4].w, a[4 * j4 + 3]);
+                    }
+                }
+            }
+            M = Mn;
+        }
+    }
+    const float inv = 1.f / Ls;
+    T *o = out_base + (int64_t)h * D + part * E;
+    store_slice<T, E>(o, a, inv);
+}
+
 // Merge of the sequences with a shared prefix (after the attention launch,
 // which left their pieces in the workspace): one warp per (member of a
-// group, KV head), all pieces of its own blocks and of its shared prefix.
+// group, KV head).  The piece ranges depend only on the plan kernel's output,
+// so they are worked out before waiting for the attention launch (which lets
+// this grid start as its CTAs finish); only the pieces are read after it.
 template <int D>
 __global__ void __launch_bounds__(256) shared_merge_kernel(
     __nv_bfloat16 *__restrict__ out, const int32_t *__restrict__ cu, int32_t N, int32_t H, int32_t Hk, int32_t G,
     int32_t NH, int32_t C, const float2 *__restrict__ ml_ws, const float *__restrict__ acc_ws, const SharedArgs sh) {
-    grid_dependency_wait();  // the attention launch's pieces
     const int32_t Cs = sh.ctl[0];
     if (Cs <= 0) return;  // plan rejected: every sequence was merged in the attention launch
     const SharedView sv = shared_view(sh.plan, sh.skip, sh.ml_s, sh.acc_s, Hk, Cs);
@@ -1284,7 +1340,18 @@ __global__ void __launch_bounds__(256) shared_merge_kernel(
     const int32_t Ce = (int32_t)(W < (int64_t)(C - Cs) ? W : (int64_t)(C - Cs));
     const PieceRange rg[2] = {own_range(ml_ws, acc_ws, cu, N, seq, kvh / NH, kvh % NH, G, NH * G, W, Ce),
                               shared_range(sv, seq, kvh, G)};
-    merge_pieces<__nv_bfloat16, D, 4>(out + ((int64_t)seq * H + (int64_t)kvh * G) * D, rg, G, lane);
+    grid_dependency_wait();  // the attention launch's pieces
+    __nv_bfloat16 *ob = out + ((int64_t)seq * H + (int64_t)kvh * G) * D;
+    constexpr int kMaxLph = D / 4 < 32 ? D / 4 : 32;
+    constexpr int kL8 = 8 < kMaxLph ? 8 : kMaxLph, kL16 = 16 < kMaxLph ? 16 : kMaxLph;
+    if (G > 4)
+        merge_online_lph<__nv_bfloat16, D, 4>(ob, rg, G, lane);
+    else if (G > 2)
+        merge_online_lph<__nv_bfloat16, D, kL8>(ob, rg, G, lane);
+    else if (G > 1)
+        merge_online_lph<__nv_bfloat16, D, kL16>(ob, rg, G, lane);
+    else
+        merge_online_lph<__nv_bfloat16, D, kMaxLph>(ob, rg, G, lane);
 }
 
 // ====================================================================== host
@@ -1617,11 +1684,18 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         void *outp = out;
         const int32_t *planp = sh.plan;
         int32_t *skipp = (int32_t *)sh.skip, *ctlp = (int32_t *)sh.ctl, *start_sp = (int32_t *)sh.start_s;
-        void *pargs[] = {&seq_lens, &Nv, &Bv, &ml_v, &HDv, &lens_ws, &cu, &cnt, &nc, &outp, &NGv, &Cv, &start_seq,
-                         &err, &planp, &Gv, &Hkv, &NHv, &skipp, &ctlp, &start_sp};
+        // the plan's words in shared memory when they fit (at most 96 KiB)
+        const size_t plan_bytes = sizeof(int32_t) * (7 * (size_t)num_seqs + 16);
+        int32_t in_smem = p.shared && plan_bytes <= 96 * 1024 ? 1 : 0;
         const void *pfn = cache->dtype == PA_BF16 ? (const void *)decode_plan_kernel<__nv_bfloat16>
                                                   : (const void *)decode_plan_kernel<float>;
-        if (launch_pdl(pfn, dim3(1), dim3(1024), pargs, 0, s) != cudaSuccess) return PA_ERR_CUDA;
+        const size_t psmem = in_smem ? plan_bytes : 0;
+        if (psmem > 48 * 1024 &&
+            cudaFuncSetAttribute(pfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem) != cudaSuccess)
+            return PA_ERR_CUDA;
+        void *pargs[] = {&seq_lens, &Nv, &Bv, &ml_v, &HDv, &lens_ws, &cu, &cnt, &nc, &outp, &NGv, &Cv, &start_seq,
+                         &err, &planp, &Gv, &Hkv, &NHv, &skipp, &ctlp, &start_sp, &in_smem};
+        if (launch_pdl(pfn, dim3(1), dim3(1024), pargs, psmem, s) != cudaSuccess) return PA_ERR_CUDA;
     }
 
     if (opts && opts->ev_partial_begin && cudaEventRecord((cudaEvent_t)opts->ev_partial_begin, s) != cudaSuccess)
