@@ -33,7 +33,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention: KV bytes read GB/s (% of GB300 HBM peak), tokens/s"
 EXTRA = [("cfg2", {}), ("cfg4", {"block_size": 32}), ("cfg1", {}), ("cfg3", {"prompt_len": 2008}), ("cfg4", {"block_size": 16}),
-         ("cfg4", {"block_size": 16, "layout": "split"}), ("cfg2", {"layout": "split"}), ("prefix", {})]
+         ("cfg4", {"block_size": 16, "layout": "split"}), ("cfg2", {"layout": "split"}), ("prefix", {}),
+         ("cfg3", {"prompt_len": 2008, "shared": True}), ("prefix", {"shared": True})]
 FLUSH_BYTES = 512 << 20  # > 129 MB L2: written between timed steps
 FALLBACK_HBM_GBS = 6800.0
 
@@ -62,7 +63,9 @@ WORKLOADS = {"cfg4-b16": ("cfg4", {"block_size": 16}), "cfg4-b32": ("cfg4", {"bl
              "cfg2": ("cfg2", {}), "cfg1": ("cfg1", {}), "cfg3-p2000": ("cfg3", {}),
              "cfg3-p2008": ("cfg3", {"prompt_len": 2008}),
              "cfg4-b16-split": ("cfg4", {"block_size": 16, "layout": "split"}),
-             "cfg2-split": ("cfg2", {"layout": "split"}), "prefix": ("prefix", {})}
+             "cfg2-split": ("cfg2", {"layout": "split"}), "prefix": ("prefix", {}),
+             "cfg3-p2008-shared": ("cfg3", {"prompt_len": 2008, "shared": True}),
+             "prefix-shared": ("prefix", {"shared": True})}
 
 
 # ---------------------------------------------------------------- helpers
@@ -202,10 +205,14 @@ class Step:
         self.pa = pa
         kw = dict(kw)
         layout = kw.pop("layout", "row")
+        shared = kw.pop("shared", False)
         wl = inputs.workload(cfg, **kw)
         wl.seed += seed_offset
         if layout == "split":
             wl.name += "-split"
+        if shared:
+            wl.name += "-shared"
+        self.shared = shared
         self.wl = wl
         self.layout = layout
         vals = inputs.make_values(wl, device="cuda")
@@ -224,6 +231,13 @@ class Step:
         per_step = {"q": vals["q"], "k": vals["k"], "v": vals["v"], "slots": torch.from_numpy(slots),
                     "tables": torch.from_numpy(tables), "lens": torch.from_numpy(lens),
                     "pairs": torch.from_numpy(pairs)}
+        self.plan_ms, self.plan_info = None, None
+        if shared:  # shared-prefix plan of this batch, built on the host like the tables
+            t1 = time.perf_counter()
+            plan, self.plan_info = pa.shared_prefix_plan(tables, lens, wl.block_size, wl.num_q_heads,
+                                                         wl.num_kv_heads)
+            self.plan_ms = (time.perf_counter() - t1) * 1e3
+            per_step["plan"] = plan
         offs, total = {}, 0
         for name, t in per_step.items():
             offs[name] = total
@@ -238,10 +252,12 @@ class Step:
         self.packed_bytes = total
         vals["q"], vals["k"], vals["v"] = views["q"], views["k"], views["v"]
         self.slots, self.tables, self.lens, self.pairs = views["slots"], views["tables"], views["lens"], views["pairs"]
+        self.plan = views.get("plan")
         self.out = torch.empty_like(vals["q"])
-        ws = pa.pa_decode_workspace_bytes(vals["k_cache"], wl.num_seqs, wl.num_q_heads)
+        ws = pa.pa_decode_workspace_bytes(vals["k_cache"], wl.num_seqs, wl.num_q_heads, shared=shared)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device="cuda")
-        self.kernel_launches = 4 + (1 if pairs.shape[0] else 0)
+        # cache write, plan kernel, attention kernel; block copy and shared-prefix merge when present
+        self.kernel_launches = 3 + (1 if pairs.shape[0] else 0) + (1 if shared else 0)
         H, D, eb = wl.num_q_heads, wl.head_dim, wl.elem_bytes
         self.kv_bytes = wl.kv_bytes_read()
         # distinct physical blocks the decode reads (shared prefixes counted once)
@@ -263,7 +279,7 @@ class Step:
             pa.pa_copy_blocks(v["k_cache"], v["v_cache"], self.pairs)
         pa.pa_reshape_and_cache(v["k"], v["v"], self.slots, v["k_cache"], v["v_cache"])
         pa.pa_decode(v["q"], v["k_cache"], v["v_cache"], self.tables, self.lens, self.wl.scale, out=self.out,
-                     workspace=self.workspace, events=events)
+                     workspace=self.workspace, events=events, shared_plan=self.plan)
 
 
 def _events(n):
@@ -527,6 +543,11 @@ def run_ours(args, rank, world):
                                  "written_rows": int((st.host["slots"] >= 0).sum()),
                                  "cache_layout": st.layout,
                                  "write_copy": time_write_copy(st, 50, peak)}
+            if st.unique_block_bytes < st.kv_bytes:  # blocks shared between sequences: the bytes read once
+                extra[st.wl.name]["unique_gbs"] = round(st.unique_block_bytes / (mean_ms / 1e3) / 1e9, 2)
+                extra[st.wl.name]["unique_hbm_frac"] = round(st.unique_block_bytes / (mean_ms / 1e3) / 1e9 / peak, 4)
+            if st.shared:
+                extra[st.wl.name]["shared_plan"] = dict(st.plan_info, host_ms=round(st.plan_ms, 3))
             del st
             torch.cuda.empty_cache()
         line["workloads"] = extra

@@ -37,10 +37,20 @@ namespace pa {
 __device__ __forceinline__ void store_out(float *p, float v) { *p = v; }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
 
-// A lane's slice of E merged outputs, a[j] * inv: 16-byte stores where the
-// slice allows (bf16, E % 8 == 0, 16-byte aligned), else element by element.
+// A lane's slice of E merged outputs, a[j] * inv: 16-byte (or, for slices
+// of 4, 8-byte) stores where the slice allows (bf16, aligned), else element
+// by element.
 template <typename T, int E>
 __device__ __forceinline__ void store_slice(T *o, const float (&a)[E], float inv) {
+    if constexpr (sizeof(T) == 2 && E == 4) {
+        if (((uintptr_t)o & 7) == 0) {
+            uint2 u;
+            u.x = pack_bf16x2(a[0] * inv, a[1] * inv);
+            u.y = pack_bf16x2(a[2] * inv, a[3] * inv);
+            *reinterpret_cast<uint2 *>(o) = u;
+            return;
+        }
+    }
     if constexpr (sizeof(T) == 2 && E % 8 == 0) {
         if (((uintptr_t)o & 15) == 0) {
 #pragma unroll
