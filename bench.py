@@ -53,6 +53,8 @@ def parse():
                          "cfg4-b16-split, cfg2-split, prefix")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-write-copy", action="store_true",
+                    help="skip timing the cache write and block copy on their own (launch lists of a step)")
     ap.add_argument("--l2", choices=["none", "write"], default="none",
                     help="between timed steps: nothing (every workload's KV is several times the 129 MB L2) "
                          "or write a 512 MiB buffer (leaves dirty lines whose write-back the next step pays)")
@@ -478,7 +480,7 @@ def run_ours(args, rank, world):
     achieved = step.kernel_bytes / (kern_avg_ms / 1e3) / 1e9
     traffic, _ = profiled_traffic(workload_name(step))
 
-    write_copy = time_write_copy(step, 50, peak)
+    write_copy = None if args.no_write_copy else time_write_copy(step, 50, peak)
     if args.no_e2e:
         e2e = None
     else:
@@ -542,7 +544,7 @@ def run_ours(args, rank, world):
                                  "unique_block_bytes": st.unique_block_bytes,
                                  "written_rows": int((st.host["slots"] >= 0).sum()),
                                  "cache_layout": st.layout,
-                                 "write_copy": time_write_copy(st, 50, peak)}
+                                 "write_copy": None if args.no_write_copy else time_write_copy(st, 50, peak)}
             if st.unique_block_bytes < st.kv_bytes:  # blocks shared between sequences: the bytes read once
                 extra[st.wl.name]["unique_gbs"] = round(st.unique_block_bytes / (mean_ms / 1e3) / 1e9, 2)
                 extra[st.wl.name]["unique_hbm_frac"] = round(st.unique_block_bytes / (mean_ms / 1e3) / 1e9 / peak, 4)
