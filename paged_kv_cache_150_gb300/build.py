@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBRARY = os.path.join(HERE, "libpa.so")
 SOURCES = ["pa_api.cu", "cache_ops.cu", "decode.cu", "block_manager.cpp", "simulator.cpp", "shared_plan.cpp"]
-HEADERS = ["pa_common.cuh", "pa_internal.h"]
+HEADERS = ["pa_common.cuh", "pa_internal.h", "decode_merge.cuh", "decode_plan.cuh", "decode_simt.cuh", "decode_mma.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

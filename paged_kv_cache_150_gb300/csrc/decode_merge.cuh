@@ -1,0 +1,325 @@
+// Split-K merge of decode pieces (part of decode.cu's translation unit).
+//
+// A piece is the partial result (running max, sum, accumulator) of one
+// (sequence, KV head) over one CTA's part of its blocks; the merge folds all
+// pieces of a pair with the max/sum rescaling.  Fused into the attention
+// kernel (last arriver) for sequences without a shared prefix, and run as
+// shared_merge_kernel for sequences with one.
+#pragma once
+
+#include "pa_internal.h"
+
+namespace pa {
+
+// ------------------------------------------------------------ output stores
+__device__ __forceinline__ void store_out(float *p, float v) { *p = v; }
+__device__ __forceinline__ void store_out(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+
+// A lane's slice of E merged outputs, a[j] * inv: 16-byte (or, for slices
+// of 4, 8-byte) stores where the slice allows (bf16, aligned), else element
+// by element.
+template <typename T, int E>
+__device__ __forceinline__ void store_slice(T *o, const float (&a)[E], float inv) {
+    if constexpr (sizeof(T) == 2 && E == 4) {
+        if (((uintptr_t)o & 7) == 0) {
+            uint2 u;
+            u.x = pack_bf16x2(a[0] * inv, a[1] * inv);
+            u.y = pack_bf16x2(a[2] * inv, a[3] * inv);
+            *reinterpret_cast<uint2 *>(o) = u;
+            return;
+        }
+    }
+    if constexpr (sizeof(T) == 2 && E % 8 == 0) {
+        if (((uintptr_t)o & 15) == 0) {
+#pragma unroll
+            for (int j8 = 0; j8 < E / 8; ++j8) {
+                uint4 u;
+                u.x = pack_bf16x2(a[8 * j8 + 0] * inv, a[8 * j8 + 1] * inv);
+                u.y = pack_bf16x2(a[8 * j8 + 2] * inv, a[8 * j8 + 3] * inv);
+                u.z = pack_bf16x2(a[8 * j8 + 4] * inv, a[8 * j8 + 5] * inv);
+                u.w = pack_bf16x2(a[8 * j8 + 6] * inv, a[8 * j8 + 7] * inv);
+                *reinterpret_cast<uint4 *>(o + 8 * j8) = u;
+            }
+            return;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < E; ++j) store_out(o + j, a[j] * inv);
+}
+
+// ------------------------------------------------------------ piece merge
+// Partial results of one (sequence, KV head) are "pieces": (m, l) in ml[] and
+// the unnormalised accumulator in acc[] (D floats), for each of the G query
+// heads.  A PieceRange names the pieces held by CTAs c0..c1 of one split:
+// head h of the piece of CTA c is element (c + base) * stride + col + h.  The
+// own-block pieces of a sequence form one range; with a shared-prefix plan,
+// the pieces of its shared prefix form a second one.
+struct PieceRange {
+    const float2 *ml;
+    const float *acc;
+    int64_t base;
+    int32_t stride, col, c0, c1;  // empty when c0 > c1
+};
+
+// Run by the warp that finished the last piece of one (sequence, KV head):
+// merges both ranges for its G query heads.  Lanes split the G heads x D
+// outputs: LPH lanes per head, each a contiguous slice of E = D / LPH
+// elements.  With LPH a compile-time constant every load of a piece is issued
+// back to back (the merge runs at the end of the kernel, so its L2 latency is
+// on the kernel's critical path); two passes, the maximum over all pieces
+// first, then the weighted sums.
+template <typename T, int D, int LPH>
+__device__ __forceinline__ void merge_pieces_lph(T *__restrict__ out_base, const PieceRange (&rg)[2], int32_t G,
+                                                 int lane) {
+    constexpr int E = D / LPH;
+    static_assert(E % 4 == 0, "slices are whole float4s");
+    const int h = lane / LPH;
+    const int part = lane % LPH;
+    if (h >= G) return;
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const PieceRange &p = rg[k];
+#pragma unroll 8
+        for (int32_t c = p.c0; c <= p.c1; ++c)
+            M = fmaxf(M, __ldcg(&p.ml[(c + p.base) * p.stride + p.col + h]).x);
+    }
+    float a[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) a[j] = 0.f;
+    float Ls = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const PieceRange &p = rg[k];
+#pragma unroll 1
+        for (int32_t c = p.c0; c <= p.c1; ++c) {
+            const int64_t idx = (c + p.base) * p.stride + p.col + h;
+            const float4 *ap = reinterpret_cast<const float4 *>(p.acc + idx * D + part * E);
+            float4 x[E / 4];
+#pragma unroll
+            for (int j4 = 0; j4 < E / 4; ++j4) x[j4] = __ldcg(ap + j4);
+            const float2 v = __ldcg(&p.ml[idx]);
+            const float wgt = ex2_approx(v.x - M);
+            Ls = fmaf(wgt, v.y, Ls);
+#pragma unroll
+            for (int j4 = 0; j4 < E / 4; ++j4) {
+                a[4 * j4 + 0] = fmaf(wgt, x[j4].x, a[4 * j4 + 0]);
+                a[4 * j4 + 1] = fmaf(wgt, x[j4].y, a[4 * j4 + 1]);
+                a[4 * j4 + 2] = fmaf(wgt, x[j4].z, a[4 * j4 + 2]);
+                a[4 * j4 + 3] = fmaf(wgt, x[j4].w, a[4 * j4 + 3]);
+            }
+        }
+    }
+    const float inv = 1.f / Ls;
+    T *o = out_base + (int64_t)h * D + part * E;
+    store_slice<T, E>(o, a, inv);
+}
+
+// Lanes per head: 32 / (G rounded up to a power of two), with slices of at
+// least 4 elements.
+template <typename T, int D>
+__device__ __forceinline__ void merge_pieces(T *__restrict__ out_base, const PieceRange (&rg)[2], int32_t G,
+                                             int lane) {
+    constexpr int kMaxLph = D / 4 < 32 ? D / 4 : 32;
+    constexpr int kL8 = 8 < kMaxLph ? 8 : kMaxLph, kL16 = 16 < kMaxLph ? 16 : kMaxLph;
+    if (G > 4)
+        merge_pieces_lph<T, D, 4>(out_base, rg, G, lane);
+    else if (G > 2)
+        merge_pieces_lph<T, D, kL8>(out_base, rg, G, lane);
+    else if (G > 1)
+        merge_pieces_lph<T, D, kL16>(out_base, rg, G, lane);
+    else
+        merge_pieces_lph<T, D, kMaxLph>(out_base, rg, G, lane);
+}
+
+// Pieces of the sequence's own blocks: its range of the flattened (head
+// group g, sequence, own block) list of W blocks cut over Ce CTAs; warp w of
+// the group holds KV head g * NH + w.
+__device__ __forceinline__ PieceRange own_range(const float2 *ml, const float *acc, const int32_t *__restrict__ cu,
+                                                int32_t N, int32_t seq, int32_t g, int32_t w, int32_t G,
+                                                int32_t HPG, int64_t W, int32_t Ce) {
+    const int64_t x0 = (int64_t)g * cu[N] + cu[seq];
+    const int32_t nb = cu[seq + 1] - cu[seq];
+    return PieceRange{ml, acc, (int64_t)g * N + seq, HPG, w * G, split_owner(x0, W, Ce),
+                      split_owner(x0 + nb - 1, W, Ce)};
+}
+
+__device__ __forceinline__ PieceRange no_range() { return PieceRange{nullptr, nullptr, 0, 0, 0, 0, -1}; }
+
+// The shared-prefix part of a launch, as the merge needs it: the shared
+// split is the flattened (head group hg of kPlanHeads heads, virtual
+// sequence, block) list of Ws entries cut over Ce_s CTAs.
+struct SharedView {
+    PlanView pv;
+    const int32_t *skip;
+    const float2 *ml_s;
+    const float *acc_s;
+    int64_t Ws;
+    int32_t Ce_s;
+};
+
+__device__ __forceinline__ SharedView shared_view(const int32_t *plan, const int32_t *skip, const float2 *ml_s,
+                                                  const float *acc_s, int32_t Hk, int32_t Cs) {
+    SharedView sv;
+    sv.pv = PlanView::at(plan);
+    sv.skip = skip;
+    sv.ml_s = ml_s;
+    sv.acc_s = acc_s;
+    sv.Ws = (int64_t)(Hk / kPlanHeads) * sv.pv.cu_s[sv.pv.V];
+    sv.Ce_s = (int32_t)(sv.Ws < (int64_t)Cs ? sv.Ws : (int64_t)Cs);
+    return sv;
+}
+
+// Pieces of the shared prefix of sequence seq for KV head kvh (none when the
+// sequence is computed without sharing): the virtual sequence v that holds
+// its G query rows, in slots c + hg * V + v, rows (kvh % 4) * 16 + row % 16.
+__device__ __forceinline__ PieceRange shared_range(const SharedView &sv, int32_t seq, int32_t kvh, int32_t G) {
+    if (sv.skip[seq] <= 0) return no_range();
+    const PlanView &pv = sv.pv;
+    const int32_t hg = kvh / kPlanHeads;
+    const int32_t grp = pv.seq_group[seq];
+    const int32_t row0 = pv.seq_member[seq] * G;
+    const int32_t v = pv.group_vbase[grp] + row0 / kPlanRows;
+    const int64_t xs = (int64_t)hg * pv.cu_s[pv.V] + pv.cu_s[v];
+    const int32_t P = pv.cu_s[v + 1] - pv.cu_s[v];
+    return PieceRange{sv.ml_s, sv.acc_s, (int64_t)hg * pv.V + v, kPlanSlotRows,
+                      (kvh - hg * kPlanHeads) * kPlanRows + row0 % kPlanRows, split_owner(xs, sv.Ws, sv.Ce_s),
+                      split_owner(xs + P - 1, sv.Ws, sv.Ce_s)};
+}
+
+// After a warp published a piece of (sequence seq, KV head kvh): count the
+// arrival.  True for the warp whose piece arrived last; that warp merges.
+__device__ __forceinline__ bool arrive_piece(unsigned int *__restrict__ counters, const PieceRange (&rg)[2],
+                                             int64_t counter, int lane) {
+    const unsigned int total = (unsigned int)(rg[0].c1 - rg[0].c0 + 1) +
+                               (unsigned int)(rg[1].c1 >= rg[1].c0 ? rg[1].c1 - rg[1].c0 + 1 : 0);
+    __threadfence();  // this lane's partial stores, before the arrival below
+    __syncwarp();
+    unsigned int last = 0;
+    if (lane == 0) last = atomicAdd(&counters[counter], 1u) + 1u == total;
+    return __shfl_sync(0xffffffffu, last, 0) != 0;
+}
+
+// Arrival counter of (sequence seq, KV head kvh): [head group][seq][head in group].
+__device__ __forceinline__ int64_t counter_index(int32_t seq, int32_t kvh, int32_t N, int32_t NH) {
+    const int32_t g = kvh / NH;
+    return ((int64_t)g * N + seq) * NH + (kvh - g * NH);
+}
+
+// Count a published piece; the last arriver merges every piece of the pair.
+template <typename T, int D>
+__device__ __forceinline__ void finish_piece(T *__restrict__ out, const PieceRange (&rg)[2],
+                                             unsigned int *__restrict__ counters, int32_t N, int32_t NH, int32_t H,
+                                             int32_t G, int32_t seq, int32_t kvh, int lane) {
+    if (!arrive_piece(counters, rg, counter_index(seq, kvh, N, NH), lane)) return;
+    __threadfence();  // every other piece is published: read them
+    merge_pieces<T, D>(out + ((int64_t)seq * H + (int64_t)kvh * G) * D, rg, G, lane);
+}
+
+// Workspace of the shared-prefix part of a launch (all nullptr without a plan).
+struct SharedArgs {
+    const int32_t *plan;   // the plan's words (device)
+    const int32_t *skip;   // [N] shared blocks of each sequence, 0 = none (plan kernel)
+    const int32_t *ctl;    // ctl[0]: CTAs given to shared prefixes (plan kernel)
+    const int32_t *start_s;
+    float2 *ml_s;          // shared-prefix pieces: [slot][kPlanSlotRows] (m, l)
+    float *acc_s;          //                       [slot][kPlanSlotRows][D]
+};
+
+// Single-pass merge for the merge kernel: pieces are loaded kBatch at a
+// time and folded in with a running maximum, so a merge costs one dependent
+// load per batch.  Lanes as in merge_pieces_lph.
+template <typename T, int D, int LPH>
+__device__ __forceinline__ void merge_online_lph(T *__restrict__ out_base, const PieceRange (&rg)[2], int32_t G,
+                                                 int lane) {
+    constexpr int E = D / LPH, kBatch = E >= 32 ? 2 : 4;  // kBatch * E floats of pieces in flight
+    static_assert(E % 4 == 0, "slices are whole float4s");
+    const int h = lane / LPH, part = lane % LPH;
+    if (h >= G) return;
+    float a[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) a[j] = 0.f;
+    float M = -INFINITY, Ls = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const PieceRange &p = rg[k];
+#pragma unroll 1
+        for (int32_t cb = p.c0; cb <= p.c1; cb += kBatch) {
+            float4 x[kBatch][E / 4];
+            float2 v[kBatch];
+            float mb = -INFINITY;
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                if (cb + b <= p.c1) {
+                    const int64_t idx = (cb + b + p.base) * p.stride + p.col + h;
+                    const float4 *ap = reinterpret_cast<const float4 *>(p.acc + idx * D + part * E);
+#pragma unroll
+                    for (int j4 = 0; j4 < E / 4; ++j4) x[b][j4] = __ldcg(ap + j4);
+                    v[b] = __ldcg(&p.ml[idx]);
+                    mb = fmaxf(mb, v[b].x);
+                }
+            }
+            const float Mn = fmaxf(M, mb);
+            const float sc = M == -INFINITY ? 0.f : ex2_approx(M - Mn);  // every piece has a finite max
+            Ls *= sc;
+#pragma unroll
+            for (int j = 0; j < E; ++j) a[j] *= sc;
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                if (cb + b <= p.c1) {
+                    const float wgt = ex2_approx(v[b].x - Mn);
+                    Ls = fmaf(wgt, v[b].y, Ls);
+#pragma unroll
+                    for (int j4 = 0; j4 < E / 4; ++j4) {
+                        a[4 * j4 + 0] = fmaf(wgt, x[b][j4].x, a[4 * j4 + 0]);
+                        a[4 * j4 + 1] = fmaf(wgt, x[b][j4].y, a[4 * j4 + 1]);
+                        a[4 * j4 + 2] = fmaf(wgt, x[b][j4].z, a[4 * j4 + 2]);
+                        a[4 * j4 + 3] = fmaf(wgt, x[b][j4].w, a[4 * j4 + 3]);
+                    }
+                }
+            }
+            M = Mn;
+        }
+    }
+    const float inv = 1.f / Ls;
+    T *o = out_base + (int64_t)h * D + part * E;
+    store_slice<T, E>(o, a, inv);
+}
+
+// Merge of the sequences with a shared prefix (after the attention launch,
+// which left their pieces in the workspace): one warp per (member of a
+// group, KV head).  The piece ranges depend only on the plan kernel's output,
+// so they are worked out before waiting for the attention launch (which lets
+// this grid start as its CTAs finish); only the pieces are read after it.
+template <int D>
+__global__ void __launch_bounds__(256) shared_merge_kernel(
+    __nv_bfloat16 *__restrict__ out, const int32_t *__restrict__ cu, int32_t N, int32_t H, int32_t Hk, int32_t G,
+    int32_t NH, int32_t C, const float2 *__restrict__ ml_ws, const float *__restrict__ acc_ws, const SharedArgs sh) {
+    const int32_t Cs = sh.ctl[0];
+    if (Cs <= 0) return;  // plan rejected: every sequence was merged in the attention launch
+    const SharedView sv = shared_view(sh.plan, sh.skip, sh.ml_s, sh.acc_s, Hk, Cs);
+    const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= (int64_t)sv.pv.M * Hk) return;
+    const int32_t seq = sv.pv.members[wid / Hk];
+    const int32_t kvh = (int32_t)(wid % Hk);
+    if (sh.skip[seq] <= 0) return;  // computed without sharing: merged in the attention launch
+    const int64_t W = (int64_t)(Hk / NH) * cu[N];
+    const int32_t Ce = (int32_t)(W < (int64_t)(C - Cs) ? W : (int64_t)(C - Cs));
+    const PieceRange rg[2] = {own_range(ml_ws, acc_ws, cu, N, seq, kvh / NH, kvh % NH, G, NH * G, W, Ce),
+                              shared_range(sv, seq, kvh, G)};
+    grid_dependency_wait();  // the attention launch's pieces
+    __nv_bfloat16 *ob = out + ((int64_t)seq * H + (int64_t)kvh * G) * D;
+    constexpr int kMaxLph = D / 4 < 32 ? D / 4 : 32;
+    constexpr int kL8 = 8 < kMaxLph ? 8 : kMaxLph, kL16 = 16 < kMaxLph ? 16 : kMaxLph;
+    if (G > 4)
+        merge_online_lph<__nv_bfloat16, D, 4>(ob, rg, G, lane);
+    else if (G > 2)
+        merge_online_lph<__nv_bfloat16, D, kL8>(ob, rg, G, lane);
+    else if (G > 1)
+        merge_online_lph<__nv_bfloat16, D, kL16>(ob, rg, G, lane);
+    else
+        merge_online_lph<__nv_bfloat16, D, kMaxLph>(ob, rg, G, lane);
+}
+
+}  // namespace pa
