@@ -34,7 +34,8 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode attention: KV bytes read GB/s (% of GB300 HBM peak), tokens/s"
 EXTRA = [("cfg2", {}), ("cfg4", {"block_size": 32}), ("cfg1", {}), ("cfg3", {"prompt_len": 2008}), ("cfg4", {"block_size": 16}),
          ("cfg4", {"block_size": 16, "layout": "split"}), ("cfg2", {"layout": "split"}), ("prefix", {}),
-         ("cfg3", {"prompt_len": 2008, "shared": True}), ("prefix", {"shared": True})]
+         ("cfg3", {"prompt_len": 2008, "shared": True}), ("prefix", {"shared": True}),
+         ("cfg4", {"block_size": 16, "placement": "contiguous"})]
 FLUSH_BYTES = 512 << 20  # > 129 MB L2: written between timed steps
 FALLBACK_HBM_GBS = 6800.0
 
@@ -66,6 +67,7 @@ WORKLOADS = {"cfg4-b16": ("cfg4", {"block_size": 16}), "cfg4-b32": ("cfg4", {"bl
              "cfg3-p2008": ("cfg3", {"prompt_len": 2008}),
              "cfg4-b16-split": ("cfg4", {"block_size": 16, "layout": "split"}),
              "cfg2-split": ("cfg2", {"layout": "split"}), "prefix": ("prefix", {}),
+             "cfg4-b16-contiguous": ("cfg4", {"block_size": 16, "placement": "contiguous"}),
              "cfg3-p2008-shared": ("cfg3", {"prompt_len": 2008, "shared": True}),
              "prefix-shared": ("prefix", {"shared": True})}
 

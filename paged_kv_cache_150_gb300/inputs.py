@@ -97,19 +97,26 @@ def _shuffled_free_order(rng: np.random.Generator, num_blocks: int) -> np.ndarra
 def decode_workload(name: str, lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
                     block_size: int, dtype: str, seed: int, pool_factor: float = 1.0,
                     num_blocks: Optional[int] = None, rng: Optional[np.random.Generator] = None,
-                    note: str = "") -> Workload:
+                    note: str = "", placement: str = "random") -> Workload:
     """One decode step over independent sequences of the given final lengths.
 
     Each sequence is created with L-1 tokens and then receives one new token
     (the token this step writes); a length of 0 creates an empty sequence and
-    writes nothing."""
+    writes nothing.  ``placement``: "random" (a seed-shuffled free list) or
+    "contiguous" (an ascending free list: the manager hands every sequence
+    consecutive physical blocks in order, as one contiguous KV region would)."""
+    if placement not in ("random", "contiguous"):
+        raise ValueError("placement must be 'random' or 'contiguous'")
     lens = np.asarray(lens, dtype=np.int32)
     if rng is None:
         rng = np.random.default_rng(seed)
     need = int(sum(-(-int(L) // block_size) for L in lens))
     if num_blocks is None:
         num_blocks = max(1, int(math.ceil(pool_factor * need)))
-    free_order = _shuffled_free_order(rng, num_blocks)
+    if placement == "contiguous":
+        free_order = np.arange(num_blocks, dtype=np.int32)
+    else:
+        free_order = _shuffled_free_order(rng, num_blocks)
     script: List[Tuple] = []
     for L in lens:
         script.append((NEW, max(int(L) - 1, 0)))
@@ -290,7 +297,7 @@ def prefix_workload(name: str, num_prompts: int, requests_per_prompt: int, syste
 
 
 def workload(cfg: str, small: bool = False, block_size: Optional[int] = None,
-             prompt_len: Optional[int] = None) -> Workload:
+             prompt_len: Optional[int] = None, placement: str = "random") -> Workload:
     """The named benchmark workload ("cfg0".."cfg4"), or its reduced-size twin.
 
     ``block_size`` selects 16 or 32 for cfg4; ``prompt_len`` overrides cfg3's
@@ -336,9 +343,12 @@ def workload(cfg: str, small: bool = False, block_size: Optional[int] = None,
             lens = [4096 + 5, 2 * bs + 3]
         else:
             lens = [32768] * 16
-        return decode_workload("cfg4-b%d" % bs + ("-small" if small else ""), lens, 64, 8, 128, bs,
-                               "bf16", seed, pool_factor=1.05, rng=rng,
-                               note="long-context decode, block_size %d" % bs)
+        contiguous = placement == "contiguous"
+        return decode_workload("cfg4-b%d" % bs + ("-small" if small else "") + ("-contiguous" if contiguous else ""),
+                               lens, 64, 8, 128, bs, "bf16", seed, pool_factor=1.05, rng=rng,
+                               note="long-context decode, block_size %d%s"
+                                    % (bs, ", blocks of each sequence physically contiguous" if contiguous else ""),
+                               placement=placement)
     raise ValueError("unknown workload %r" % cfg)
 
 

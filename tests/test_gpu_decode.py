@@ -19,7 +19,8 @@ pytestmark = pytest.mark.gpu
 
 SMALL = [("cfg0", {}), ("cfg1", {"small": True}), ("cfg2", {"small": True}),
          ("cfg3", {"small": True}), ("cfg3", {"small": True, "prompt_len": 200}),
-         ("cfg4", {"small": True}), ("cfg4", {"small": True, "block_size": 32})]
+         ("cfg4", {"small": True}), ("cfg4", {"small": True, "block_size": 32}),
+         ("cfg4", {"small": True, "placement": "contiguous"})]
 
 
 @pytest.mark.parametrize("cfg,kw", SMALL)
@@ -35,7 +36,7 @@ def test_decode_small(cfg, kw, kernel, splits):
 
 
 FULL = [("cfg1", {}, 64), ("cfg2", {}, 96), ("cfg3", {}, 48), ("cfg3", {"prompt_len": 2008}, 48),
-        ("cfg4", {}, 24), ("cfg4", {"block_size": 32}, 24)]
+        ("cfg4", {}, 24), ("cfg4", {"block_size": 32}, 24), ("cfg4", {"placement": "contiguous"}, 24)]
 
 
 @pytest.mark.parametrize("cfg,kw,nsample", FULL)
