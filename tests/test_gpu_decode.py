@@ -176,3 +176,20 @@ def test_bounded_wait_times_out_and_the_context_stays_usable():
     r = oracle_step(wl, host)
     g = gpu_step(wl, dev)
     assert max_abs_err(g["out"], oracle_decode(wl, host, r)) <= TOL["f32"]
+
+
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
+def test_many_sequences_prefix_sums_in_global_memory(kernel):
+    """3000 sequences: more than the plan kernel keeps in shared memory, so
+    the prefix sums and the start search run from global memory; empty
+    sequences scattered through the batch."""
+    rng = np.random.default_rng(31)
+    lens = rng.integers(1, 45, size=3000)
+    lens[::97] = 0
+    wl = inputs.decode_workload("many", lens, 16, 8, 128, 16, "bf16", seed=31, pool_factor=1.2)
+    dev, host = host_values(wl, "cuda")
+    r = oracle_step(wl, host)
+    g = gpu_step(wl, dev, kernel=kernel)
+    pairs = sample_pairs(wl, 400)
+    assert max_abs_err(g["out"], oracle_decode(wl, host, r, pairs=pairs), pairs) <= TOL["bf16"]
+    assert (g["out"][::97] == 0).all()

@@ -195,3 +195,16 @@ def test_plan_with_q_not_16_byte_aligned_is_ignored_quietly():
     out = pa.pa_decode(q, g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale, shared_plan=plan.cuda())
     assert pa.pa_get_device_error(raise_on_error=False) == 0
     assert max_abs_err(out, oracle_decode(wl, host, r)) <= TOL["bf16"]
+
+
+def test_shared_prefix_plan_too_large_for_shared_memory():
+    """4000 sequences in 1000 groups: the plan's words (about 112 KB) are read
+    from global memory by the plan kernel instead of a shared-memory copy."""
+    wl = _sampling("many-groups", 1000, 40, 4, 20, 32, 8, 128, 16, seed=91)
+    assert 4 * (7 * wl.num_seqs + 16) > 96 * 1024
+    dev, host = host_values(wl, "cuda")
+    r = oracle_step(wl, host)
+    g = gpu_step(wl, dev, shared=True)
+    assert g["plan_info"]["num_groups"] == 1000
+    pairs = sample_pairs(wl, 400)
+    assert max_abs_err(g["out"], oracle_decode(wl, host, r, pairs=pairs), pairs) <= TOL["bf16"]
