@@ -286,6 +286,22 @@ __device__ __forceinline__ void merge_online_lph(T *__restrict__ out_base, const
     store_slice<T, E>(o, a, inv);
 }
 
+// merge_online_lph with lanes per head chosen from G (as merge_pieces).
+template <typename T, int D>
+__device__ __forceinline__ void merge_online(T *__restrict__ out_base, const PieceRange (&rg)[2], int32_t G,
+                                             int lane) {
+    constexpr int kMaxLph = D / 4 < 32 ? D / 4 : 32;
+    constexpr int kL8 = 8 < kMaxLph ? 8 : kMaxLph, kL16 = 16 < kMaxLph ? 16 : kMaxLph;
+    if (G > 4)
+        merge_online_lph<T, D, 4>(out_base, rg, G, lane);
+    else if (G > 2)
+        merge_online_lph<T, D, kL8>(out_base, rg, G, lane);
+    else if (G > 1)
+        merge_online_lph<T, D, kL16>(out_base, rg, G, lane);
+    else
+        merge_online_lph<T, D, kMaxLph>(out_base, rg, G, lane);
+}
+
 // Merge of the sequences with a shared prefix (after the attention launch,
 // which left their pieces in the workspace): one warp per (member of a
 // group, KV head).  The piece ranges depend only on the plan kernel's output,
@@ -309,17 +325,7 @@ __global__ void __launch_bounds__(256) shared_merge_kernel(
     const PieceRange rg[2] = {own_range(ml_ws, acc_ws, cu, N, seq, kvh / NH, kvh % NH, G, NH * G, W, Ce),
                               shared_range(sv, seq, kvh, G)};
     grid_dependency_wait();  // the attention launch's pieces
-    __nv_bfloat16 *ob = out + ((int64_t)seq * H + (int64_t)kvh * G) * D;
-    constexpr int kMaxLph = D / 4 < 32 ? D / 4 : 32;
-    constexpr int kL8 = 8 < kMaxLph ? 8 : kMaxLph, kL16 = 16 < kMaxLph ? 16 : kMaxLph;
-    if (G > 4)
-        merge_online_lph<__nv_bfloat16, D, 4>(ob, rg, G, lane);
-    else if (G > 2)
-        merge_online_lph<__nv_bfloat16, D, kL8>(ob, rg, G, lane);
-    else if (G > 1)
-        merge_online_lph<__nv_bfloat16, D, kL16>(ob, rg, G, lane);
-    else
-        merge_online_lph<__nv_bfloat16, D, kMaxLph>(ob, rg, G, lane);
+    merge_online<__nv_bfloat16, D>(out + ((int64_t)seq * H + (int64_t)kvh * G) * D, rg, G, lane);
 }
 
 }  // namespace pa

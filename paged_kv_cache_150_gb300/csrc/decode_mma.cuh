@@ -422,6 +422,11 @@ __device__ __forceinline__ void own_block_cta(
     const int64_t lo = split_begin(c, W, Ce), hi = split_begin(c + 1, W, Ce);
     const int64_t n = hi - lo;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Sequences whose merge falls to a consumer warp, done after its block
+    // loop where the loop's registers are free for the pieces' loads.  Only
+    // the first and the last segment of a range are pieces: at most two.
+    __shared__ int32_t pending[kMmaMaxHeads][2];
+    if (threadIdx.x < 2 * kMmaMaxHeads) pending[threadIdx.x >> 1][threadIdx.x & 1] = -1;
 
     if (threadIdx.x == 0) {
 #pragma unroll
@@ -634,16 +639,32 @@ __device__ __forceinline__ void own_block_cta(
                     if (h1 < G) ml_ws[slot * HPG + warp * G + h1] = make_float2(m1, lt1);
                 }
                 // A sequence with a shared prefix is merged by shared_merge_kernel
-                // after this launch; every other one by its last arriver here.
+                // after this launch; every other one by its last arriver, after
+                // its block loop (pending).
                 if (!(kShared && cur.b0 > 0)) {
                     const PieceRange rg[2] = {own_range(ml_ws, acc_ws, cu, N, cur.seq, cur.g, warp, G, HPG, W, Ce),
                                               no_range()};
-                    finish_piece<__nv_bfloat16, D>(out, rg, counters, N, NH, H, G, cur.seq, kvh, lane);
+                    if (arrive_piece(counters, rg, counter_index(cur.seq, kvh, N, NH), lane) && lane == 0)
+                        pending[warp][pending[warp][0] >= 0 ? 1 : 0] = cur.g * N + cur.seq;
                 }
             }
             seg_start = true;
         }
         cur.advance(cu, N, skip);
+    }
+    __syncwarp();
+    const int32_t sp0 = pending[warp][0], sp1 = pending[warp][1];
+    if (sp0 >= 0) {
+        const int32_t g = sp0 / N, seq = sp0 - g * N;
+        const PieceRange rg[2] = {own_range(ml_ws, acc_ws, cu, N, seq, g, warp, G, NH * G, W, Ce), no_range()};
+        __threadfence();  // every other piece is published: read them
+        merge_online<__nv_bfloat16, D>(out + ((int64_t)seq * H + (int64_t)(g * NH + warp) * G) * D, rg, G, lane);
+    }
+    if (sp1 >= 0) {
+        const int32_t g = sp1 / N, seq = sp1 - g * N;
+        const PieceRange rg[2] = {own_range(ml_ws, acc_ws, cu, N, seq, g, warp, G, NH * G, W, Ce), no_range()};
+        __threadfence();
+        merge_online<__nv_bfloat16, D>(out + ((int64_t)seq * H + (int64_t)(g * NH + warp) * G) * D, rg, G, lane);
     }
 }
 
