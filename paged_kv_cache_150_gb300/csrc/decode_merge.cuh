@@ -229,10 +229,11 @@ struct SharedArgs {
 // Single-pass merge for the merge kernel: pieces are loaded kBatch at a
 // time and folded in with a running maximum, so a merge costs one dependent
 // load per batch.  Lanes as in merge_pieces_lph.
-template <typename T, int D, int LPH>
+template <typename T, int D, int LPH, int kWideBatch>
 __device__ __forceinline__ void merge_online_lph(T *__restrict__ out_base, const PieceRange (&rg)[2], int32_t G,
                                                  int lane) {
-    constexpr int E = D / LPH, kBatch = E >= 32 ? 2 : 4;  // kBatch * E floats of pieces in flight
+    // kBatch * E floats of pieces in flight; slices of 32 take kWideBatch
+    constexpr int E = D / LPH, kBatch = E >= 32 ? kWideBatch : 4;
     static_assert(E % 4 == 0, "slices are whole float4s");
     const int h = lane / LPH, part = lane % LPH;
     if (h >= G) return;
@@ -287,19 +288,19 @@ __device__ __forceinline__ void merge_online_lph(T *__restrict__ out_base, const
 }
 
 // merge_online_lph with lanes per head chosen from G (as merge_pieces).
-template <typename T, int D>
+template <typename T, int D, int kWideBatch>
 __device__ __forceinline__ void merge_online(T *__restrict__ out_base, const PieceRange (&rg)[2], int32_t G,
                                              int lane) {
     constexpr int kMaxLph = D / 4 < 32 ? D / 4 : 32;
     constexpr int kL8 = 8 < kMaxLph ? 8 : kMaxLph, kL16 = 16 < kMaxLph ? 16 : kMaxLph;
     if (G > 4)
-        merge_online_lph<T, D, 4>(out_base, rg, G, lane);
+        merge_online_lph<T, D, 4, kWideBatch>(out_base, rg, G, lane);
     else if (G > 2)
-        merge_online_lph<T, D, kL8>(out_base, rg, G, lane);
+        merge_online_lph<T, D, kL8, kWideBatch>(out_base, rg, G, lane);
     else if (G > 1)
-        merge_online_lph<T, D, kL16>(out_base, rg, G, lane);
+        merge_online_lph<T, D, kL16, kWideBatch>(out_base, rg, G, lane);
     else
-        merge_online_lph<T, D, kMaxLph>(out_base, rg, G, lane);
+        merge_online_lph<T, D, kMaxLph, kWideBatch>(out_base, rg, G, lane);
 }
 
 // Merge of the sequences with a shared prefix (after the attention launch,
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(256) shared_merge_kernel(
     const PieceRange rg[2] = {own_range(ml_ws, acc_ws, cu, N, seq, kvh / NH, kvh % NH, G, NH * G, W, Ce),
                               shared_range(sv, seq, kvh, G)};
     grid_dependency_wait();  // the attention launch's pieces
-    merge_online<__nv_bfloat16, D>(out + ((int64_t)seq * H + (int64_t)kvh * G) * D, rg, G, lane);
+    merge_online<__nv_bfloat16, D, 2>(out + ((int64_t)seq * H + (int64_t)kvh * G) * D, rg, G, lane);
 }
 
 }  // namespace pa

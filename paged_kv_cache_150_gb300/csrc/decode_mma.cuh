@@ -658,13 +658,13 @@ __device__ __forceinline__ void own_block_cta(
         const int32_t g = sp0 / N, seq = sp0 - g * N;
         const PieceRange rg[2] = {own_range(ml_ws, acc_ws, cu, N, seq, g, warp, G, NH * G, W, Ce), no_range()};
         __threadfence();  // every other piece is published: read them
-        merge_online<__nv_bfloat16, D>(out + ((int64_t)seq * H + (int64_t)(g * NH + warp) * G) * D, rg, G, lane);
+        merge_online<__nv_bfloat16, D, 3>(out + ((int64_t)seq * H + (int64_t)(g * NH + warp) * G) * D, rg, G, lane);
     }
     if (sp1 >= 0) {
         const int32_t g = sp1 / N, seq = sp1 - g * N;
         const PieceRange rg[2] = {own_range(ml_ws, acc_ws, cu, N, seq, g, warp, G, NH * G, W, Ce), no_range()};
         __threadfence();
-        merge_online<__nv_bfloat16, D>(out + ((int64_t)seq * H + (int64_t)(g * NH + warp) * G) * D, rg, G, lane);
+        merge_online<__nv_bfloat16, D, 3>(out + ((int64_t)seq * H + (int64_t)(g * NH + warp) * G) * D, rg, G, lane);
     }
 }
 

@@ -118,3 +118,29 @@ def test_write_many_tokens_several_grid_passes():
     pa.pa_reshape_and_cache(k, v, slots_d, kc, vc)
     assert pa.pa_get_device_error(raise_on_error=False) == 0
     assert torch.equal(kc.view(-1, hk, d), ref_k) and torch.equal(vc.view(-1, hk, d), ref_v)
+
+
+@pytest.mark.parametrize("cfg,kw", [("cfg3", {"small": True, "prompt_len": 200}), ("cfg3", {"small": True}),
+                                    ("cfg3", {"prompt_len": 2008})])
+def test_shared_blocks_are_never_written_in_place(cfg, kw):
+    """Copy-on-write invariant on the device: in the parallel-sampling step
+    (the prompt's rows predate it; the step writes only the samples' new
+    tokens) every block still shared (refcount > 1) after the manager's
+    operations keeps its bytes through the block copies and the cache write.
+    (With prefix caching the first holder writes a prompt block in the same
+    step that later requests come to share it, so the test does not apply.)"""
+    wl = inputs.workload(cfg, **kw)
+    dev, _ = host_values(wl, "cuda" if not kw.get("small") else "cpu")
+    bm = pa.BlockManager(wl.num_blocks, wl.block_size, wl.free_order)
+    slots, pairs = bm.apply_script(wl.script)
+    shared = [b for b in range(wl.num_blocks) if bm.refcount(b) > 1]
+    assert shared
+    idx = torch.tensor(shared, dtype=torch.long, device="cuda")
+    before_k, before_v = dev["k_cache"][idx].clone(), dev["v_cache"][idx].clone()
+    pa.pa_copy_blocks(dev["k_cache"], dev["v_cache"], torch.from_numpy(pairs).cuda())
+    pa.pa_reshape_and_cache(dev["k"], dev["v"], torch.from_numpy(slots).cuda(), dev["k_cache"], dev["v_cache"])
+    assert pa.pa_get_device_error(raise_on_error=False) == 0
+    assert torch.equal(dev["k_cache"][idx], before_k) and torch.equal(dev["v_cache"][idx], before_v)
+    # and the written slots all lie in blocks held by one sequence
+    written = np.unique(slots[slots >= 0] // wl.block_size)
+    assert not set(written.tolist()) & set(shared)
