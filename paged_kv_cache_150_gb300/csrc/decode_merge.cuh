@@ -2,9 +2,11 @@
 //
 // A piece is the partial result (running max, sum, accumulator) of one
 // (sequence, KV head) over one CTA's part of its blocks; the merge folds all
-// pieces of a pair with the max/sum rescaling.  Fused into the attention
-// kernel (last arriver) for sequences without a shared prefix, and run as
-// shared_merge_kernel for sequences with one.
+// pieces of a pair with the max/sum rescaling.  Done by the pair's last
+// arriver inside the attention kernels for sequences without a shared prefix
+// (in the block loop for the CUDA-core kernel, merge_pieces; after the block
+// loop for the tensor-core kernel, merge_online), and by shared_merge_kernel
+// for sequences with one.
 #pragma once
 
 #include "pa_internal.h"
@@ -61,12 +63,11 @@ struct PieceRange {
     int32_t stride, col, c0, c1;  // empty when c0 > c1
 };
 
-// Run by the warp that finished the last piece of one (sequence, KV head):
-// merges both ranges for its G query heads.  Lanes split the G heads x D
-// outputs: LPH lanes per head, each a contiguous slice of E = D / LPH
-// elements.  With LPH a compile-time constant every load of a piece is issued
-// back to back (the merge runs at the end of the kernel, so its L2 latency is
-// on the kernel's critical path); two passes, the maximum over all pieces
+// Merge of both ranges for the G query heads of one (sequence, KV head), one
+// piece per L2 round trip (few registers: it runs inside the CUDA-core
+// kernel's block loop).  Lanes split the G heads x D outputs: LPH lanes per
+// head, each a contiguous slice of E = D / LPH elements, so every load of a
+// piece is issued back to back; two passes, the maximum over all pieces
 // first, then the weighted sums.
 template <typename T, int D, int LPH>
 __device__ __forceinline__ void merge_pieces_lph(T *__restrict__ out_base, const PieceRange (&rg)[2], int32_t G,
@@ -226,8 +227,9 @@ struct SharedArgs {
     float *acc_s;          //                       [slot][kPlanSlotRows][D]
 };
 
-// Single-pass merge for the merge kernel: pieces are loaded kBatch at a
-// time and folded in with a running maximum, so a merge costs one dependent
+// Single-pass merge (after the tensor-core kernel's block loop and in
+// shared_merge_kernel, where registers are free): pieces are loaded kBatch at
+// a time and folded in with a running maximum, so a merge costs one dependent
 // load per batch.  Lanes as in merge_pieces_lph.
 template <typename T, int D, int LPH, int kWideBatch>
 __device__ __forceinline__ void merge_online_lph(T *__restrict__ out_base, const PieceRange (&rg)[2], int32_t G,

@@ -187,23 +187,20 @@ __device__ __forceinline__ void mma_block_tiles(uint32_t kslab, uint32_t vslab, 
     }
 }
 
-
 // A CTA of the shared-prefix part.  Its range of the flattened (head group
 // hg, virtual sequence v, block) list: W_s = (Hk / 4) * cu_s[V] entries cut
 // over Ce_s CTAs.  The ring, its stages and the TMA box of 4 KV heads are the
 // own-block CTAs'.  Each block of a group's prefix is read once (the table of
 // the group's first member) and warp w applies head hg * 4 + w to the pass's
 // 16 query rows (member m = row / G, query head h = kvh * G + row % G), as
-// two 8-column MMA tiles.  A piece's partial goes to slot c + hg * V + v, and
-// each member sequence whose rows it holds gets an arrival on its
-// (sequence, KV head) counter; the last arriver merges.
+// two 8-column MMA tiles.  A piece's partial goes to slot c + hg * V + v;
+// shared_merge_kernel merges the members' pieces after the launch.
 template <int D, int B, int LAYOUT>
-__device__ __forceinline__ void shared_prefix_cta(
-    uint8_t *smem, const CUtensorMap *tmk, const CUtensorMap *tmv, const __nv_bfloat16 *__restrict__ q,
-    __nv_bfloat16 *__restrict__ out, const int32_t *__restrict__ tables, int32_t max_blocks, int32_t H,
-    int32_t G, int32_t NB, float scale_log2, unsigned int *__restrict__ counters,
-    const int32_t *__restrict__ cu, int32_t N, int32_t NH, int32_t Hk, int32_t C, int32_t Cs, float2 *ml_ws,
-    float *acc_ws, const SharedArgs &sh, unsigned int *__restrict__ err) {
+__device__ __forceinline__ void shared_prefix_cta(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMap *tmv,
+                                                  const __nv_bfloat16 *__restrict__ q,
+                                                  const int32_t *__restrict__ tables, int32_t max_blocks, int32_t H,
+                                                  int32_t G, int32_t NB, float scale_log2, int32_t Hk, int32_t Cs,
+                                                  const SharedArgs &sh, unsigned int *__restrict__ err) {
     using Tile = MmaTile<D, B>;
     constexpr int S = Tile::kStages;
     constexpr int KT = D / 16;
@@ -690,8 +687,8 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
     if (kShared) grid_launch_dependents();
     const int32_t Cs = kShared ? sh.ctl[0] : 0;
     if (kShared && (int32_t)blockIdx.x < Cs)
-        shared_prefix_cta<D, B, LAYOUT>(smem, &tmk, &tmv, q, out, tables, max_blocks, H, G, NB, scale_log2,
-                                        counters, cu, N, NH, Hk, C, Cs, ml_ws, acc_ws, sh, err);
+        shared_prefix_cta<D, B, LAYOUT>(smem, &tmk, &tmv, q, tables, max_blocks, H, G, NB, scale_log2, Hk, Cs, sh,
+                                        err);
     else
         own_block_cta<D, B, LAYOUT, kShared>(smem, &tmk, &tmv, q, out, tables, max_blocks, lens, cu, N, H, G, NB,
                                              NH, scale_log2, ml_ws, acc_ws, counters, start_seq, Hk, C, Cs, sh,
