@@ -30,7 +30,10 @@
 //
 // Device code: decode_merge.cuh (pieces and merges), decode_plan.cuh (plan
 // kernel), decode_simt.cuh (CUDA-core kernel), decode_mma.cuh (tensor-core
-// kernel); this file holds the host side and the C ABI entry points.
+// kernel).  The attention kernels are instantiated in decode_simt.cu,
+// decode_mma_plain.cu and decode_mma_shared.cu (compiled in parallel); this
+// file holds the plan and merge kernels, the host side and the C ABI entry
+// points.
 //
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -39,11 +42,9 @@
 
 #include "pa_internal.h"
 
-// Device code, in the order it builds on itself.
+#include "decode_kernels.h"
 #include "decode_merge.cuh"
 #include "decode_plan.cuh"
-#include "decode_simt.cuh"
-#include "decode_mma.cuh"
 
 namespace pa {
 
@@ -83,8 +84,6 @@ bool simt_supported(const pa_cache_desc_t *c, int G) {
     return d_ok && G >= 1 && G <= 8;
 }
 
-int simt_gmax(int G) { return G <= 1 ? 1 : (G <= 4 ? 4 : 8); }
-
 // kMmaStages stages of NH head slabs of K and of V (the shared-prefix CTAs
 // use the same ring with NH = kPlanHeads), mbarriers after the tiles, with
 // shared prefixes the query rows of the shared-prefix warps (QRows, 256
@@ -96,45 +95,8 @@ size_t mma_smem_bytes(int D, int B, int NH, bool shared) {
     return bytes;
 }
 
-template <typename T, int D, int GMAX>
-const void *simt_fn(int layout) {
-    return layout == PA_LAYOUT_SPLIT ? (const void *)decode_simt_kernel<T, D, GMAX, PA_LAYOUT_SPLIT>
-                                     : (const void *)decode_simt_kernel<T, D, GMAX, PA_LAYOUT_ROW>;
-}
-
-const void *simt_kernel_ptr(int dtype, int D, int G, int layout) {
-    const int gm = simt_gmax(G);
-#define PA_SIMT_CASE(TT, DD)                                        \
-    if (D == DD) {                                                  \
-        if (gm == 1) return simt_fn<TT, DD, 1>(layout);             \
-        if (gm == 4) return simt_fn<TT, DD, 4>(layout);             \
-        return simt_fn<TT, DD, 8>(layout);                          \
-    }
-    if (dtype == PA_F32) {
-        PA_SIMT_CASE(float, 64)
-        PA_SIMT_CASE(float, 128)
-    } else {
-        PA_SIMT_CASE(__nv_bfloat16, 64)
-        PA_SIMT_CASE(__nv_bfloat16, 128)
-        PA_SIMT_CASE(__nv_bfloat16, 256)
-    }
-#undef PA_SIMT_CASE
-    return nullptr;
-}
-
-template <int LAYOUT, bool kShared>
-const void *mma_fn(int D, int B) {
-    if (D == 128 && B == 16) return (const void *)decode_mma_kernel<128, 16, LAYOUT, kShared>;
-    if (D == 128 && B == 32) return (const void *)decode_mma_kernel<128, 32, LAYOUT, kShared>;
-    if (D == 64 && B == 16) return (const void *)decode_mma_kernel<64, 16, LAYOUT, kShared>;
-    if (D == 64 && B == 32) return (const void *)decode_mma_kernel<64, 32, LAYOUT, kShared>;
-    return nullptr;
-}
-
 const void *mma_kernel_ptr(int D, int B, int layout, bool shared) {
-    if (shared)
-        return layout == PA_LAYOUT_SPLIT ? mma_fn<PA_LAYOUT_SPLIT, true>(D, B) : mma_fn<PA_LAYOUT_ROW, true>(D, B);
-    return layout == PA_LAYOUT_SPLIT ? mma_fn<PA_LAYOUT_SPLIT, false>(D, B) : mma_fn<PA_LAYOUT_ROW, false>(D, B);
+    return shared ? mma_kernel_ptr_shared(D, B, layout) : mma_kernel_ptr_plain(D, B, layout);
 }
 
 // Occupancy-based default split count: one full wave of resident CTAs.

@@ -1,4 +1,4 @@
-// Split-K merge of decode pieces (part of decode.cu's translation unit).
+// Split-K merge of decode pieces (used by every decode translation unit).
 //
 // A piece is the partial result (running max, sum, accumulator) of one
 // (sequence, KV head) over one CTA's part of its blocks; the merge folds all

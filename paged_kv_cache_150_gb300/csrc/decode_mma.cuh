@@ -1,9 +1,12 @@
-// TMA + tensor-core decode kernel (part of decode.cu's translation unit).
+// TMA + tensor-core decode kernel (instantiated in decode_mma_plain.cu and
+// decode_mma_shared.cu).
 //
 // TMA tiles of (block, 4 KV heads) through an mbarrier ring, mma.sync for
 // S^T = K Q^T and O^T += V^T P^T; own-block CTAs and, with a plan,
 // shared-prefix CTAs in one launch.
 #pragma once
+
+#include <cuda.h>  // CUtensorMap
 
 #include "pa_internal.h"
 

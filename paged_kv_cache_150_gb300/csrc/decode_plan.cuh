@@ -1,4 +1,4 @@
-// Decode plan kernel and shared-prefix plan checks (part of decode.cu's translation unit).
+// Decode plan kernel and shared-prefix plan checks (part of decode.cu).
 //
 // One CTA per call: lengths to block counts and prefix sums, arrival
 // counters, empty outputs, per-CTA start sequences, and the check of an

@@ -1,4 +1,4 @@
-// CUDA-core decode kernel (part of decode.cu's translation unit).
+// CUDA-core decode kernel (instantiated in decode_simt.cu).
 //
 // fp32 (and bf16 shapes the tensor-core kernel does not cover): one warp per
 // KV head, warp-shuffle q.k and online softmax over one token at a time.
