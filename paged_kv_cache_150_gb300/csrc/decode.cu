@@ -23,6 +23,11 @@
 //    arrives last merges every piece (the split-K reduce, fused):
 //      out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
 //    Nothing ever waits for another CTA: the merge is done by whoever is last.
+//    Without a shared-prefix plan and with N + 1 <= kLocalCuMax, each
+//    tensor-core CTA computes the same cu[] from seq_lens in its own shared
+//    memory and starts on its blocks while the plan kernel still runs; it
+//    waits for that kernel only before its first arrival (the counters must
+//    be zeroed) and before it exits.
 // 3. With a shared-prefix plan (sequences whose tables start with the same
 //    physical blocks), part of the grid reads each shared block once for all
 //    sharers' query heads, the rest reads each sequence's own blocks, and
@@ -58,6 +63,7 @@ struct DecodePlan {
     int HPG;       // query heads per group = NH * G
     int C;         // persistent CTAs
     bool shared;   // a shared-prefix plan is used
+    bool local_cu; // tensor-core CTAs compute the prefix sums themselves (kLocalCuMax)
     size_t smem;   // dynamic shared memory of the attention kernel
     // workspace layout (byte offsets)
     size_t off_lens, off_cu, off_cnt, off_start, off_ml, off_acc;
@@ -141,12 +147,13 @@ pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_d
     }
     p->NG = c->num_kv_heads / p->NH;
     p->HPG = p->NH * G;
-    int C = opts ? opts->num_splits : 0;
+    const int threads = kernel == PA_KERNEL_MMA ? (p->NH + 1) * 32 : p->NH * 32;
+    const int C_given = opts ? opts->num_splits : 0;
+    int C = C_given;
     if (C == 0) {
         if (!need_default_splits) return PA_ERR_INVALID_ARG;
         const void *fn = kernel == PA_KERNEL_MMA ? mma_kernel_ptr(c->head_dim, c->block_size, c->layout, p->shared)
                                                  : simt_kernel_ptr(c->dtype, c->head_dim, G, c->layout);
-        const int threads = kernel == PA_KERNEL_MMA ? (p->NH + 1) * 32 : p->NH * 32;
         C = default_ctas(fn, threads, p->smem);
         if (C <= 0) return PA_ERR_CUDA;
     }
@@ -154,6 +161,21 @@ pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_d
     if (p->shared && C < 2) {  // shared prefixes need a CTA of each kind
         p->shared = false;
         p->smem = mma_smem_bytes(c->head_dim, c->block_size, p->NH, false);
+    }
+    // Without a plan, tensor-core CTAs keep their own prefix sums when they
+    // fit and the room for them leaves as many CTAs resident per SM.
+    p->local_cu = false;
+    if (kernel == PA_KERNEL_MMA && !p->shared && N + 1 <= kLocalCuMax) {
+        const size_t extra = ((size_t)(N + 1) * sizeof(int32_t) + 15) & ~(size_t)15;
+        bool fits = true;
+        if (C_given == 0) {
+            const void *fn = mma_kernel_ptr(c->head_dim, c->block_size, c->layout, false);
+            fits = default_ctas(fn, threads, p->smem + extra) == C;
+        }
+        if (fits) {
+            p->local_cu = true;
+            p->smem += extra;
+        }
     }
     const size_t slots = (size_t)C + (size_t)p->NG * N;
     size_t off = 0;
@@ -369,8 +391,9 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         int32_t NB = cache->num_blocks, Hk = cache->num_kv_heads, NHv = p.NH, Cv = p.C;
         int32_t Nv = num_seqs, Hv = num_heads, Gv = G, mb = max_blocks_per_seq;
         float sl = scale_log2;
+        int32_t local_cu = p.local_cu ? 1 : 0;
         void *args[] = {&tmk, &tmv, &qb, &ob, &block_tables, &mb, &lens_ws, &cu, &Nv, &Hv, &Hk,
-                        &Gv, &NB, &NHv, &sl, &Cv, &ml, &acc, &cnt, &start_seq, &err, &sh};
+                        &Gv, &NB, &NHv, &sl, &Cv, &ml, &acc, &cnt, &start_seq, &err, &sh, &seq_lens, &local_cu};
         if (launch_pdl(fn, grid, block, args, p.smem, s) != cudaSuccess) return PA_ERR_CUDA;
         if (p.shared) {
             // one warp per (sequence, KV head) bound: members <= N

@@ -398,12 +398,15 @@ __device__ __forceinline__ void shared_prefix_cta(uint8_t *smem, const CUtensorM
 // A CTA of the own-block part (the whole grid without a plan): CTA c of Co
 // takes its range of the flattened (head group, sequence, own block) list.
 // Consumer warp w owns KV head g * NH + w and its G query heads.  kShared:
-// sequences may start after a shared prefix (skip[seq] blocks).
+// sequences may start after a shared prefix (skip[seq] blocks).  cu[] is the
+// plan kernel's (global memory) or the CTA's own copy (shared memory); lens[]
+// is clamped here as the plan kernel clamps it; without a start table
+// (start_seq == nullptr) the CTA finds its first sequence by search.
 template <int D, int B, int LAYOUT, bool kShared>
 __device__ __forceinline__ void own_block_cta(
     uint8_t *smem, const CUtensorMap *tmk, const CUtensorMap *tmv, const __nv_bfloat16 *__restrict__ q,
     __nv_bfloat16 *__restrict__ out, const int32_t *__restrict__ tables, int32_t max_blocks,
-    const int32_t *__restrict__ lens, const int32_t *__restrict__ cu, int32_t N, int32_t H, int32_t G, int32_t NB,
+    const int32_t *__restrict__ lens, const int32_t *cu, int32_t N, int32_t H, int32_t G, int32_t NB,
     int32_t NH, float scale_log2, float2 *__restrict__ ml_ws, float *__restrict__ acc_ws,
     unsigned int *__restrict__ counters, const int32_t *__restrict__ start_seq, int32_t Hk, int32_t C,
     int32_t Cs, const SharedArgs &sh, unsigned int *__restrict__ err) {
@@ -447,8 +450,12 @@ __device__ __forceinline__ void own_block_cta(
             // the partials, q and tables that are read again.
             const uint64_t kv_policy = l2_policy_evict_first();
             BlockCursor cur, ahead;
-            cur.init_at(lo, start_seq[c], cu, N, skip);
-            ahead.init_at(lo, start_seq[c], cu, N, skip);
+            if (start_seq) {
+                cur.init_at(lo, start_seq[c], cu, N, skip);
+            } else {
+                cur.init(lo, cu, N, skip);
+            }
+            ahead = cur;
             // Block-table entries are loaded kTablePrefetch blocks ahead of their
             // TMA issue (a register shift ring), so the L2 latency of the table
             // read is off the issue path.
@@ -503,7 +510,11 @@ __device__ __forceinline__ void own_block_cta(
     float o[KT][4];
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     BlockCursor cur;
-    cur.init_at(lo, start_seq[c], cu, N, skip);
+    if (start_seq) {
+        cur.init_at(lo, start_seq[c], cu, N, skip);
+    } else {
+        cur.init(lo, cu, N, skip);
+    }
     bool seg_start = true, seg_from_first = false, have_next_q = false;
     // B operand of S^T = K Q^T: column n = query head r of this KV head.
     auto load_q = [&](uint32_t (&dst)[KT][2], int32_t seq, int32_t grp) {
@@ -524,6 +535,7 @@ __device__ __forceinline__ void own_block_cta(
         const int32_t kvh = cur.g * NH + warp;
         if (seg_start) {
             L = lens[cur.seq];
+            L = (L < 0 || L > max_blocks * B) ? 0 : L;  // as the plan kernel clamps it
             if (have_next_q) {
 #pragma unroll
                 for (int kk = 0; kk < KT; ++kk) {
@@ -644,6 +656,9 @@ __device__ __forceinline__ void own_block_cta(
                 if (!(kShared && cur.b0 > 0)) {
                     const PieceRange rg[2] = {own_range(ml_ws, acc_ws, cu, N, cur.seq, cur.g, warp, G, HPG, W, Ce),
                                               no_range()};
+                    // The plan kernel zeroes the arrival counters: it has
+                    // finished before the first arrival (at once if it has).
+                    grid_dependency_wait();
                     if (arrive_piece(counters, rg, counter_index(cur.seq, kvh, N, NH), lane) && lane == 0)
                         pending[warp][pending[warp][0] >= 0 ? 1 : 0] = cur.g * N + cur.seq;
                 }
@@ -668,6 +683,53 @@ __device__ __forceinline__ void own_block_cta(
     }
 }
 
+// Block counts of the N sequences and their exclusive prefix sums, written to
+// cu_l[0..N] in shared memory by the whole CTA: the plan kernel's cu[] (the
+// same clamping of bad lengths to 0), without waiting for that kernel.  Each
+// thread scans a contiguous chunk; one block-wide scan joins the chunks.
+__device__ __forceinline__ void local_prefix_sums(const int32_t *__restrict__ seq_lens, int32_t N, int32_t B,
+                                                  int32_t max_len, int32_t *cu_l) {
+    __shared__ int32_t warp_sum[32];
+    const int32_t t = threadIdx.x, nt = blockDim.x;
+    const int lane = t & 31, w = t >> 5, nw = (nt + 31) >> 5;
+    for (int32_t i = t; i < N; i += nt) {
+        int32_t L = seq_lens[i];
+        L = (L < 0 || L > max_len) ? 0 : L;
+        cu_l[i] = (L + B - 1) / B;
+    }
+    __syncthreads();
+    const int32_t per = (N + nt - 1) / nt;
+    const int32_t i0 = min(t * per, N), i1 = min(i0 + per, N);
+    int32_t mine = 0;
+    for (int32_t i = i0; i < i1; ++i) mine += cu_l[i];
+    int32_t x = mine;  // inclusive scan of the chunk sums within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sum[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int32_t v = lane < nw ? warp_sum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
+        }
+        warp_sum[lane] = v;
+    }
+    __syncthreads();
+    int32_t run = x - mine + (w > 0 ? warp_sum[w - 1] : 0);  // exclusive prefix of this chunk
+    for (int32_t i = i0; i < i1; ++i) {
+        const int32_t nb = cu_l[i];
+        cu_l[i] = run;
+        run += nb;
+    }
+    if (t == nt - 1) cu_l[N] = run;  // the last chunk ends at N: run is the total
+    __syncthreads();
+}
+
 // The attention launch.  Without a plan (kShared = false) every CTA is an
 // own-block CTA.  With one, the plan kernel gives CTAs [0, Cs) to the shared
 // prefixes and the rest to the sequences' own blocks; both kinds run at once
@@ -680,11 +742,28 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
     const int32_t *__restrict__ cu, int32_t N, int32_t H, int32_t Hk, int32_t G, int32_t NB,
     int32_t NH, float scale_log2, int32_t C, float2 *__restrict__ ml_ws, float *__restrict__ acc_ws,
     unsigned int *__restrict__ counters, const int32_t *__restrict__ start_seq, unsigned int *__restrict__ err,
-    const SharedArgs sh) {
+    const SharedArgs sh, const int32_t *__restrict__ seq_lens, int32_t local_cu) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
 
-    grid_dependency_wait();  // the plan kernel's cu[] / lens / split (programmatic launch)
+    // local_cu (no plan, N + 1 <= kLocalCuMax; the host adds the room): the
+    // CTA computes cu[] from seq_lens itself and starts on its blocks while
+    // the plan kernel still runs; it waits for that kernel only before its
+    // first arrival (the counters) and before it ends.  Otherwise it waits
+    // here for the plan kernel's cu[], lens and start table.
+    const bool local = !kShared && local_cu != 0;
+    const int32_t *cu_p = cu, *lens_p = lens, *start_p = start_seq;  // generic: global or shared memory
+    if (local) {
+        using Tile = MmaTile<D, B>;
+        int32_t *cu_l = (int32_t *)(smem + (size_t)Tile::kStages * 2 * NH * Tile::kSlabBytes +
+                                    2 * Tile::kStages * sizeof(uint64_t));
+        local_prefix_sums(seq_lens, N, B, max_blocks * B, cu_l);
+        cu_p = cu_l;
+        lens_p = seq_lens;
+        start_p = nullptr;
+    } else {
+        grid_dependency_wait();  // the plan kernel's cu[] / lens / split (programmatic launch)
+    }
     // With a plan, the merge kernel may become resident as CTAs finish and
     // work out its piece ranges from the plan while the last ones run.
     if (kShared) grid_launch_dependents();
@@ -693,9 +772,12 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
         shared_prefix_cta<D, B, LAYOUT>(smem, &tmk, &tmv, q, tables, max_blocks, H, G, NB, scale_log2, Hk, Cs, sh,
                                         err);
     else
-        own_block_cta<D, B, LAYOUT, kShared>(smem, &tmk, &tmv, q, out, tables, max_blocks, lens, cu, N, H, G, NB,
-                                             NH, scale_log2, ml_ws, acc_ws, counters, start_seq, Hk, C, Cs, sh,
+        own_block_cta<D, B, LAYOUT, kShared>(smem, &tmk, &tmv, q, out, tables, max_blocks, lens_p, cu_p, N, H, G,
+                                             NB, NH, scale_log2, ml_ws, acc_ws, counters, start_p, Hk, C, Cs, sh,
                                              err);
+    // The grid ends after the plan kernel (which also writes the zero output
+    // of empty sequences), as a grid that waited at its start does.
+    if (local) grid_dependency_wait();
 }
 
 }  // namespace pa

@@ -36,6 +36,9 @@ constexpr int kTablePrefetch = 4;
 // SM) were 2-3% slower on every workload.
 constexpr int kMmaStages = 2;
 constexpr int kMmaMaxHeads = 4;
+// Sequences (+ 1) whose block-count prefix sums a tensor-core CTA computes in
+// its own shared memory (16 KiB) instead of waiting for the plan kernel's.
+constexpr int kLocalCuMax = 4096;
 
 // ---------------------------------------------------------------- work split
 // CTA c of C owns flattened blocks [split_begin(c), split_begin(c + 1)).

@@ -179,12 +179,15 @@ def test_bounded_wait_times_out_and_the_context_stays_usable():
 
 
 @pytest.mark.parametrize("kernel", ["auto", "simt"])
-def test_many_sequences_prefix_sums_in_global_memory(kernel):
+@pytest.mark.parametrize("num_seqs", [3000, 5000])
+def test_many_sequences_prefix_sums_in_global_memory(kernel, num_seqs):
     """3000 sequences: more than the plan kernel keeps in shared memory, so
-    the prefix sums and the start search run from global memory; empty
-    sequences scattered through the batch."""
+    its prefix sums and start search run from global memory, while each
+    tensor-core CTA still computes its own copy (chunks of 19 per thread).
+    5000: more than a tensor-core CTA keeps, so it waits for the plan
+    kernel's.  Empty sequences scattered through the batch."""
     rng = np.random.default_rng(31)
-    lens = rng.integers(1, 45, size=3000)
+    lens = rng.integers(1, 45, size=num_seqs)
     lens[::97] = 0
     wl = inputs.decode_workload("many", lens, 16, 8, 128, 16, "bf16", seed=31, pool_factor=1.2)
     dev, host = host_values(wl, "cuda")
