@@ -179,13 +179,14 @@ def test_bounded_wait_times_out_and_the_context_stays_usable():
 
 
 @pytest.mark.parametrize("kernel", ["auto", "simt"])
-@pytest.mark.parametrize("num_seqs", [3000, 5000])
+@pytest.mark.parametrize("num_seqs", [3000, 4095, 4096])
 def test_many_sequences_prefix_sums_in_global_memory(kernel, num_seqs):
     """3000 sequences: more than the plan kernel keeps in shared memory, so
     its prefix sums and start search run from global memory, while each
     tensor-core CTA still computes its own copy (chunks of 19 per thread).
-    5000: more than a tensor-core CTA keeps, so it waits for the plan
-    kernel's.  Empty sequences scattered through the batch."""
+    4095: the largest batch whose prefix sums (4096 entries, 16 KiB) a
+    tensor-core CTA keeps; 4096: the smallest it leaves to the plan kernel.
+    Empty sequences scattered through the batch."""
     rng = np.random.default_rng(31)
     lens = rng.integers(1, 45, size=num_seqs)
     lens[::97] = 0
