@@ -44,6 +44,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <vector>
 
 #include "pa_internal.h"
 
@@ -105,8 +106,26 @@ const void *mma_kernel_ptr(int D, int B, int layout, bool shared) {
     return shared ? mma_kernel_ptr_shared(D, B, layout) : mma_kernel_ptr_plain(D, B, layout);
 }
 
-// Occupancy-based default split count: one full wave of resident CTAs.
+// Occupancy-based default split count: one full wave of resident CTAs.  The
+// answer is fixed per (device, kernel, threads, shared memory) and cached: the
+// occupancy query costs about a microsecond of host time per call.
 int default_ctas(const void *fn, int threads, size_t smem) {
+    struct Entry {
+        int dev;
+        const void *fn;
+        int threads;
+        size_t smem;
+        int ctas;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (const Entry &e : cache)
+            if (e.dev == dev && e.fn == fn && e.threads == threads && e.smem == smem) return e.ctas;
+    }
     const int sms = num_sms();
     if (sms <= 0) return -1;
     int per_sm = 0;
@@ -114,7 +133,10 @@ int default_ctas(const void *fn, int threads, size_t smem) {
         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return -1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess) return -1;
-    return sms * std::max(per_sm, 1);
+    const int ctas = sms * std::max(per_sm, 1);
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() < 1024) cache.push_back(Entry{dev, fn, threads, smem, ctas});
+    return ctas;
 }
 
 pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_decode_opts_t *opts,
@@ -163,14 +185,15 @@ pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_d
         p->smem = mma_smem_bytes(c->head_dim, c->block_size, p->NH, false);
     }
     // Without a plan, tensor-core CTAs keep their own prefix sums when they
-    // fit and the room for them leaves as many CTAs resident per SM.
+    // fit and the room for them leaves as many CTAs resident per SM (checked
+    // for the largest room, kLocalCuMax entries: one cached answer per shape).
     p->local_cu = false;
     if (kernel == PA_KERNEL_MMA && !p->shared && N + 1 <= kLocalCuMax) {
         const size_t extra = ((size_t)(N + 1) * sizeof(int32_t) + 15) & ~(size_t)15;
         bool fits = true;
         if (C_given == 0) {
             const void *fn = mma_kernel_ptr(c->head_dim, c->block_size, c->layout, false);
-            fits = default_ctas(fn, threads, p->smem + extra) == C;
+            fits = default_ctas(fn, threads, p->smem + (size_t)kLocalCuMax * sizeof(int32_t)) == C;
         }
         if (fits) {
             p->local_cu = true;

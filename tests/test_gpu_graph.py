@@ -58,3 +58,11 @@ def test_step_replayed_from_a_cuda_graph(cfg, kw, shared):
     graph.replay()
     torch.cuda.synchronize()
     assert max_abs_err(out, oracle_decode(wl, host2, r)) <= TOL["bf16"]
+
+
+def test_calls_take_torchs_current_stream():
+    assert (pa._stream().value or 0) == torch.cuda.current_stream().cuda_stream
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        assert pa._stream().value == side.cuda_stream
+    assert (pa._stream().value or 0) == torch.cuda.current_stream().cuda_stream
