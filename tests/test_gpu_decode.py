@@ -197,3 +197,34 @@ def test_many_sequences_prefix_sums_in_global_memory(kernel, num_seqs):
     pairs = sample_pairs(wl, 400)
     assert max_abs_err(g["out"], oracle_decode(wl, host, r, pairs=pairs), pairs) <= TOL["bf16"]
     assert (g["out"][::97] == 0).all()
+
+
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
+def test_one_long_sequence_merged_from_every_cta(kernel):
+    """A 131,077-token sequence beside short ones (one of them exactly 256
+    blocks).  With the default split the tensor-core kernel cuts its blocks
+    across about 147 CTAs per head group (the CUDA-core kernel across all of
+    its CTAs), so the last arriver of each (sequence, KV head) merges that
+    many pieces."""
+    lens = [131072 + 5, 17, 1, 4096]
+    wl = inputs.decode_workload("long", lens, 64, 8, 128, 16, "bf16", seed=41, pool_factor=1.05)
+    dev, host = host_values(wl, "cuda")
+    r = oracle_step(wl, host)
+    g = gpu_step(wl, dev, kernel=kernel)
+    pairs = [(0, h) for h in range(0, 64, 7)] + [(0, 63), (1, 3), (2, 63), (3, 10), (3, 32)]
+    ref = oracle_decode(wl, host, r, pairs=pairs)
+    assert max_abs_err(g["out"], ref, pairs) <= TOL["bf16"]
+    assert torch.isfinite(g["out"].float()).all()
+
+
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
+def test_batch_of_only_empty_sequences(kernel):
+    """No blocks at all: every attention CTA leaves at once; the output is
+    all zeros (written by the plan kernel) and no error is recorded."""
+    wl = inputs.decode_workload("empty", [0, 0, 0, 0, 0], 16, 8, 128, 16, "bf16", seed=43, pool_factor=1.0)
+    dev, host = host_values(wl, "cpu")
+    out = torch.full_like(dev["q"], float("nan"))
+    g = gpu_step(wl, dev, decode=False)
+    pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale, out=out, kernel=kernel)
+    assert pa.pa_get_device_error(raise_on_error=False) == 0
+    assert (out == 0).all()
