@@ -429,9 +429,10 @@ def time_write_copy(step, iters, peak):
     return out
 
 
-def oracle_baseline(step, max_groups, threads):
+def oracle_baseline(step, max_groups, threads, repeat=1):
     """The CPU oracle, as it stands, on a bounded sample of the workload:
-    whole (sequence, KV head) groups, all G query heads of each."""
+    whole (sequence, KV head) groups, all G query heads of each (timed
+    ``repeat`` times over, for samples too small to time once)."""
     import oracle
 
     wl = step.wl
@@ -447,10 +448,30 @@ def oracle_baseline(step, max_groups, threads):
     groups = [(s, kh) for s in range(wl.num_seqs) for kh in range(wl.num_kv_heads)][:max_groups]
     pairs = [(s, kh * G + j) for s, kh in groups for j in range(G)]
     t0 = time.perf_counter()
-    ref = oracle.decode(host["q"], kc, vc, tables, r["lens"], wl.scale, pairs=pairs, num_threads=threads)
+    for _ in range(repeat):
+        ref = oracle.decode(host["q"], kc, vc, tables, r["lens"], wl.scale, pairs=pairs, num_threads=threads)
     dt = time.perf_counter() - t0
-    bytes_ = sum(int(wl.seq_lens[s]) * wl.head_dim * 2 * wl.elem_bytes for s, _ in groups)
+    bytes_ = repeat * sum(int(wl.seq_lens[s]) * wl.head_dim * 2 * wl.elem_bytes for s, _ in groups)
     return ref, pairs, dt, bytes_, len(groups)
+
+
+def oracle_single_thread():
+    """The oracle with one host thread on the three smaller workloads (cfg0
+    whole, cfg1 and cfg2 on a sample of (sequence, KV head) groups): a
+    per-core figure beside the all-core baseline."""
+    import torch
+
+    out = {}
+    for cfg, kw, max_groups, repeat in (("cfg0", {}, 10 ** 9, 200), ("cfg1", {}, 10 ** 9, 1), ("cfg2", {}, 768, 1)):
+        st = Step(cfg, kw)
+        st.keep_initial_host_copy()
+        _, _, dt, nbytes, ngroups = oracle_baseline(st, max_groups, 1, repeat)
+        out[st.wl.name] = {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+                           "sample": "%d of %d (sequence, KV head) groups, all query heads, x%d, %.2f s" %
+                                     (ngroups, st.wl.num_seqs * st.wl.num_kv_heads, repeat, dt)}
+        del st
+        torch.cuda.empty_cache()
+    return out
 
 
 def allocation_simulator():
@@ -560,6 +581,8 @@ def run_ours(args, rank, world):
                           "tolerance": 2e-2}
     del step
     torch.cuda.empty_cache()
+    if do_cpu:
+        line["cpu_baseline"]["single_thread"] = oracle_single_thread()
     if not args.no_extra:
         extra = {}
         for cfg, kw in EXTRA:
