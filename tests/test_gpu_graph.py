@@ -66,3 +66,39 @@ def test_calls_take_torchs_current_stream():
     with torch.cuda.stream(side):
         assert pa._stream().value == side.cuda_stream
     assert (pa._stream().value or 0) == torch.cuda.current_stream().cuda_stream
+
+
+def test_concurrent_decodes_on_two_streams_match_sequential_ones():
+    """Two batches decoded at the same time on two streams, each with its
+    own workspace: the library keeps no other per-call state on the device,
+    so the outputs equal those of the same calls made one after another."""
+    wls = [inputs.workload("cfg2", small=True), inputs.workload("cfg4", small=True)]
+    steps = []
+    for wl in wls:
+        dev, host = host_values(wl, "cpu")
+        g = gpu_step(wl, dev, decode=False)
+        ws = torch.empty(pa.pa_decode_workspace_bytes(g["k_cache"], wl.num_seqs, wl.num_q_heads),
+                         dtype=torch.uint8, device="cuda")
+        steps.append((wl, g, ws))
+
+    def decode(wl, g, ws, out):
+        pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale, out=out, workspace=ws)
+
+    ref = []
+    for wl, g, ws in steps:
+        out = torch.empty_like(g["q"])
+        decode(wl, g, ws, out)
+        ref.append(out)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.empty_like(g["q"]) for _, g, _ in steps]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for _ in range(20):
+        for (wl, g, ws), s, out in zip(steps, streams, outs):
+            with torch.cuda.stream(s):
+                decode(wl, g, ws, out)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error(raise_on_error=False) == 0
+    for out, r in zip(outs, ref):
+        assert torch.equal(out, r)
