@@ -26,6 +26,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -127,7 +128,9 @@ class ClockSampler:
 
     def __init__(self, device_index):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_r%d.csv" % os.getpid())
+        # raw samples: PA_CLOCKS_DIR if set (to keep them), else the temp directory
+        self.path = os.path.join(os.environ.get("PA_CLOCKS_DIR") or tempfile.gettempdir(),
+                                 "pa_clocks_r%d.csv" % os.getpid())
         try:
             import torch
 
