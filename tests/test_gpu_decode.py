@@ -228,3 +228,21 @@ def test_batch_of_only_empty_sequences(kernel):
     pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale, out=out, kernel=kernel)
     assert pa.pa_get_device_error(raise_on_error=False) == 0
     assert (out == 0).all()
+
+
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
+def test_large_scores_underflow_cleanly_through_the_merge(kernel):
+    """q scaled 50x: scores spread over about +-150, so most softmax weights
+    underflow to exactly 0 and the pieces of a split sequence carry maxima
+    far apart (their rescaling factors 2^(m_p - M) reach 0).  The result
+    stays finite and matches the oracle."""
+    lens = [20000, 3, 700, 17, 4096 + 5]
+    wl = inputs.decode_workload("peaked", lens, 32, 8, 128, 16, "bf16", seed=47, pool_factor=1.1)
+    dev, host = host_values(wl, "cpu")
+    dev["q"] = (dev["q"].float() * 50.0).to(torch.bfloat16)
+    host["q"] = inputs.to_numpy_elems(dev["q"]).copy()
+    r = oracle_step(wl, host)
+    ref = oracle_decode(wl, host, r)
+    g = gpu_step(wl, dev, kernel=kernel)
+    assert torch.isfinite(g["out"].float()).all()
+    assert max_abs_err(g["out"], ref) <= TOL["bf16"]
