@@ -1,0 +1,45 @@
+"""Seeded random sweep against the oracle: element type, KV heads, query
+heads per KV head (including 3), head dim, block size, cache layout, batch
+size, lengths (with 0, 1 and values at block edges) and split counts, on
+both kernels.  The cache write is compared byte for byte, decode within the
+tolerance of its element type."""
+import numpy as np
+import pytest
+
+from paged_kv_cache_150_gb300 import inputs
+from _pipeline import TOL, gpu_step, host_values, max_abs_err, oracle_decode, oracle_step
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(seed):
+    rng = np.random.default_rng(10_000 + seed)
+    dtype = "f32" if rng.random() < 0.25 else "bf16"
+    Hk = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 3, 4, 8]))
+    if dtype == "f32":
+        D, B = int(rng.choice([64, 128])), int(rng.choice([4, 8, 16, 32]))
+    else:
+        D, B = int(rng.choice([64, 128, 128, 256])), int(rng.choice([8, 16, 16, 32]))
+    layout = "split" if rng.random() < 0.25 else "row"
+    N = int(rng.integers(1, 24))
+    edges = [0, 1, B - 1, B, B + 1, 2 * B, 3 * B + 1]
+    lens = [int(rng.choice(edges)) if rng.random() < 0.4 else int(rng.integers(1, 40 * B)) for _ in range(N)]
+    splits = int(rng.choice([0, 0, 1, 2, 5, 13]))
+    return dtype, Hk * G, Hk, D, B, layout, lens, splits
+
+
+@pytest.mark.parametrize("seed", range(160))
+def test_random_shapes_match_the_oracle(seed):
+    dtype, H, Hk, D, B, layout, lens, splits = _case(seed)
+    wl = inputs.decode_workload("fuzz%d" % seed, lens, H, Hk, D, B, dtype, seed=20_000 + seed, pool_factor=1.3)
+    dev, host = host_values(wl, "cpu", layout=layout)
+    r = oracle_step(wl, host)
+    ref = oracle_decode(wl, host, r)
+    shape = (dtype, H, Hk, D, B, layout, splits)
+    for kernel in ("auto", "simt"):
+        g = gpu_step(wl, {k: v.clone() for k, v in dev.items()}, kernel=kernel, num_splits=splits)
+        assert np.array_equal(inputs.to_numpy_elems(g["k_cache"]), r["k_cache"]), shape
+        assert np.array_equal(inputs.to_numpy_elems(g["v_cache"]), r["v_cache"]), shape
+        err = max_abs_err(g["out"], ref)
+        assert err <= TOL[dtype], (kernel, err, shape)
