@@ -1,8 +1,12 @@
-"""Seeded random sweep against the oracle: element type, KV heads, query
-heads per KV head (including 3), head dim, block size, cache layout, batch
-size, lengths (with 0, 1 and values at block edges) and split counts, on
-both kernels.  The cache write is compared byte for byte, decode within the
-tolerance of its element type."""
+"""Seeded random sweeps against the oracle.
+
+Independent sequences: element type, KV heads, query heads per KV head
+(including 3), head dim, block size, cache layout, batch size, lengths
+(with 0, 1 and values at block edges) and split counts, on both kernels;
+the cache write is compared byte for byte, decode within the tolerance of
+its element type.  Parallel sampling with a shared-prefix plan: random
+prompt counts and lengths, samples, appended tokens, head ratios, head
+dims, block sizes, layouts and split counts."""
 import numpy as np
 import pytest
 
@@ -43,3 +47,32 @@ def test_random_shapes_match_the_oracle(seed):
         assert np.array_equal(inputs.to_numpy_elems(g["v_cache"]), r["v_cache"]), shape
         err = max_abs_err(g["out"], ref)
         assert err <= TOL[dtype], (kernel, err, shape)
+
+
+def _sampling_case(seed):
+    rng = np.random.default_rng(30_000 + seed)
+    Hk, G = int(rng.choice([4, 8])), int(rng.choice([1, 2, 4, 8]))
+    D, B = int(rng.choice([64, 128])), int(rng.choice([16, 32]))
+    prompts, samples = int(rng.integers(1, 6)), int(rng.integers(2, 12))
+    prompt_len = int(rng.integers(B + 1, 40 * B))  # at least one whole block to share
+    max_append = int(rng.integers(1, 3 * B))
+    layout = "split" if rng.random() < 0.25 else "row"
+    splits = int(rng.choice([0, 0, 2, 5, 13]))
+    return prompts, prompt_len, samples, max_append, Hk * G, Hk, D, B, layout, splits
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_parallel_sampling_with_a_shared_prefix_plan(seed):
+    """Forked prompts decoded with a shared-prefix plan, over random prompt
+    counts and lengths, samples per prompt, appended tokens, head ratios,
+    head dims, block sizes, layouts and split counts."""
+    prompts, plen, samples, max_append, H, Hk, D, B, layout, splits = _sampling_case(seed)
+    wl = inputs.sampling_workload("sfuzz%d" % seed, prompts, plen, samples, max_append, H, Hk, D, B, "bf16",
+                                  40_000 + seed)
+    dev, host = host_values(wl, "cpu", layout=layout)
+    r = oracle_step(wl, host)
+    ref = oracle_decode(wl, host, r)
+    g = gpu_step(wl, dev, shared=True, num_splits=splits)
+    assert g["plan_info"]["num_groups"] == prompts
+    err = max_abs_err(g["out"], ref)
+    assert err <= TOL["bf16"], (err, prompts, plen, samples, max_append, H, Hk, D, B, layout, splits)
