@@ -264,8 +264,10 @@ class Step:
         self.out = torch.empty_like(vals["q"])
         ws = pa.pa_decode_workspace_bytes(vals["k_cache"], wl.num_seqs, wl.num_q_heads, shared=shared)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device="cuda")
-        # cache write, plan kernel, attention kernel; block copy and shared-prefix merge when present
-        self.kernel_launches = 3 + (1 if pairs.shape[0] else 0) + (1 if shared else 0)
+        # block copy when there are pairs, the cache write, and the kernels of the
+        # decode call as the library counts them (plan, attention, merges)
+        self.kernel_launches = (1 if pairs.shape[0] else 0) + 1 + pa.pa_decode_launch_count(
+            vals["k_cache"], wl.num_seqs, wl.num_q_heads, wl.max_blocks_per_seq, shared=shared, host_seq_lens=lens)
         H, D, eb = wl.num_q_heads, wl.head_dim, wl.elem_bytes
         self.kv_bytes = wl.kv_bytes_read()
         # distinct physical blocks the decode reads (shared prefixes counted once)
@@ -286,8 +288,10 @@ class Step:
         if self.pairs.shape[0]:
             pa.pa_copy_blocks(v["k_cache"], v["v_cache"], self.pairs)
         pa.pa_reshape_and_cache(v["k"], v["v"], self.slots, v["k_cache"], v["v_cache"])
+        # the host copy of the lengths, as a serving loop that builds its tables on the host has it
         pa.pa_decode(v["q"], v["k_cache"], v["v_cache"], self.tables, self.lens, self.wl.scale, out=self.out,
-                     workspace=self.workspace, events=events, shared_plan=self.plan)
+                     workspace=self.workspace, events=events, shared_plan=self.plan,
+                     host_seq_lens=self.host["lens"])
 
 
 def _events(n):

@@ -171,6 +171,14 @@ typedef struct pa_decode_opts {
     pa_event_t ev_partial_begin; /* optional: recorded just before the attention kernel */
     pa_event_t ev_partial_end;   /* optional: recorded just after the attention kernel */
     const int32_t *shared_plan;  /* optional device copy of a pa_shared_plan_build plan (NULL = none) */
+    /* Optional HOST copy of seq_lens (num_seqs entries; NULL = none), a hint
+     * read on the host during the call.  With it, when some sequence is cut
+     * into 5 or more pieces (long contexts), those sequences are merged by a
+     * second kernel that spreads their merges over the GPU instead of
+     * leaving each to the CTA that finishes last.  Without it, or with any
+     * other values, the results are the same: the device decides per
+     * sequence from seq_lens itself; only which merge path runs changes. */
+    const int32_t *host_seq_lens;
 } pa_decode_opts_t;
 
 size_t pa_decode_workspace_bytes(const pa_cache_desc_t *cache, int32_t num_seqs, int32_t num_heads,
@@ -275,6 +283,14 @@ pa_status_t pa_shared_plan_build(const int32_t *block_tables, int32_t max_blocks
  * device for this shape, or a negative pa_status_t. */
 int32_t pa_decode_default_splits(const pa_cache_desc_t *cache, int32_t num_heads,
                                  const pa_decode_opts_t *opts);
+
+/* Kernels that one pa_decode call with these arguments launches on the
+ * current device (its plan kernel, the attention kernel and the merge
+ * kernels its options bring in), assuming q is 16-byte aligned; or a
+ * negative pa_status_t.  Host-only: launches nothing, reads only host memory
+ * (opts->host_seq_lens when given). */
+int32_t pa_decode_launch_count(const pa_cache_desc_t *cache, int32_t num_seqs, int32_t num_heads,
+                               int32_t max_blocks_per_seq, const pa_decode_opts_t *opts);
 
 /* Host mirror of the decode work split (the kernels use the same integer
  * formulas): CTA c of num_splits owns flattened blocks [begin, end) of

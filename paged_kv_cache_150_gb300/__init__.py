@@ -145,6 +145,27 @@ def pa_decode_workspace_bytes(k_cache, num_seqs, num_heads, num_splits=0, kernel
     return int(n)
 
 
+def pa_decode_launch_count(k_cache, num_seqs, num_heads, max_blocks_per_seq, num_splits=0, kernel="auto",
+                           shared=False, host_seq_lens=None):
+    """Kernels one pa_decode call with these arguments launches (plan kernel,
+    attention kernel and the merge kernels its options bring in)."""
+    desc = _cache_desc_from_k(k_cache)
+    o = _opts(num_splits, kernel, None)
+    if shared:
+        o.shared_plan = ctypes.c_void_p(1)  # only tested for NULL here
+    host_lens = None
+    if host_seq_lens is not None:
+        host_lens = np.ascontiguousarray(np.asarray(host_seq_lens, dtype=np.int32))
+        if host_lens.shape != (int(num_seqs),):
+            raise ValueError("host_seq_lens must be [num_seqs]")
+        o.host_seq_lens = host_lens.ctypes.data
+    n = _lib.load().pa_decode_launch_count(ctypes.byref(desc), int(num_seqs), int(num_heads),
+                                           int(max_blocks_per_seq), ctypes.byref(o))
+    if n < 0:
+        raise PagedAttentionError("pa_decode_launch_count", n)
+    return int(n)
+
+
 def pa_decode_default_splits(k_cache, num_heads, kernel="auto"):
     desc = _cache_desc_from_k(k_cache)
     o = _opts(0, kernel, None)
@@ -155,13 +176,16 @@ def pa_decode_default_splits(k_cache, num_heads, kernel="auto"):
 
 
 def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None, workspace=None,
-              num_splits=0, kernel="auto", events=None, shared_plan=None):
+              num_splits=0, kernel="auto", events=None, shared_plan=None, host_seq_lens=None):
     """Decode attention through block tables; returns ``out`` [N, H, D].
 
     ``events``: optional (begin, end) torch.cuda.Event pair recorded around the
     attention kernel on the current stream.  ``shared_plan``: optional device
     int32 tensor from shared_prefix_plan (built from the same tables and
-    lengths), so that blocks shared by several sequences are read once."""
+    lengths), so that blocks shared by several sequences are read once.
+    ``host_seq_lens``: optional host copy of seq_lens (numpy or CPU tensor), a
+    hint that lets long contexts be merged across the GPU; the results do
+    not depend on it."""
     torch = _torch()
     desc = _cache_desc(k_cache, v_cache)
     N, H, D = q.shape
@@ -174,6 +198,12 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None, work
     elif out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("out must match q")
     o = _opts(num_splits, kernel, events, shared_plan)
+    host_lens = None
+    if host_seq_lens is not None:
+        host_lens = np.ascontiguousarray(np.asarray(host_seq_lens, dtype=np.int32))
+        if host_lens.shape != (N,):
+            raise ValueError("host_seq_lens must be [num_seqs]")
+        o.host_seq_lens = host_lens.ctypes.data
     lib = _lib.load()
     if workspace is None:  # a caller's workspace is checked by the library (PA_ERR_WORKSPACE)
         need = lib.pa_decode_workspace_bytes(ctypes.byref(desc), N, H, ctypes.byref(o))
@@ -428,7 +458,7 @@ def version():
 
 __all__ = [
     "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_workspace_bytes", "pa_decode_no_alloc",
-    "pa_decode_default_splits", "pa_get_device_error", "pa_selftest_wait_timeout", "pa_split_range",
-    "pa_split_owner",
+    "pa_decode_default_splits", "pa_decode_launch_count", "pa_get_device_error", "pa_selftest_wait_timeout",
+    "pa_split_range", "pa_split_owner",
     "BlockManager", "PagedAttentionError", "simulate", "version",
 ]

@@ -53,7 +53,7 @@ class SimResult(ctypes.Structure):
 class DecodeOpts(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int32), ("kernel", ctypes.c_int32),
                 ("ev_partial_begin", ctypes.c_void_p), ("ev_partial_end", ctypes.c_void_p),
-                ("shared_plan", ctypes.c_void_p)]
+                ("shared_plan", ctypes.c_void_p), ("host_seq_lens", ctypes.c_void_p)]
 
 
 class SharedPlanInfo(ctypes.Structure):
@@ -82,6 +82,7 @@ SIGNATURES = {
     "pa_decode": (_I32, [_P, _P, _P, _P, _DESC, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P,
                          ctypes.c_size_t, _OPTS, _P]),
     "pa_decode_default_splits": (_I32, [_DESC, _I32, _OPTS]),
+    "pa_decode_launch_count": (_I32, [_DESC, _I32, _I32, _I32, _OPTS]),
     "pa_decode_no_alloc": (_I32, [_P, _P, _P, _P, _DESC, _P, _I32, _P, _I32, _I32, ctypes.c_float, _OPTS, _P]),
     "pa_split_range": (None, [_I64, _I32, _I32, _PI64, _PI64]),
     "pa_split_owner": (_I32, [_I64, _I32, _I64]),

@@ -102,6 +102,41 @@ size_t mma_smem_bytes(int D, int B, int NH, bool shared) {
     return bytes;
 }
 
+// Pieces from which a (sequence, KV head) is merged by long_merge_kernel
+// rather than by the CTA whose piece arrives last.
+constexpr int32_t kLongMergePieces = 8;
+
+// kLongMergePieces if, with these host lengths (clamped as the plan kernel
+// clamps them), some sequence is cut into that many pieces; else 0.  A hint
+// only: the device decides per sequence from its own seq_lens.
+int32_t long_merge_pieces(const int32_t *host_lens, int32_t N, int32_t B, int32_t max_len, int32_t NG, int32_t C) {
+    std::vector<int64_t> cu((size_t)N + 1, 0);
+    for (int32_t i = 0; i < N; ++i) {
+        int32_t L = host_lens[i];
+        if (L < 0 || L > max_len) L = 0;
+        cu[(size_t)i + 1] = cu[(size_t)i] + (L + B - 1) / B;
+    }
+    const int64_t Wg = cu[(size_t)N], W = (int64_t)NG * Wg;
+    if (W == 0) return 0;
+    const int64_t Ce = std::min<int64_t>(C, W);
+    for (int32_t g = 0; g < NG; ++g)
+        for (int32_t i = 0; i < N; ++i) {
+            const int64_t nb = cu[(size_t)i + 1] - cu[(size_t)i];
+            if (nb == 0) continue;
+            const int64_t x0 = g * Wg + cu[(size_t)i];
+            if (split_owner(x0 + nb - 1, W, Ce) - split_owner(x0, W, Ce) + 1 >= kLongMergePieces)
+                return kLongMergePieces;
+        }
+    return 0;
+}
+
+// The min_pieces of a call: long_merge_pieces from the host hint, for the
+// tensor-core kernel without a shared-prefix plan; else 0.
+int32_t call_min_pieces(const DecodePlan &p, const pa_decode_opts_t *opts, int32_t N, int32_t B, int32_t max_len) {
+    if (p.kernel != PA_KERNEL_MMA || p.shared || !opts || !opts->host_seq_lens) return 0;
+    return long_merge_pieces(opts->host_seq_lens, N, B, max_len, p.NG, p.C);
+}
+
 const void *mma_kernel_ptr(int D, int B, int layout, bool shared) {
     return shared ? mma_kernel_ptr_shared(D, B, layout) : mma_kernel_ptr_plain(D, B, layout);
 }
@@ -309,9 +344,22 @@ extern "C" size_t pa_decode_workspace_bytes(const pa_cache_desc_t *cache, int32_
     return p.total;
 }
 
+extern "C" int32_t pa_decode_launch_count(const pa_cache_desc_t *cache, int32_t num_seqs, int32_t num_heads,
+                                          int32_t max_blocks_per_seq, const pa_decode_opts_t *opts) {
+    DecodePlan p;
+    const pa_status_t st = make_plan(cache, num_seqs, num_heads, opts, true, &p);
+    if (st != PA_OK) return (int32_t)st;
+    if (num_seqs == 0) return 0;
+    if (max_blocks_per_seq <= 0 || (int64_t)max_blocks_per_seq * cache->block_size >= ((int64_t)1 << 31))
+        return (int32_t)PA_ERR_INVALID_ARG;
+    const int32_t min_pieces =
+        call_min_pieces(p, opts, num_seqs, cache->block_size, max_blocks_per_seq * cache->block_size);
+    return 2 + (p.shared ? 1 : 0) + (min_pieces > 0 ? 1 : 0);
+}
+
 extern "C" int32_t pa_decode_default_splits(const pa_cache_desc_t *cache, int32_t num_heads,
                                             const pa_decode_opts_t *opts) {
-    pa_decode_opts_t o = opts ? *opts : pa_decode_opts_t{0, PA_KERNEL_AUTO, nullptr, nullptr, nullptr};
+    pa_decode_opts_t o = opts ? *opts : pa_decode_opts_t{0, PA_KERNEL_AUTO, nullptr, nullptr, nullptr, nullptr};
     o.num_splits = 0;
     DecodePlan p;
     const pa_status_t st = make_plan(cache, 1, num_heads, &o, true, &p);
@@ -415,9 +463,20 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         int32_t Nv = num_seqs, Hv = num_heads, Gv = G, mb = max_blocks_per_seq;
         float sl = scale_log2;
         int32_t local_cu = p.local_cu ? 1 : 0;
+        int32_t min_pieces = call_min_pieces(p, opts, num_seqs, cache->block_size, max_len);
         void *args[] = {&tmk, &tmv, &qb, &ob, &block_tables, &mb, &lens_ws, &cu, &Nv, &Hv, &Hk,
-                        &Gv, &NB, &NHv, &sl, &Cv, &ml, &acc, &cnt, &start_seq, &err, &sh, &seq_lens, &local_cu};
+                        &Gv, &NB, &NHv, &sl, &Cv, &ml, &acc, &cnt, &start_seq, &err, &sh, &seq_lens, &local_cu,
+                        &min_pieces};
         if (launch_pdl(fn, grid, block, args, p.smem, s) != cudaSuccess) return PA_ERR_CUDA;
+        if (min_pieces > 0) {
+            // one CTA per SM takes the long (sequence, KV head) merges in turn
+            const int64_t tasks = (int64_t)num_seqs * Hk;
+            const dim3 lgrid((unsigned)std::min<int64_t>(tasks, std::max(num_sms(), 1))), lblock(256);
+            void *largs[] = {&ob, &cu, &Nv, &Hv, &Hk, &Gv, &NHv, &Cv, &ml, &acc, &min_pieces};
+            const void *lfn = cache->head_dim == 128 ? (const void *)long_merge_kernel<128>
+                                                     : (const void *)long_merge_kernel<64>;
+            if (launch_pdl(lfn, lgrid, lblock, largs, 0, s) != cudaSuccess) return PA_ERR_CUDA;
+        }
         if (p.shared) {
             // one warp per (sequence, KV head) bound: members <= N
             const int64_t warps = (int64_t)num_seqs * Hk;

@@ -409,7 +409,7 @@ __device__ __forceinline__ void own_block_cta(
     const int32_t *__restrict__ lens, const int32_t *cu, int32_t N, int32_t H, int32_t G, int32_t NB,
     int32_t NH, float scale_log2, float2 *__restrict__ ml_ws, float *__restrict__ acc_ws,
     unsigned int *__restrict__ counters, const int32_t *__restrict__ start_seq, int32_t Hk, int32_t C,
-    int32_t Cs, const SharedArgs &sh, unsigned int *__restrict__ err) {
+    int32_t Cs, const SharedArgs &sh, unsigned int *__restrict__ err, int32_t min_pieces) {
     using Tile = MmaTile<D, B>;
     constexpr int S = Tile::kStages;
     constexpr int KT = D / 16;  // k-steps of q.k and m-tiles of O^T
@@ -651,11 +651,13 @@ __device__ __forceinline__ void own_block_cta(
                     if (h1 < G) ml_ws[slot * HPG + warp * G + h1] = make_float2(m1, lt1);
                 }
                 // A sequence with a shared prefix is merged by shared_merge_kernel
-                // after this launch; every other one by its last arriver, after
+                // after this launch, one cut into min_pieces or more pieces by
+                // long_merge_kernel, every other one by its last arriver after
                 // its block loop (pending).
-                if (!(kShared && cur.b0 > 0)) {
-                    const PieceRange rg[2] = {own_range(ml_ws, acc_ws, cu, N, cur.seq, cur.g, warp, G, HPG, W, Ce),
-                                              no_range()};
+                const PieceRange rg[2] = {own_range(ml_ws, acc_ws, cu, N, cur.seq, cur.g, warp, G, HPG, W, Ce),
+                                          no_range()};
+                const bool long_seq = min_pieces > 0 && rg[0].c1 - rg[0].c0 + 1 >= min_pieces;
+                if (!(kShared && cur.b0 > 0) && !long_seq) {
                     // The plan kernel zeroes the arrival counters: it has
                     // finished before the first arrival (at once if it has).
                     grid_dependency_wait();
@@ -742,7 +744,7 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
     const int32_t *__restrict__ cu, int32_t N, int32_t H, int32_t Hk, int32_t G, int32_t NB,
     int32_t NH, float scale_log2, int32_t C, float2 *__restrict__ ml_ws, float *__restrict__ acc_ws,
     unsigned int *__restrict__ counters, const int32_t *__restrict__ start_seq, unsigned int *__restrict__ err,
-    const SharedArgs sh, const int32_t *__restrict__ seq_lens, int32_t local_cu) {
+    const SharedArgs sh, const int32_t *__restrict__ seq_lens, int32_t local_cu, int32_t min_pieces) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
 
@@ -764,9 +766,9 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
     } else {
         grid_dependency_wait();  // the plan kernel's cu[] / lens / split (programmatic launch)
     }
-    // With a plan, the merge kernel may become resident as CTAs finish and
-    // work out its piece ranges from the plan while the last ones run.
-    if (kShared) grid_launch_dependents();
+    // With a plan or with long sequences, the merge kernel that follows may
+    // become resident now and wait for this launch there.
+    if (kShared || min_pieces > 0) grid_launch_dependents();
     const int32_t Cs = kShared ? sh.ctl[0] : 0;
     if (kShared && (int32_t)blockIdx.x < Cs)
         shared_prefix_cta<D, B, LAYOUT>(smem, &tmk, &tmv, q, tables, max_blocks, H, G, NB, scale_log2, Hk, Cs, sh,
@@ -774,7 +776,7 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
     else
         own_block_cta<D, B, LAYOUT, kShared>(smem, &tmk, &tmv, q, out, tables, max_blocks, lens_p, cu_p, N, H, G,
                                              NB, NH, scale_log2, ml_ws, acc_ws, counters, start_p, Hk, C, Cs, sh,
-                                             err);
+                                             err, kShared ? 0 : min_pieces);
     // The grid ends after the plan kernel (which also writes the zero output
     // of empty sequences), as a grid that waited at its start does.
     if (local) grid_dependency_wait();

@@ -42,8 +42,10 @@ def oracle_decode(wl, host, r, pairs=None):
                          pairs=pairs, num_threads=oracle.available_threads())
 
 
-def gpu_step(wl, dev, kernel="auto", num_splits=0, decode=True, shared=False):
-    """``shared``: decode with a shared-prefix plan built from the host tables."""
+def gpu_step(wl, dev, kernel="auto", num_splits=0, decode=True, shared=False, host_lens=None):
+    """``shared``: decode with a shared-prefix plan built from the host tables.
+    ``host_lens``: the host-lengths hint of pa_decode, "exact" for the true
+    lengths or any int32 array of num_seqs entries."""
     bm = pa.BlockManager(wl.num_blocks, wl.block_size, wl.free_order)
     slots, pairs = bm.apply_script(wl.script)
     tables, lens = bm.export(list(range(wl.num_seqs)), wl.max_blocks_per_seq)
@@ -59,8 +61,9 @@ def gpu_step(wl, dev, kernel="auto", num_splits=0, decode=True, shared=False):
         plan, g["plan_info"] = pa.shared_prefix_plan(tables, lens, wl.block_size, wl.num_q_heads, wl.num_kv_heads)
         plan = plan.cuda()
     if decode:
+        hint = lens if isinstance(host_lens, str) and host_lens == "exact" else host_lens
         g["out"] = pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale,
-                                kernel=kernel, num_splits=num_splits, shared_plan=plan)
+                                kernel=kernel, num_splits=num_splits, shared_plan=plan, host_seq_lens=hint)
     assert pa.pa_get_device_error(raise_on_error=False) == 0
     g["host_tables"], g["host_slots"], g["host_pairs"] = tables, slots, pairs
     return g

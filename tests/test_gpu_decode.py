@@ -246,3 +246,71 @@ def test_large_scores_underflow_cleanly_through_the_merge(kernel):
     g = gpu_step(wl, dev, kernel=kernel)
     assert torch.isfinite(g["out"].float()).all()
     assert max_abs_err(g["out"], ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
+@pytest.mark.parametrize("hint", ["exact", "zeros", "all-long"])
+def test_long_context_merge_kernel_whatever_the_host_hint(kernel, hint):
+    """With the host copy of the lengths, sequences cut into 8 or more pieces
+    are merged by long_merge_kernel instead of their last-arriving CTA.  The
+    hint only chooses the merge path: exact lengths (the long sequence goes
+    to the second kernel), zeros (no second kernel) and lengths that claim
+    every sequence is as long as the table allows (the second kernel runs
+    and the device still picks only the truly long sequence) all match the
+    oracle.  The CUDA-core kernel ignores the hint."""
+    lens = [131072 + 5, 17, 1, 4096 + 5, 300, 0]
+    wl = inputs.decode_workload("longhint", lens, 64, 8, 128, 16, "bf16", seed=53, pool_factor=1.05)
+    dev, host = host_values(wl, "cuda")
+    r = oracle_step(wl, host)
+    hints = {"exact": "exact", "zeros": np.zeros(len(lens), np.int32),
+             "all-long": np.full(len(lens), wl.max_blocks_per_seq * wl.block_size, np.int32)}
+    g = gpu_step(wl, dev, kernel=kernel, host_lens=hints[hint])
+    pairs = [(0, h) for h in range(0, 64, 5)] + [(1, 0), (2, 63), (3, 31), (4, 7), (5, 0)]
+    ref = oracle_decode(wl, host, r, pairs=pairs[:-1])
+    assert max_abs_err(g["out"], ref, pairs[:-1]) <= TOL["bf16"]
+    assert (g["out"][5] == 0).all()
+    assert torch.isfinite(g["out"].float()).all()
+
+
+def test_long_context_merge_full_size_with_host_lengths():
+    """The long-context workload (every sequence cut into ~10 pieces) in the
+    benchmark's launch configuration, with the host lengths given."""
+    wl = inputs.workload("cfg4")
+    dev, host = host_values(wl, "cuda")
+    r = oracle_step(wl, host)
+    g = gpu_step(wl, dev, host_lens="exact")
+    pairs = sample_pairs(wl, 24)
+    assert max_abs_err(g["out"], oracle_decode(wl, host, r, pairs=pairs), pairs) <= TOL["bf16"]
+
+
+def test_host_hint_leaves_short_sequences_bit_identical():
+    """In a batch where the hint does bring in the second merge kernel, the
+    sequences below the piece threshold are still merged in the attention
+    launch: with and without the hint their outputs are the same bits."""
+    lens = [131072 + 5, 17, 1, 4096 + 5, 300, 0, 2000]
+    wl = inputs.decode_workload("longhint2", lens, 64, 8, 128, 16, "bf16", seed=59, pool_factor=1.05)
+    dev, host = host_values(wl, "cuda")
+    a = gpu_step(wl, {k: v.clone() for k, v in dev.items()})
+    b = gpu_step(wl, {k: v.clone() for k, v in dev.items()}, host_lens="exact")
+    assert torch.equal(a["out"][1:], b["out"][1:])
+    assert (a["out"][0].float() - b["out"][0].float()).abs().max().item() <= TOL["bf16"]
+
+
+def test_launch_count_follows_the_options():
+    """pa_decode_launch_count: plan + attention, plus the long-context merge
+    when the host lengths show a sequence cut into 8+ pieces, plus the
+    shared-prefix merge with a plan."""
+    wl = inputs.workload("cfg4")
+    kc = torch.empty(4, wl.block_size, wl.num_kv_heads, wl.head_dim, dtype=torch.bfloat16, device="cuda")
+    lens = np.asarray(wl.seq_lens, np.int32)
+    args = (kc, wl.num_seqs, wl.num_q_heads, wl.max_blocks_per_seq)
+    assert pa.pa_decode_launch_count(*args) == 2
+    assert pa.pa_decode_launch_count(*args, host_seq_lens=lens) == 3
+    assert pa.pa_decode_launch_count(*args, host_seq_lens=np.zeros_like(lens)) == 2
+    assert pa.pa_decode_launch_count(*args, kernel="simt", host_seq_lens=lens) == 2
+    assert pa.pa_decode_launch_count(*args, shared=True, host_seq_lens=lens) == 3  # shared merge, no long merge
+    w2 = inputs.workload("cfg2")
+    k2 = torch.empty(4, w2.block_size, w2.num_kv_heads, w2.head_dim, dtype=torch.bfloat16, device="cuda")
+    assert pa.pa_decode_launch_count(k2, w2.num_seqs, w2.num_q_heads, w2.max_blocks_per_seq,
+                                     host_seq_lens=np.asarray(w2.seq_lens, np.int32)) == 2
+    assert pa.pa_decode_launch_count(k2, 0, w2.num_q_heads, w2.max_blocks_per_seq) == 0
