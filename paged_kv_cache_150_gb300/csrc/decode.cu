@@ -23,6 +23,10 @@
 //    arrives last merges every piece (the split-K reduce, fused):
 //      out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
 //    Nothing ever waits for another CTA: the merge is done by whoever is last.
+//    With the caller's host copy of the lengths showing a sequence cut into
+//    kLongMergePieces or more pieces (long contexts), such (sequence, KV head)
+//    pairs are merged instead by long_merge_kernel right after the launch,
+//    spread over the GPU; the device decides per sequence from its own cu[].
 //    Without a shared-prefix plan and with N + 1 <= kLocalCuMax, each
 //    tensor-core CTA computes the same cu[] from seq_lens in its own shared
 //    memory and starts on its blocks while the plan kernel still runs; it
