@@ -142,7 +142,9 @@ def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables
         pairs_arr = None
         npairs = 0
     else:
-        pairs_arr = _c(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+        # each (seq, head) once: the C loop writes a pair's row in place, and a
+        # pair listed twice could be computed by two threads at the same time
+        pairs_arr = _c(np.unique(np.asarray(pairs, dtype=np.int32).reshape(-1, 2), axis=0))
         npairs = pairs_arr.shape[0]
     rc = _load().orc_decode(_ptr(out), code, _ptr(q), _ptr(k_cache), _ptr(v_cache), nb, bs, hk, d,
                             _ptr(tables), tables.shape[1], _ptr(lens), n, h, float(scale),

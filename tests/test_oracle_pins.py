@@ -252,6 +252,17 @@ def test_pair_subset_matches_full_run():
     assert np.isnan(part[0, 0]).all()
 
 
+def test_repeated_pairs_give_the_same_values_on_many_threads():
+    """A pair listed several times is computed once: with 8 threads the
+    repeats would otherwise race on the same output row."""
+    q, kc, vc, tables, lens = _rand_case("bf16", 3, [6000, 40, 7], 4, 2, 32, 16, 400, 17)
+    full = _oracle(q, kc, vc, tables, lens, 0.2)
+    pairs = [(0, 1)] * 16 + [(0, 2)] * 16 + [(1, 2), (2, 3)] * 3
+    part = _oracle(q, kc, vc, tables, lens, 0.2, pairs=pairs, num_threads=8)
+    for s, h in set(pairs):
+        np.testing.assert_array_equal(part[s, h], full[s, h])
+
+
 # ----------------------------------------------------------- write and copy
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_cache_write_matches_indexed_assignment(dtype):
