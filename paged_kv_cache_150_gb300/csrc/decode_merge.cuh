@@ -305,20 +305,83 @@ __device__ __forceinline__ void merge_online(T *__restrict__ out_base, const Pie
         merge_online_lph<T, D, kMaxLph, kWideBatch>(out_base, rg, G, lane);
 }
 
+// One (sequence, KV head) merge of long_merge_kernel: thread i owns float4
+// i of the G x D output (threads with i >= G * D / 4 have none) and folds the
+// pieces kBatch at a time with a running maximum, in the same order on every
+// call.
+template <int D>
+__device__ __forceinline__ void long_merge_one(__nv_bfloat16 *__restrict__ out, const PieceRange &p, int32_t H,
+                                               int32_t G, int32_t NH, int32_t seq, int32_t g, int32_t w) {
+    constexpr int kQ = D / 4, kBatch = 8;
+    const int h = (int)threadIdx.x / kQ, q4 = (int)threadIdx.x - h * kQ;
+    if (h >= G) return;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    float M = -INFINITY, Ls = 0.f;
+#pragma unroll 1
+    for (int32_t cb = p.c0; cb <= p.c1; cb += kBatch) {
+        float4 x[kBatch];
+        float2 v[kBatch];
+        float mb = -INFINITY;
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            if (cb + b <= p.c1) {
+                const int64_t idx = (cb + b + p.base) * p.stride + p.col + h;
+                x[b] = __ldcg(reinterpret_cast<const float4 *>(p.acc + idx * D) + q4);
+                v[b] = __ldcg(&p.ml[idx]);
+                mb = fmaxf(mb, v[b].x);
+            }
+        }
+        const float Mn = fmaxf(M, mb);
+        const float sc = M == -INFINITY ? 0.f : ex2_approx(M - Mn);  // every piece has a finite max
+        Ls *= sc;
+        a.x *= sc, a.y *= sc, a.z *= sc, a.w *= sc;
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            if (cb + b <= p.c1) {
+                const float wgt = ex2_approx(v[b].x - Mn);
+                Ls = fmaf(wgt, v[b].y, Ls);
+                a.x = fmaf(wgt, x[b].x, a.x), a.y = fmaf(wgt, x[b].y, a.y);
+                a.z = fmaf(wgt, x[b].z, a.z), a.w = fmaf(wgt, x[b].w, a.w);
+            }
+        }
+        M = Mn;
+    }
+    const float inv = 1.f / Ls;
+    __nv_bfloat16 *o = out + ((int64_t)seq * H + (int64_t)(g * NH + w) * G + h) * D + q4 * 4;
+    const uint32_t lo = pack_bf16x2(a.x * inv, a.y * inv), hi = pack_bf16x2(a.z * inv, a.w * inv);
+    if (((uintptr_t)o & 7u) == 0) {  // out itself is only 4-byte aligned
+        *reinterpret_cast<uint2 *>(o) = make_uint2(lo, hi);
+    } else {
+        reinterpret_cast<uint32_t *>(o)[0] = lo;
+        reinterpret_cast<uint32_t *>(o)[1] = hi;
+    }
+}
+
+// Whether the split cuts (head group g, sequence seq) into min_pieces or more.
+__device__ __forceinline__ bool pair_is_long(const int32_t *cu, int32_t Wg, int64_t W, int32_t Ce, int32_t min_pieces,
+                                             int32_t g, int32_t seq) {
+    const int32_t nb = cu[seq + 1] - cu[seq];
+    if (nb == 0) return false;
+    const int64_t x0 = (int64_t)g * Wg + cu[seq];
+    return split_owner(x0 + nb - 1, W, Ce) - split_owner(x0, W, Ce) + 1 >= min_pieces;
+}
+
 // Merge of the long sequences (after the attention launch, which leaves to
-// this kernel every (sequence, KV head) cut into at least min_pieces pieces).
-// Each CTA takes (sequence, KV head) tasks in turn; a thread owns one float4
-// of the G x D output and folds the pieces kBatch at a time with a running
-// maximum, so the merges of a long context are spread over the GPU instead of
-// falling to the CTAs that finish last.  The same fold order on every call.
-// Whether a task is long is decided from cu[] here exactly as in the
-// attention launch, so both agree whatever the caller's host hint was.
+// this kernel every (sequence, KV head) cut into at least min_pieces pieces;
+// whether a (head group, sequence) pair is long is decided from cu[] here
+// exactly as there, so both agree whatever the caller's host hint was).
+// With few pairs each CTA tests the pair of its own (pair, KV head) tasks.
+// With many, the pairs are tested 256 at a time, one per thread, the long
+// ones of each chunk listed in order in shared memory (every CTA builds the
+// same list), and their merges dealt out over the grid.
 template <int D>
 __global__ void __launch_bounds__(256) long_merge_kernel(
     __nv_bfloat16 *__restrict__ out, const int32_t *__restrict__ cu, int32_t N, int32_t H, int32_t Hk, int32_t G,
     int32_t NH, int32_t C, const float2 *__restrict__ ml_ws, const float *__restrict__ acc_ws, int32_t min_pieces) {
-    constexpr int kQ = D / 4, kBatch = 8, kSmemCu = 4096;
+    constexpr int kSmemCu = 4096, kChunk = 256;
     __shared__ int32_t cu_s[kSmemCu];
+    __shared__ int32_t longs[kChunk];
+    __shared__ int32_t warp_count[kChunk / 32];
     grid_dependency_wait();  // the attention launch's pieces (after the plan kernel's cu[])
     const bool in_smem = N + 1 <= kSmemCu;
     if (in_smem) {
@@ -326,57 +389,39 @@ __global__ void __launch_bounds__(256) long_merge_kernel(
         __syncthreads();
     }
     const int32_t *c = in_smem ? cu_s : cu;
-    const int64_t W = (int64_t)(Hk / NH) * c[N];
+    const int32_t NG = Hk / NH, Wg = c[N];
+    const int64_t W = (int64_t)NG * Wg;
     const int32_t Ce = (int32_t)(W < (int64_t)C ? W : (int64_t)C);
-    const int i = threadIdx.x, h = i / kQ, q4 = i - h * kQ;
-    const bool act = h < G;
-    for (int64_t t = blockIdx.x; t < (int64_t)N * Hk; t += gridDim.x) {
-        const int32_t seq = (int32_t)(t / Hk), kvh = (int32_t)(t - (int64_t)seq * Hk);
-        if (c[seq + 1] == c[seq]) continue;  // empty
-        const int32_t g = kvh / NH;
-        const PieceRange p = own_range(ml_ws, acc_ws, c, N, seq, g, kvh - g * NH, G, NH * G, W, Ce);
-        if (p.c1 - p.c0 + 1 < min_pieces || !act) continue;  // merged in the attention launch
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        float M = -INFINITY, Ls = 0.f;
-#pragma unroll 1
-        for (int32_t cb = p.c0; cb <= p.c1; cb += kBatch) {
-            float4 x[kBatch];
-            float2 v[kBatch];
-            float mb = -INFINITY;
-#pragma unroll
-            for (int b = 0; b < kBatch; ++b) {
-                if (cb + b <= p.c1) {
-                    const int64_t idx = (cb + b + p.base) * p.stride + p.col + h;
-                    x[b] = __ldcg(reinterpret_cast<const float4 *>(p.acc + idx * D) + q4);
-                    v[b] = __ldcg(&p.ml[idx]);
-                    mb = fmaxf(mb, v[b].x);
-                }
+    const int64_t pairs = (int64_t)NG * N;
+    const bool direct = pairs * NH <= 2 * (int64_t)gridDim.x;
+    const int i = threadIdx.x, lane = i & 31, wid = i >> 5;
+    for (int64_t k0 = 0; k0 < pairs; k0 += direct ? pairs : kChunk) {
+        int64_t total = pairs;  // direct: every pair is a candidate, tested by its CTA
+        if (!direct) {
+            const int64_t k = k0 + i;
+            const bool is_long =
+                k < pairs && pair_is_long(c, Wg, W, Ce, min_pieces, (int32_t)(k / N), (int32_t)(k - (k / N) * N));
+            const unsigned int bal = __ballot_sync(0xffffffffu, is_long);
+            if (lane == 0) warp_count[wid] = __popc(bal);
+            __syncthreads();
+            int32_t before = 0, cnt = 0;
+            for (int w = 0; w < kChunk / 32; ++w) {
+                before += w < wid ? warp_count[w] : 0;
+                cnt += warp_count[w];
             }
-            const float Mn = fmaxf(M, mb);
-            const float sc = M == -INFINITY ? 0.f : ex2_approx(M - Mn);  // every piece has a finite max
-            Ls *= sc;
-            a.x *= sc, a.y *= sc, a.z *= sc, a.w *= sc;
-#pragma unroll
-            for (int b = 0; b < kBatch; ++b) {
-                if (cb + b <= p.c1) {
-                    const float wgt = ex2_approx(v[b].x - Mn);
-                    Ls = fmaf(wgt, v[b].y, Ls);
-                    a.x = fmaf(wgt, x[b].x, a.x), a.y = fmaf(wgt, x[b].y, a.y);
-                    a.z = fmaf(wgt, x[b].z, a.z), a.w = fmaf(wgt, x[b].w, a.w);
-                }
-            }
-            M = Mn;
+            if (is_long) longs[before + __popc(bal & ((1u << lane) - 1u))] = (int32_t)(k - k0);
+            __syncthreads();
+            total = cnt;
         }
-        const float inv = 1.f / Ls;
-        const float r[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
-        __nv_bfloat16 *o = out + ((int64_t)seq * H + (int64_t)kvh * G + h) * D + q4 * 4;
-        const uint32_t lo = pack_bf16x2(r[0], r[1]), hi = pack_bf16x2(r[2], r[3]);
-        if (((uintptr_t)o & 7u) == 0) {  // out itself is only 4-byte aligned
-            *reinterpret_cast<uint2 *>(o) = make_uint2(lo, hi);
-        } else {
-            reinterpret_cast<uint32_t *>(o)[0] = lo;
-            reinterpret_cast<uint32_t *>(o)[1] = hi;
+        for (int64_t t = blockIdx.x; t < total * NH; t += gridDim.x) {
+            const int64_t kk = direct ? t / NH : k0 + longs[t / NH];
+            const int32_t g = (int32_t)(kk / N), seq = (int32_t)(kk - (int64_t)g * N), w = (int32_t)(t % NH);
+            if (direct && c[seq + 1] == c[seq]) continue;  // empty
+            const PieceRange p = own_range(ml_ws, acc_ws, c, N, seq, g, w, G, NH * G, W, Ce);
+            if (direct && p.c1 - p.c0 + 1 < min_pieces) continue;  // merged in the attention launch
+            long_merge_one<D>(out, p, H, G, NH, seq, g, w);
         }
+        if (!direct) __syncthreads();  // the list is rebuilt for the next chunk
     }
 }
 

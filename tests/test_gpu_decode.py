@@ -314,3 +314,21 @@ def test_launch_count_follows_the_options():
     assert pa.pa_decode_launch_count(k2, w2.num_seqs, w2.num_q_heads, w2.max_blocks_per_seq,
                                      host_seq_lens=np.asarray(w2.seq_lens, np.int32)) == 2
     assert pa.pa_decode_launch_count(k2, 0, w2.num_q_heads, w2.max_blocks_per_seq) == 0
+
+
+def test_long_merge_among_many_short_sequences():
+    """Two long contexts among 298 short sequences: enough (head group,
+    sequence) pairs that long_merge_kernel lists the long ones 256 pairs at a
+    time before dealing out their merges."""
+    rng = np.random.default_rng(61)
+    lens = rng.integers(1, 500, size=300)
+    lens[17], lens[250] = 65536 + 3, 40000
+    lens[::41] = 0
+    wl = inputs.decode_workload("manylong", lens, 32, 8, 128, 16, "bf16", seed=61, pool_factor=1.1)
+    dev, host = host_values(wl, "cuda")
+    r = oracle_step(wl, host)
+    g = gpu_step(wl, dev, host_lens="exact")
+    pairs = sample_pairs(wl, 200) + [(250, h) for h in range(32)]
+    ref = oracle_decode(wl, host, r, pairs=pairs)
+    assert max_abs_err(g["out"], ref, pairs) <= TOL["bf16"]
+    assert (g["out"][::41] == 0).all()
