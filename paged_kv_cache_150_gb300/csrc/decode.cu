@@ -123,14 +123,16 @@ int32_t long_merge_pieces(const int32_t *host_lens, int32_t N, int32_t B, int32_
     const int64_t Wg = cu[(size_t)N], W = (int64_t)NG * Wg;
     if (W == 0) return 0;
     const int64_t Ce = std::min<int64_t>(C, W);
-    for (int32_t g = 0; g < NG; ++g)
-        for (int32_t i = 0; i < N; ++i) {
-            const int64_t nb = cu[(size_t)i + 1] - cu[(size_t)i];
-            if (nb == 0) continue;
+    for (int32_t i = 0; i < N; ++i) {
+        const int64_t nb = cu[(size_t)i + 1] - cu[(size_t)i];
+        // nb blocks span at most nb * Ce / W + 2 CTAs: most sequences need no exact count
+        if (nb == 0 || nb * Ce < (int64_t)(kLongMergePieces - 2) * W) continue;
+        for (int32_t g = 0; g < NG; ++g) {
             const int64_t x0 = g * Wg + cu[(size_t)i];
             if (split_owner(x0 + nb - 1, W, Ce) - split_owner(x0, W, Ce) + 1 >= kLongMergePieces)
                 return kLongMergePieces;
         }
+    }
     return 0;
 }
 
