@@ -156,3 +156,45 @@ def test_reduce_visits_exactly_the_ctas_holding_a_piece():
             visited = {c for c in range(c0, c1 + 1) if pa.pa_split_range(W, C, c)[0] < pa.pa_split_range(W, C, c)[1]}
             owners = {pa.pa_split_owner(W, C, x) for x in range(int(cu[i]), int(cu[i + 1]))}
             assert visited == owners
+
+
+def test_launch_count_with_host_lengths_follows_the_split(lib):
+    """Host-only (the split count is given, so no occupancy query): with a
+    host copy of the lengths, pa_decode_launch_count is 3 exactly when some
+    (head group, sequence) overlaps 8 or more of the split's CTA ranges
+    (counted here over the ranges pa_split_range returns), else 2; the
+    CUDA-core kernel and a shared-prefix plan never bring in that merge."""
+    d = _desc()
+    rng = np.random.default_rng(5)
+    NH, NG, B, max_blocks = 4, 2, 16, 4096
+    for trial in range(60):
+        N = int(rng.integers(1, 40))
+        C = int(rng.choice([7, 64, 152, 304]))
+        lens = rng.integers(0, 3000, size=N)
+        if trial % 3 == 0:
+            lens[rng.integers(0, N)] = int(rng.integers(10000, max_blocks * B))
+        if trial % 7 == 0:
+            lens[rng.integers(0, N)] = max_blocks * B + 5  # out of range: counts as 0
+        lens = np.ascontiguousarray(lens, np.int32)
+        nb = [0 if (L < 0 or L > max_blocks * B) else -(-int(L) // B) for L in lens]
+        cu = np.concatenate([[0], np.cumsum(nb)]).astype(np.int64)
+        Wg = int(cu[-1])
+        W = NG * Wg
+        expect = 2
+        if W > 0:
+            Ce = min(C, W)
+            ranges = [pa.pa_split_range(W, Ce, c) for c in range(Ce)]
+            for g in range(NG):
+                for i in range(N):
+                    if nb[i] == 0:
+                        continue
+                    a, b = g * Wg + int(cu[i]), g * Wg + int(cu[i + 1])
+                    if sum(1 for lo, hi in ranges if lo < b and a < hi) >= 8:
+                        expect = 3
+        o = _lib.DecodeOpts(C, _lib.PA_KERNEL_MMA, None, None, None, lens.ctypes.data)
+        assert lib.pa_decode_launch_count(ctypes.byref(d), N, 32, max_blocks, ctypes.byref(o)) == expect
+        o_simt = _lib.DecodeOpts(C, _lib.PA_KERNEL_SIMT, None, None, None, lens.ctypes.data)
+        assert lib.pa_decode_launch_count(ctypes.byref(d), N, 32, max_blocks, ctypes.byref(o_simt)) == 2
+        if C >= 2:
+            o_plan = _lib.DecodeOpts(C, _lib.PA_KERNEL_MMA, None, None, ctypes.c_void_p(1), lens.ctypes.data)
+            assert lib.pa_decode_launch_count(ctypes.byref(d), N, 32, max_blocks, ctypes.byref(o_plan)) == 3
