@@ -123,6 +123,18 @@ def _opts(num_splits, kernel, events, shared_plan=None):
     return o
 
 
+def _set_host_lens(o, host_seq_lens, num_seqs):
+    """Put the host-lengths hint into options ``o``; returns the int32 array,
+    which the caller keeps alive until the call returns (or None)."""
+    if host_seq_lens is None:
+        return None
+    host_lens = np.ascontiguousarray(np.asarray(host_seq_lens, dtype=np.int32))
+    if host_lens.shape != (int(num_seqs),):
+        raise ValueError("host_seq_lens must be [num_seqs]")
+    o.host_seq_lens = host_lens.ctypes.data
+    return host_lens
+
+
 def _cache_desc_from_k(k_cache):
     """Descriptor from the K cache alone (its shape fixes the layout)."""
     if k_cache.dim() == 5:
@@ -153,12 +165,7 @@ def pa_decode_launch_count(k_cache, num_seqs, num_heads, max_blocks_per_seq, num
     o = _opts(num_splits, kernel, None)
     if shared:
         o.shared_plan = ctypes.c_void_p(1)  # only tested for NULL here
-    host_lens = None
-    if host_seq_lens is not None:
-        host_lens = np.ascontiguousarray(np.asarray(host_seq_lens, dtype=np.int32))
-        if host_lens.shape != (int(num_seqs),):
-            raise ValueError("host_seq_lens must be [num_seqs]")
-        o.host_seq_lens = host_lens.ctypes.data
+    host_lens = _set_host_lens(o, host_seq_lens, num_seqs)  # noqa: F841 (alive for the call)
     n = _lib.load().pa_decode_launch_count(ctypes.byref(desc), int(num_seqs), int(num_heads),
                                            int(max_blocks_per_seq), ctypes.byref(o))
     if n < 0:
@@ -198,12 +205,7 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None, work
     elif out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("out must match q")
     o = _opts(num_splits, kernel, events, shared_plan)
-    host_lens = None
-    if host_seq_lens is not None:
-        host_lens = np.ascontiguousarray(np.asarray(host_seq_lens, dtype=np.int32))
-        if host_lens.shape != (N,):
-            raise ValueError("host_seq_lens must be [num_seqs]")
-        o.host_seq_lens = host_lens.ctypes.data
+    host_lens = _set_host_lens(o, host_seq_lens, N)  # noqa: F841 (alive for the call)
     lib = _lib.load()
     if workspace is None:  # a caller's workspace is checked by the library (PA_ERR_WORKSPACE)
         need = lib.pa_decode_workspace_bytes(ctypes.byref(desc), N, H, ctypes.byref(o))
@@ -242,14 +244,16 @@ def shared_prefix_plan(block_tables, seq_lens, block_size, num_heads, num_kv_hea
                                     "shared_blocks": info.shared_blocks, "saved_blocks": info.saved_blocks}
 
 
-def pa_decode_no_alloc(q, k_cache, v_cache, block_tables, seq_lens, scale, out, num_splits=0, kernel="auto"):
+def pa_decode_no_alloc(q, k_cache, v_cache, block_tables, seq_lens, scale, out, num_splits=0, kernel="auto",
+                       host_seq_lens=None):
     """pa_decode without a workspace argument, for callers that cannot allocate
     device memory (a pool that took all free memory at startup, a framework
     that owns the allocator, a loop that cannot afford cudaMalloc's implicit
     synchronisation).  Its scratch is a fixed array of
     PA_NO_ALLOC_SCRATCH_BYTES inside the library, shared by every call on a
     device; calls that can overlap on the GPU race on it.  ``out`` is
-    required: this path allocates nothing."""
+    required: this path allocates nothing.  ``host_seq_lens`` as in
+    pa_decode."""
     torch = _torch()
     desc = _cache_desc(k_cache, v_cache)
     N, H, D = q.shape
@@ -260,6 +264,7 @@ def pa_decode_no_alloc(q, k_cache, v_cache, block_tables, seq_lens, scale, out, 
     if out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("out must match q")
     o = _opts(num_splits, kernel, None)
+    host_lens = _set_host_lens(o, host_seq_lens, N)  # noqa: F841 (alive for the call)
     st = _lib.load().pa_decode_no_alloc(
         _dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(desc),
         _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],

@@ -45,3 +45,26 @@ def test_no_alloc_refuses_a_shape_beyond_its_scratch():
     st = _lib.load().pa_decode_no_alloc(p, p, p, p, ctypes.byref(desc), p, 4, p, 8192, 64, 0.088,
                                         ctypes.byref(opts), None)
     assert st == _lib.PA_ERR_WORKSPACE
+
+
+def test_no_alloc_with_the_host_lengths_matches_pa_decode():
+    """The long-context merge path (a host copy of the lengths) through the
+    no-allocation entry point: the same bits as pa_decode with the same
+    hint, and the oracle within tolerance."""
+    import numpy as np
+
+    from _pipeline import max_abs_err, oracle_decode, oracle_step
+
+    lens = [131072 + 5, 17, 1, 4096 + 5, 300, 0]
+    wl = inputs.decode_workload("noalloc-long", lens, 64, 8, 128, 16, "bf16", seed=53, pool_factor=1.05)
+    dev, host = host_values(wl, "cuda")
+    g = gpu_step(wl, dev, host_lens="exact")
+    host_lens = np.asarray(wl.seq_lens, np.int32)
+    out = torch.full_like(g["out"], float("nan"))
+    pa.pa_decode_no_alloc(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale, out,
+                          host_seq_lens=host_lens)
+    assert pa.pa_get_device_error(raise_on_error=False) == 0
+    assert torch.equal(out, g["out"])
+    r = oracle_step(wl, host)
+    pairs = [(0, h) for h in range(0, 64, 9)] + [(3, 5), (4, 60)]
+    assert max_abs_err(out, oracle_decode(wl, host, r, pairs=pairs), pairs) <= TOL["bf16"]
