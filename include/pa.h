@@ -141,7 +141,12 @@ pa_status_t pa_copy_blocks(void *k_cache, void *v_cache, const pa_cache_desc_t *
  *
  * The work is split over a grid of persistent CTAs that share the flattened
  * list of (KV-head group, sequence, block) evenly; a sequence cut between
- * CTAs is merged by a rescaling reduce (running max and sum).
+ * CTAs is merged by a rescaling reduce (running max and sum), done by the CTA
+ * whose piece arrives last or, for sequences cut into many pieces when the
+ * options carry host_seq_lens, by a second kernel spread over the GPU.  The
+ * split depends only on the lengths and the split count, so the same call
+ * gives the same bits every time.  A call launches 2 to 3 kernels
+ * (pa_decode_launch_count), all on `stream`.
  *
  * out           device [num_seqs, H, D] (written).
  * q             device [num_seqs, H, D].
