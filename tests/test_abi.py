@@ -198,3 +198,19 @@ def test_launch_count_with_host_lengths_follows_the_split(lib):
         if C >= 2:
             o_plan = _lib.DecodeOpts(C, _lib.PA_KERNEL_MMA, None, None, ctypes.c_void_p(1), lens.ctypes.data)
             assert lib.pa_decode_launch_count(ctypes.byref(d), N, 32, max_blocks, ctypes.byref(o_plan)) == 3
+
+
+def test_a_run_of_blocks_spans_at_most_its_share_plus_two_ctas():
+    """The host's long-context decision skips the exact count for sequences
+    with nb * Ce < 6 * W: nb consecutive blocks of a W-block list cut into Ce
+    even ranges touch at most nb * Ce / W + 2 of them."""
+    rng = np.random.default_rng(9)
+    for _ in range(3000):
+        W = int(rng.integers(1, 1 << 22))
+        Ce = int(min(rng.integers(1, 5000), W))
+        nb = int(rng.integers(1, W + 1))
+        x0 = int(rng.integers(0, W - nb + 1))
+        pieces = pa.pa_split_owner(W, Ce, x0 + nb - 1) - pa.pa_split_owner(W, Ce, x0) + 1
+        assert pieces <= nb * Ce / W + 2
+        if nb * Ce < 6 * W:
+            assert pieces < 8
