@@ -392,9 +392,23 @@ pa_status_t pa_bm_new_seq_cached(pa_bm_t *bm, const int32_t *token_ids, int32_t 
 /* Slots of positions [first_pos, first_pos + count) of seq (host slots_out). */
 pa_status_t pa_bm_slots(const pa_bm_t *bm, int32_t seq, int32_t first_pos, int32_t count, int32_t *slots_out);
 
-/* Prefix-cache counters: registered blocks, block hits, block lookups. */
+/* Prefix-cache counters: registered blocks (evictable ones included), block
+ * hits, block lookups. */
 pa_status_t pa_bm_cache_stats(const pa_bm_t *bm, int32_t *cached_blocks_out, int64_t *hits_out,
                               int64_t *lookups_out);
+
+/* Retention of prefix-cached blocks (off by default; the eviction of the
+ * hands-on exercise of [PidokuInfra 10] section 10 A).  On: a registered
+ * block whose refcount reaches 0 stays registered as evictable instead of
+ * returning to the free list; a later prompt that hits it revives it; an
+ * allocation takes free blocks first and then evicts the least recently
+ * released evictable blocks, one at a time onto the free stack (the hash
+ * entry is dropped).  Evictable blocks count as free in pa_bm_stats.  Off:
+ * evictable blocks become free, oldest first.  Never fails for a valid bm. */
+pa_status_t pa_bm_set_prefix_retention(pa_bm_t *bm, int32_t on);
+
+/* Number of evictable (retained, refcount 0) blocks. */
+pa_status_t pa_bm_evictable(const pa_bm_t *bm, int32_t *count_out);
 
 /* Export tables for a decode batch: tables_out [n, max_blocks] (host) padded
  * with -1, lens_out [n]; PA_ERR_INVALID_ARG if a table is longer than

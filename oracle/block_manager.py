@@ -35,7 +35,15 @@ Readings where the pages are silent or differ:
     0.  A hit also compares the stored token ids.
   * Only full blocks of a prompt are registered, when the sequence is
     created, so a cached block is never written (no copy-on-write for it).
-    A block leaves the map when its refcount reaches 0.
+    By default a block leaves the map when its refcount reaches 0.
+  * Eviction ([PidokuInfra 10] section 10 A names it beside the prefix hash
+    table, without rules), when retention is switched on: a registered block
+    whose refcount reaches 0 stays registered as evictable, in order of
+    release; a prompt that hits it takes it back; an allocation uses the free
+    stack and, when that is short, moves the least recently released
+    evictable blocks onto it one at a time (dropping their hash entries)
+    before taking the top n.  Evictable blocks count as free.  Switching
+    retention off frees the evictable blocks, oldest first.
   * The free order is a parameter (the stack's bottom first).  The default is
     the Go constructor's: ids pushed from num_blocks-1 down to 0.
   * A failed append (no free block for a new block or for a copy) changes no
@@ -89,17 +97,35 @@ class OracleBlockManager:
         self.block_key = {}   # block -> (hash, token ids) while registered
         self.hits = 0
         self.lookups = 0
+        self.retain = False
+        self.evictable = []   # registered blocks at refcount 0, oldest release first
+
+    def _unregister(self, b):
+        del self.cached[self.block_key.pop(b)[0]]
+
+    def set_retention(self, on):
+        if not on:
+            for b in self.evictable:
+                self._unregister(b)
+                self.free.append(b)
+            self.evictable = []
+        self.retain = bool(on)
 
     # ---- block-level calls (PidokuInfra section 4) ----
     def blocks_needed(self, tokens):
         return (tokens + self.block_size - 1) // self.block_size
 
     def allocate(self, n):
-        """Top n free ids in slice order, refcount 1; None (no change) when short."""
-        if len(self.free) < n:
+        """Top n free ids in slice order, refcount 1; None (no change) when short.
+        With too few free ids, evictable blocks are evicted onto the stack first."""
+        if len(self.free) + len(self.evictable) < n:
             return None
         if n == 0:
             return []
+        while len(self.free) < n:
+            b = self.evictable.pop(0)
+            self._unregister(b)
+            self.free.append(b)
         blocks = self.free[len(self.free) - n:]
         del self.free[len(self.free) - n:]
         for b in blocks:
@@ -111,9 +137,12 @@ class OracleBlockManager:
             self.ref[b] -= 1
             if self.ref[b] == 0:
                 del self.ref[b]
-                self.free.append(b)
-                if b in self.block_key:
-                    del self.cached[self.block_key.pop(b)[0]]
+                if self.retain and b in self.block_key:
+                    self.evictable.append(b)
+                else:
+                    self.free.append(b)
+                    if b in self.block_key:
+                        self._unregister(b)
 
     def fork_blocks(self, blocks):
         for b in blocks:
@@ -148,13 +177,17 @@ class OracleBlockManager:
             if b is None or self.block_key[b][1] != tuple(tokens[j * B:(j + 1) * B]):
                 break
             reused.append(b)
-        fresh = self.allocate(self.blocks_needed(len(tokens)) - len(reused))
-        if fresh is None:
+        need = self.blocks_needed(len(tokens)) - len(reused)
+        revived = [b for b in reused if b in self.evictable]
+        if len(self.free) + len(self.evictable) - len(revived) < need:
             return None
+        for b in revived:
+            self.evictable.remove(b)
+        for b in reused:
+            self.ref[b] = self.ref.get(b, 0) + 1
+        fresh = self.allocate(need)
         self.lookups += lookups
         self.hits += len(reused)
-        for b in reused:
-            self.ref[b] += 1
         table = reused + fresh
         for j in range(len(reused), n_full):
             b = table[j]
@@ -212,13 +245,14 @@ class OracleBlockManager:
     def stats(self):
         """(free, used, shared) block counts."""
         shared = sum(1 for r in self.ref.values() if r > 1)
-        return len(self.free), self.num_blocks - len(self.free), shared
+        free = len(self.free) + len(self.evictable)
+        return free, self.num_blocks - free, shared
 
 
 def run_script(num_blocks, block_size, free_order, script, manager=None):
     """Run a workload's block-manager script: ("new", tokens), ("new_cached",
-    token_ids), ("fork", parent), ("free", seq), ("append", seq, count), on a
-    fresh manager or on ``manager``.  Sequences are numbered in creation order.
+    token_ids), ("fork", parent), ("free", seq), ("append", seq, count),
+    ("retain", on), on a fresh manager or on ``manager``.  Sequences are numbered in creation order.
 
     Returns a dict with the manager, the final ``tables`` (list per sequence),
     ``lens``, the ``slots`` of every appended token in script order, the
@@ -246,6 +280,8 @@ def run_script(num_blocks, block_size, free_order, script, manager=None):
             m.fork(op[1])
         elif op[0] == "free":
             m.free_seq(op[1])
+        elif op[0] == "retain":
+            m.set_retention(op[1])
         elif op[0] == "append":
             for _ in range(op[2]):
                 got = m.append_token(op[1])

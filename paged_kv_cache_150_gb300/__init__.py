@@ -347,6 +347,18 @@ class BlockManager:
         self._call("pa_bm_slots", int(seq), int(first_pos), int(count), _i32p(out))
         return out[:int(count)]
 
+    def set_prefix_retention(self, on=True):
+        """Keep prefix-cached blocks registered when their refcount reaches 0
+        (evictable, least recently released evicted first) instead of freeing
+        them; off turns the evictable blocks into free ones."""
+        self._call("pa_bm_set_prefix_retention", 1 if on else 0)
+
+    def evictable(self):
+        """Number of retained blocks at refcount 0."""
+        n = ctypes.c_int32()
+        self._call("pa_bm_evictable", ctypes.byref(n))
+        return n.value
+
     def cache_stats(self):
         """(registered blocks, block hits, block lookups) of the prefix cache."""
         n, h, l = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int64()
@@ -412,9 +424,10 @@ class BlockManager:
         return tables[:n], lens[:n]
 
     def apply_script(self, script):
-        """Run a workload script ("new", tokens) / ("fork", parent) /
-        ("append", seq, count).  Returns (slots int32 [T], pairs int32 [P, 2]),
-        slots in script order and pairs in the order they were made."""
+        """Run a workload script ("new", tokens) / ("new_cached", token_ids) /
+        ("fork", parent) / ("free", seq) / ("append", seq, count) /
+        ("retain", on).  Returns (slots int32 [T], pairs int32 [P, 2]), slots
+        in script order and pairs in the order they were made."""
         slots, pairs = [], []
         for op in script:
             if op[0] == "new":
@@ -431,6 +444,8 @@ class BlockManager:
                 self.fork(op[1])
             elif op[0] == "free":
                 self.free_seq(op[1])
+            elif op[0] == "retain":
+                self.set_prefix_retention(op[1])
             elif op[0] == "append":
                 s, pair = self.append_tokens(op[1], op[2])
                 slots.append(s)

@@ -104,6 +104,8 @@ SIGNATURES = {
     "pa_bm_new_seq_cached": (_I32, [_P, _PI32, _I32, _PI32, _PI32]),
     "pa_bm_slots": (_I32, [_P, _I32, _I32, _I32, _PI32]),
     "pa_bm_cache_stats": (_I32, [_P, _PI32, _PI64, _PI64]),
+    "pa_bm_set_prefix_retention": (_I32, [_P, _I32]),
+    "pa_bm_evictable": (_I32, [_P, _PI32]),
     "pa_sim_run": (_I32, [ctypes.POINTER(SimConfig), _PI32, _PI32, _PI32, _I32, ctypes.POINTER(SimResult)]),
 }
 

@@ -14,9 +14,14 @@
 // under a chained hash (64-bit FNV-1a over the parent block's hash, 8 bytes
 // little-endian, then the block's token ids, 4 bytes little-endian each; the
 // parent of block 0 is 0), and a new prompt reuses the blocks of its longest
-// registered prefix (refcount + 1).  A hit also compares the token ids.  A
-// block leaves the map when its refcount reaches 0.
+// registered prefix (refcount + 1).  A hit also compares the token ids.  By
+// default a block leaves the map when its refcount reaches 0.  With retention
+// (the eviction of the pages' hands-on exercise, "10 PagedAttention" section
+// 10 A) it stays registered as evictable, in order of release: a later hit
+// revives it, and allocation takes free blocks first, then evicts the least
+// recently released.
 #include <cstdint>
+#include <list>
 #include <new>
 #include <unordered_map>
 #include <vector>
@@ -40,12 +45,41 @@ struct pa_bm {
     std::vector<char> registered;
     std::vector<int32_t> block_tokens;              // B token ids per registered block
     int64_t hits = 0, lookups = 0;
+    // retention: registered blocks at refcount 0, least recently released first
+    bool retain = false;
+    std::list<int32_t> lru;
+    std::vector<std::list<int32_t>::iterator> lru_it;
+    std::vector<char> in_lru;
 
+    void unregister(int32_t b) {
+        cached.erase(block_hash[b]);
+        registered[b] = 0;
+    }
     void release(int32_t b) {  // refcount reached 0
+        const bool reg = !registered.empty() && registered[b];
+        if (retain && reg) {
+            lru_it[b] = lru.insert(lru.end(), b);
+            in_lru[b] = 1;
+            return;
+        }
         free.push_back(b);
-        if (!registered.empty() && registered[b]) {
-            cached.erase(block_hash[b]);
-            registered[b] = 0;
+        if (reg) unregister(b);
+    }
+    void revive(int32_t b) {  // a hit on an evictable block
+        lru.erase(lru_it[b]);
+        in_lru[b] = 0;
+    }
+    // Blocks an allocation may use: free ones and evictable ones.
+    int64_t available() const { return (int64_t)free.size() + (int64_t)lru.size(); }
+    // Evict the least recently released blocks onto the free stack until it
+    // holds n (the caller has checked available() >= n).
+    void reserve(size_t n) {
+        while (free.size() < n && !lru.empty()) {
+            const int32_t b = lru.front();
+            lru.pop_front();
+            in_lru[b] = 0;
+            unregister(b);
+            free.push_back(b);
         }
     }
 
@@ -58,8 +92,9 @@ struct pa_bm {
     const Seq *get(int32_t s) const {
         return (s >= 0 && s < (int32_t)seqs.size() && seqs[s].live) ? &seqs[s] : nullptr;
     }
-    // Top n ids in stack order; the caller has checked free.size() >= n.
+    // Top n ids in stack order; the caller has checked available() >= n.
     void take(int32_t n, std::vector<int32_t> &out) {
+        reserve((size_t)n);
         const size_t first = free.size() - (size_t)n;
         for (size_t i = first; i < free.size(); ++i) {
             out.push_back(free[i]);
@@ -68,6 +103,7 @@ struct pa_bm {
         free.resize(first);
     }
     int32_t pop_one() {
+        reserve(1);
         const int32_t b = free.back();
         free.pop_back();
         ref[b] = 1;
@@ -109,7 +145,7 @@ extern "C" void pa_bm_destroy(pa_bm_t *bm) { delete bm; }
 extern "C" pa_status_t pa_bm_new_seq(pa_bm_t *bm, int32_t num_tokens, int32_t *seq_out) {
     if (!bm || num_tokens < 0 || !seq_out) return PA_ERR_INVALID_ARG;
     const int32_t n = bm->blocks_needed(num_tokens);
-    if ((int64_t)n > (int64_t)bm->free.size()) return PA_ERR_NO_BLOCKS;
+    if ((int64_t)n > bm->available()) return PA_ERR_NO_BLOCKS;
     pa_bm::Seq s;
     s.live = true;
     s.len = num_tokens;
@@ -163,7 +199,7 @@ extern "C" pa_status_t pa_bm_append_tokens(pa_bm_t *bm, int32_t seq, int32_t cou
     const bool cow = (pos0 % B != 0) && bm->ref[s->table[pos0 / B]] > 1;
     const int64_t grow = (int64_t)bm->blocks_needed((int64_t)pos0 + count) - (int64_t)s->table.size();
     if (cow && !cow_pairs_out) return PA_ERR_INVALID_ARG;
-    if ((int64_t)cow + grow > (int64_t)bm->free.size()) return PA_ERR_NO_BLOCKS;
+    if ((int64_t)cow + grow > bm->available()) return PA_ERR_NO_BLOCKS;
     if (cow) {
         const int32_t old = s->table[pos0 / B];
         const int32_t fresh = bm->pop_one();
@@ -235,8 +271,8 @@ extern "C" pa_status_t pa_bm_stats(const pa_bm_t *bm, int32_t *free_out, int32_t
     if (!bm) return PA_ERR_INVALID_ARG;
     int32_t shared = 0;
     for (int32_t r : bm->ref) shared += r > 1;
-    if (free_out) *free_out = (int32_t)bm->free.size();
-    if (used_out) *used_out = bm->num_blocks - (int32_t)bm->free.size();
+    if (free_out) *free_out = (int32_t)bm->available();  // evictable blocks count as free
+    if (used_out) *used_out = bm->num_blocks - (int32_t)bm->available();
     if (shared_out) *shared_out = shared;
     return PA_OK;
 }
@@ -308,8 +344,13 @@ extern "C" pa_status_t pa_bm_new_seq_cached(pa_bm_t *bm, const int32_t *token_id
     }
     const int32_t reused = (int32_t)table.size();
     const int32_t need = bm->blocks_needed(num_tokens) - reused;
-    if ((int64_t)need > (int64_t)bm->free.size()) return PA_ERR_NO_BLOCKS;
-    for (int32_t b : table) bm->ref[b] += 1;
+    int64_t revived = 0;  // hits on evictable blocks leave the evictable pool
+    for (int32_t b : table) revived += bm->ref[b] == 0 ? 1 : 0;
+    if ((int64_t)need > bm->available() - revived) return PA_ERR_NO_BLOCKS;
+    for (int32_t b : table) {
+        if (bm->ref[b] == 0) bm->revive(b);
+        bm->ref[b] += 1;
+    }
     bm->take(need, table);
     for (int32_t j = reused; j < n_full; ++j) {
         const int32_t b = table[j];
@@ -336,6 +377,31 @@ extern "C" pa_status_t pa_bm_slots(const pa_bm_t *bm, int32_t seq, int32_t first
     const pa_bm::Seq *s = bm->get(seq);
     if (!s || (int64_t)first_pos + count > s->len) return PA_ERR_INVALID_ARG;
     for (int32_t i = 0; i < count; ++i) slots_out[i] = bm->slot(*s, first_pos + i);
+    return PA_OK;
+}
+
+extern "C" pa_status_t pa_bm_set_prefix_retention(pa_bm_t *bm, int32_t on) {
+    if (!bm) return PA_ERR_INVALID_ARG;
+    if (on && bm->in_lru.empty()) {
+        bm->in_lru.assign((size_t)bm->num_blocks, 0);
+        bm->lru_it.resize((size_t)bm->num_blocks);
+    }
+    if (!on) {  // the evictable blocks become plain free blocks, oldest first
+        while (!bm->lru.empty()) {
+            const int32_t b = bm->lru.front();
+            bm->lru.pop_front();
+            bm->in_lru[b] = 0;
+            bm->unregister(b);
+            bm->free.push_back(b);
+        }
+    }
+    bm->retain = on != 0;
+    return PA_OK;
+}
+
+extern "C" pa_status_t pa_bm_evictable(const pa_bm_t *bm, int32_t *count_out) {
+    if (!bm || !count_out) return PA_ERR_INVALID_ARG;
+    *count_out = (int32_t)bm->lru.size();
     return PA_OK;
 }
 

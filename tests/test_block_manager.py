@@ -182,3 +182,66 @@ def test_beam_search_manager_matches_oracle(small):
         oracle.run_script(0, wl.block_size, None, st["select"], manager=m)
         bm.apply_script(st["select"])
         assert bm.stats() == m.stats()
+
+
+def test_prefix_retention_matches_oracle_under_pool_pressure():
+    """Retention on, a pool small enough that allocations evict: the C++
+    manager and the oracle model agree on every hit, table, free count,
+    cache counter and evictable count, through frees, appends, failed
+    allocations (no state change) and switching retention off."""
+    rng = np.random.default_rng(11)
+    order = rng.permutation(16).astype(np.int32)
+    bm = pa.BlockManager(16, 8, order)
+    m = oracle.OracleBlockManager(16, 8, order)
+    bm.set_prefix_retention(True)
+    m.set_retention(True)
+    prompts = [rng.integers(0, 30, size=int(rng.integers(16, 70))).tolist() for _ in range(5)]
+    live = []
+    failures = most_evictable = evicted = 0
+    for step in range(150):
+        if step == 120:  # retention off: evictable blocks become free, oldest first
+            bm.set_prefix_retention(False)
+            m.set_retention(False)
+        p = prompts[int(rng.integers(0, len(prompts)))]
+        toks = p[:int(rng.integers(len(p) // 2, len(p) + 1))] + rng.integers(0, 30, size=int(rng.integers(0, 6))).tolist()
+        registered = len(m.cached)
+        want = m.new_sequence_cached(toks)
+        if want is None:
+            failures += 1
+            with pytest.raises(pa.PagedAttentionError):
+                bm.new_seq_cached(toks)
+        else:
+            got = bm.new_seq_cached(toks)
+            assert got == want
+            live.append(got[0])
+            assert bm.block_table(got[0]) == m.tables[want[0]]
+            # registered blocks only go away by eviction while retention is on
+            evicted += step < 120 and len(m.cached) < registered
+        if live and rng.random() < 0.5:  # some growth of a live sequence
+            s = live[int(rng.integers(0, len(live)))]
+            if m.append_token(s) is not None:
+                bm.append_tokens(s, 1)
+        while len(live) > 4 or (live and rng.random() < 0.3):
+            victim = live.pop(int(rng.integers(0, len(live))))
+            bm.free_seq(victim)
+            m.free_seq(victim)
+        assert bm.stats() == m.stats()
+        assert bm.cache_stats() == (len(m.cached), m.hits, m.lookups)
+        assert bm.evictable() == len(m.evictable)
+        most_evictable = max(most_evictable, len(m.evictable))
+    assert failures > 0 and m.hits > 0 and most_evictable > 0 and evicted > 0
+
+
+def test_retained_prompt_is_hit_again_after_its_sequence_is_freed():
+    bm = pa.BlockManager(16, 4)
+    bm.set_prefix_retention(True)
+    toks = list(range(11))  # two full blocks and a partial one
+    s, cached = bm.new_seq_cached(toks)
+    assert cached == 0
+    bm.free_seq(s)
+    assert bm.evictable() == 2 and bm.stats()[0] == 16  # evictable blocks count as free
+    s2, cached2 = bm.new_seq_cached(toks)
+    assert cached2 == 8 and bm.evictable() == 0
+    bm.free_seq(s2)
+    bm.set_prefix_retention(False)
+    assert bm.evictable() == 0 and bm.cache_stats()[0] == 0

@@ -258,3 +258,42 @@ def test_beam_search_keeps_copy_on_write_invariants(small):
         assert all(ref == 1 for ref in r["written_refcounts"])
         oracle.run_script(0, B, None, st["select"], manager=m)
         _check_invariants(m)
+
+
+def test_retention_evicts_the_least_recently_released_block_first():
+    """Retained blocks leave in the order they were released.  Prompts A and
+    B each fill one block and are freed, A first; a request for three blocks
+    then takes the two free ones and evicts A's block, so B's prompt still
+    hits while A's prompt has left the map.  A request that neither free nor
+    evictable blocks can cover fails and changes nothing."""
+    m = oracle.OracleBlockManager(4, 2, free_order=[3, 2, 1, 0])  # block 0 is taken first
+    m.set_retention(True)
+    a, _ = m.new_sequence_cached([1, 2])
+    b, _ = m.new_sequence_cached([3, 4])
+    block_a, block_b = m.tables[a][0], m.tables[b][0]
+    m.free_seq(a)
+    m.free_seq(b)
+    assert m.evictable == [block_a, block_b] and m.stats()[0] == 4
+    c = m.new_sequence(5)  # three blocks: the two free ones and block_a
+    assert c is not None and block_a in m.tables[c] and m.evictable == [block_b]
+    assert list(m.cached.values()) == [block_b]  # A's prompt left the map
+    _, hit = m.new_sequence_cached([3, 4])
+    assert hit == 2 and m.evictable == [] and m.ref[block_b] == 1
+    state = (list(m.free), dict(m.ref), dict(m.cached), m.hits, m.lookups)
+    assert m.new_sequence_cached([1, 2, 9, 9]) is None  # two blocks wanted, none left
+    assert (list(m.free), dict(m.ref), dict(m.cached), m.hits, m.lookups) == state
+
+
+def test_retention_off_returns_retained_blocks_oldest_first():
+    """Switching retention off unregisters every retained block and pushes
+    them onto the free stack in release order, so the newest release is the
+    next block handed out."""
+    m = oracle.OracleBlockManager(3, 2, free_order=[2, 1, 0])
+    m.set_retention(True)
+    seqs = [m.new_sequence_cached([k, k])[0] for k in (1, 2, 3)]
+    released = [m.tables[s][0] for s in seqs]
+    for s in seqs:
+        m.free_seq(s)
+    m.set_retention(False)
+    assert m.free == released and m.cached == {} and m.evictable == []
+    assert m.allocate(1) == [released[-1]]
