@@ -48,8 +48,7 @@ struct pa_bm {
     // retention: registered blocks at refcount 0, least recently released first
     bool retain = false;
     std::list<int32_t> lru;
-    std::vector<std::list<int32_t>::iterator> lru_it;
-    std::vector<char> in_lru;
+    std::vector<std::list<int32_t>::iterator> lru_it;  // sized once retention is first switched on
 
     void unregister(int32_t b) {
         cached.erase(block_hash[b]);
@@ -59,28 +58,25 @@ struct pa_bm {
         const bool reg = !registered.empty() && registered[b];
         if (retain && reg) {
             lru_it[b] = lru.insert(lru.end(), b);
-            in_lru[b] = 1;
             return;
         }
         free.push_back(b);
         if (reg) unregister(b);
     }
-    void revive(int32_t b) {  // a hit on an evictable block
-        lru.erase(lru_it[b]);
-        in_lru[b] = 0;
+    void revive(int32_t b) { lru.erase(lru_it[b]); }  // a hit on an evictable block
+    // The least recently released evictable block goes back on the free stack.
+    void evict_oldest() {
+        const int32_t b = lru.front();
+        lru.pop_front();
+        unregister(b);
+        free.push_back(b);
     }
     // Blocks an allocation may use: free ones and evictable ones.
     int64_t available() const { return (int64_t)free.size() + (int64_t)lru.size(); }
     // Evict the least recently released blocks onto the free stack until it
     // holds n (the caller has checked available() >= n).
     void reserve(size_t n) {
-        while (free.size() < n && !lru.empty()) {
-            const int32_t b = lru.front();
-            lru.pop_front();
-            in_lru[b] = 0;
-            unregister(b);
-            free.push_back(b);
-        }
+        while (free.size() < n && !lru.empty()) evict_oldest();
     }
 
     int32_t blocks_needed(int64_t tokens) const {
@@ -382,19 +378,9 @@ extern "C" pa_status_t pa_bm_slots(const pa_bm_t *bm, int32_t seq, int32_t first
 
 extern "C" pa_status_t pa_bm_set_prefix_retention(pa_bm_t *bm, int32_t on) {
     if (!bm) return PA_ERR_INVALID_ARG;
-    if (on && bm->in_lru.empty()) {
-        bm->in_lru.assign((size_t)bm->num_blocks, 0);
-        bm->lru_it.resize((size_t)bm->num_blocks);
-    }
-    if (!on) {  // the evictable blocks become plain free blocks, oldest first
-        while (!bm->lru.empty()) {
-            const int32_t b = bm->lru.front();
-            bm->lru.pop_front();
-            bm->in_lru[b] = 0;
-            bm->unregister(b);
-            bm->free.push_back(b);
-        }
-    }
+    if (on && bm->lru_it.empty()) bm->lru_it.resize((size_t)bm->num_blocks);
+    if (!on)  // the evictable blocks become plain free blocks, oldest first
+        while (!bm->lru.empty()) bm->evict_oldest();
     bm->retain = on != 0;
     return PA_OK;
 }
