@@ -39,7 +39,9 @@ Readings where the pages are silent or differ:
   * Eviction ([PidokuInfra 10] section 10 A names it beside the prefix hash
     table, without rules), when retention is switched on: a registered block
     whose refcount reaches 0 stays registered as evictable, in order of
-    release; a prompt that hits it takes it back; an allocation uses the free
+    release, the blocks one call frees from the last to the first (matching
+    stops at a prompt's first miss, so a prompt should lose its tail before
+    its head); a prompt that hits it takes it back; an allocation uses the free
     stack and, when that is short, moves the least recently released
     evictable blocks onto it one at a time (dropping their hash entries)
     before taking the top n.  Evictable blocks count as free.  Switching
@@ -133,16 +135,18 @@ class OracleBlockManager:
         return list(blocks)
 
     def free_blocks(self, blocks):
+        retained = []
         for b in blocks:
             self.ref[b] -= 1
             if self.ref[b] == 0:
                 del self.ref[b]
                 if self.retain and b in self.block_key:
-                    self.evictable.append(b)
+                    retained.append(b)
                 else:
                     self.free.append(b)
                     if b in self.block_key:
                         self._unregister(b)
+        self.evictable.extend(reversed(retained))
 
     def fork_blocks(self, blocks):
         for b in blocks:

@@ -17,9 +17,10 @@
 // registered prefix (refcount + 1).  A hit also compares the token ids.  By
 // default a block leaves the map when its refcount reaches 0.  With retention
 // (the eviction of the pages' hands-on exercise, "10 PagedAttention" section
-// 10 A) it stays registered as evictable, in order of release: a later hit
-// revives it, and allocation takes free blocks first, then evicts the least
-// recently released.
+// 10 A) it stays registered as evictable, in order of release (a freed
+// sequence's blocks from its last to its first): a later hit revives it, and
+// allocation takes free blocks first, then evicts the least recently
+// released.
 #include <cstdint>
 #include <list>
 #include <new>
@@ -49,20 +50,18 @@ struct pa_bm {
     bool retain = false;
     std::list<int32_t> lru;
     std::vector<std::list<int32_t>::iterator> lru_it;  // sized once retention is first switched on
+    std::vector<int32_t> scratch;
 
     void unregister(int32_t b) {
         cached.erase(block_hash[b]);
         registered[b] = 0;
     }
-    void release(int32_t b) {  // refcount reached 0
-        const bool reg = !registered.empty() && registered[b];
-        if (retain && reg) {
-            lru_it[b] = lru.insert(lru.end(), b);
-            return;
-        }
+    bool is_registered(int32_t b) const { return !registered.empty() && registered[b]; }
+    void release(int32_t b) {  // refcount reached 0, not retained
         free.push_back(b);
-        if (reg) unregister(b);
+        if (is_registered(b)) unregister(b);
     }
+    void make_evictable(int32_t b) { lru_it[b] = lru.insert(lru.end(), b); }
     void revive(int32_t b) { lru.erase(lru_it[b]); }  // a hit on an evictable block
     // The least recently released evictable block goes back on the free stack.
     void evict_oldest() {
@@ -170,9 +169,19 @@ extern "C" pa_status_t pa_bm_free_seq(pa_bm_t *bm, int32_t seq) {
     if (!bm) return PA_ERR_INVALID_ARG;
     pa_bm::Seq *s = bm->get(seq);
     if (!s) return PA_ERR_INVALID_ARG;
+    // Retained blocks enter the eviction order from the sequence's last block
+    // to its first: prefix matching stops at a prompt's first miss, so a
+    // prompt should lose its tail before its head.
+    std::vector<int32_t> &kept = bm->scratch;
+    kept.clear();
     for (int32_t b : s->table) {
-        if (--bm->ref[b] == 0) bm->release(b);
+        if (--bm->ref[b] != 0) continue;
+        if (bm->retain && bm->is_registered(b))
+            kept.push_back(b);
+        else
+            bm->release(b);
     }
+    for (size_t i = kept.size(); i-- > 0;) bm->make_evictable(kept[i]);
     s->table.clear();
     s->table.shrink_to_fit();
     s->live = false;

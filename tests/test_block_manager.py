@@ -245,3 +245,16 @@ def test_retained_prompt_is_hit_again_after_its_sequence_is_freed():
     bm.free_seq(s2)
     bm.set_prefix_retention(False)
     assert bm.evictable() == 0 and bm.cache_stats()[0] == 0
+
+
+def test_a_freed_prompt_loses_its_tail_before_its_head():
+    bm = pa.BlockManager(4, 2)
+    bm.set_prefix_retention(True)
+    toks = [1, 2, 3, 4, 5, 6]
+    s, _ = bm.new_seq_cached(toks)
+    bm.free_seq(s)
+    other = bm.new_seq(4)  # two blocks: the free one and the prompt's evicted last block
+    assert bm.evictable() == 2
+    bm.free_seq(other)
+    _, cached = bm.new_seq_cached(toks)
+    assert cached == 4 and bm.evictable() == 0

@@ -297,3 +297,21 @@ def test_retention_off_returns_retained_blocks_oldest_first():
     m.set_retention(False)
     assert m.free == released and m.cached == {} and m.evictable == []
     assert m.allocate(1) == [released[-1]]
+
+
+def test_a_freed_prompt_loses_its_tail_before_its_head():
+    """Matching stops at a prompt's first miss, so evicting a prompt's first
+    block would strand the rest.  A freed three-block prompt gives up its
+    last block to the first eviction, and the same prompt still hits its
+    first two blocks afterwards."""
+    m = oracle.OracleBlockManager(4, 2)
+    m.set_retention(True)
+    s, _ = m.new_sequence_cached([1, 2, 3, 4, 5, 6])
+    table = list(m.tables[s])
+    m.free_seq(s)
+    assert m.evictable == table[::-1]
+    got = m.allocate(2)  # the one free block and the evicted tail
+    assert table[2] in got and m.evictable == table[1::-1]
+    m.free_blocks(got)
+    _, hit = m.new_sequence_cached([1, 2, 3, 4, 5, 6])
+    assert hit == 4
