@@ -173,6 +173,7 @@ def sampling_workload(name: str, num_prompts: int, prompt_len: int, samples: int
 
 NEW_CACHED = "new_cached"  # ("new_cached", token_ids): a prompt that may reuse cached prefix blocks
 FREE = "free"              # ("free", seq): release a sequence's blocks
+RETAIN = "retain"          # ("retain", on): keep freed prompt blocks registered until evicted
 
 
 @dataclass
@@ -295,6 +296,93 @@ def prefix_workload(name: str, num_prompts: int, requests_per_prompt: int, syste
                     extra={"system_len": system_len, "num_prompts": num_prompts,
                            "requests_per_prompt": requests_per_prompt})
 
+
+
+def retention_workload(name: str, num_prompts: int, requests_per_prompt: int, system_blocks: int,
+                       spare_blocks: int, evict_blocks: int, num_q_heads: int, num_kv_heads: int,
+                       head_dim: int, block_size: int, dtype: str, seed: int) -> Workload:
+    """Two waves of requests over a pool with prefix retention switched on
+    (the eviction of the hands-on exercise, "10 PagedAttention" section 10 A).
+
+    Wave 1 switches retention on, requests each of num_prompts system prompts
+    (system_blocks whole blocks of random token ids) requests_per_prompt times,
+    each followed by its own suffix of U[1, B-1] tokens (so every request ends
+    in a partly filled block of its own), and frees every request: the system
+    prompts' blocks stay registered, the first prompt's released first.
+
+    Wave 2 requests every prompt but the first once (prefix hits), then a
+    fresh prompt of whole blocks, as many as the free stack then holds plus
+    evict_blocks, so it evicts that many of the first prompt's blocks; the
+    fresh request is freed again, the first prompt is requested (it hits the
+    blocks it kept) and every live request appends one decode token.
+
+    ``script`` is wave 1 followed by wave 2.  Its K/V rows must be written in
+    three phases, ``extra["phases"]`` (ops, rows) each: wave 1; wave 2 up to
+    the fresh prompt; the rest.  Within a phase every slot is distinct, but
+    blocks the fresh prompt wrote are evicted and written again later in
+    wave 2.  ``extra`` also holds the live sequence ids (decode order) and the
+    counts the design fixes."""
+    assert 0 < evict_blocks <= system_blocks and block_size >= 2
+    rng = np.random.default_rng(seed)
+    B = block_size
+    systems = [rng.integers(0, 32000, size=system_blocks * B).astype(np.int32) for _ in range(num_prompts)]
+
+    def request(p):
+        suf = rng.integers(0, 32000, size=int(rng.integers(1, B))).astype(np.int32)
+        return np.concatenate([systems[p], suf])
+
+    wave1: List[Tuple] = [(RETAIN, True)]
+    rows1 = 0
+    for r in range(requests_per_prompt):
+        for p in range(num_prompts):
+            toks = request(p)
+            wave1.append((NEW_CACHED, toks))
+            rows1 += len(toks)
+    n1 = num_prompts * requests_per_prompt
+    wave1 += [(FREE, i) for i in range(n1)]
+    # free stack after wave 1: the spare blocks and every request's partly
+    # filled block; each later request for a kept prompt takes one of them
+    free_after_hits = spare_blocks + n1 - (num_prompts - 1)
+    fresh_blocks = free_after_hits + evict_blocks
+    wave2: List[Tuple] = []
+    prompts2, rows2, lens = [], 0, []
+    for p in range(num_prompts - 1, 0, -1):
+        toks = request(p)
+        wave2.append((NEW_CACHED, toks))
+        prompts2.append(toks)
+    fresh = rng.integers(0, 32000, size=fresh_blocks * B).astype(np.int32)
+    wave2.append((NEW_CACHED, fresh))
+    ops2a, rows2a = len(wave2), sum(len(t) for t in prompts2) + len(fresh)
+    fresh_id = n1 + num_prompts - 1
+    wave2.append((FREE, fresh_id))
+    toks0 = request(0)
+    wave2.append((NEW_CACHED, toks0))
+    prompts2.append(toks0)
+    live = list(range(n1, fresh_id)) + [fresh_id + 1]
+    for seq in live:
+        wave2.append((APPEND, seq, 1))
+    rows2 = sum(len(t) for t in prompts2) + len(fresh) + len(live)
+    lens = [len(t) + 1 for t in prompts2]
+    num_blocks = num_prompts * system_blocks + n1 + spare_blocks
+    free_order = _shuffled_free_order(rng, num_blocks)
+    return Workload(name, dtype, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, seed, free_order,
+                    wave1 + wave2, np.asarray(lens, dtype=np.int32), rows1 + rows2,
+                    note="%d prompts of %d blocks x %d requests, then a wave that evicts %d blocks"
+                         % (num_prompts, system_blocks, requests_per_prompt, evict_blocks),
+                    extra={"phases": [(len(wave1), rows1), (ops2a, rows2a),
+                                      (len(wave2) - ops2a, rows2 - rows2a)], "live": live,
+                           "evicted_first_prompt": evict_blocks, "fresh_blocks": fresh_blocks,
+                           "cached_tokens_first_prompt": (system_blocks - evict_blocks) * B})
+
+
+def retention(small: bool = False) -> Workload:
+    """Prefix retention over two waves: 3 prompts of 8 blocks requested twice,
+    4 blocks evicted (the reduced case), or 4 prompts of 2000 tokens requested
+    three times, 60 blocks evicted; 32 q / 8 KV heads, head_dim 128,
+    block_size 16, bf16."""
+    if small:
+        return retention_workload("retention-small", 3, 2, 8, 9, 4, 32, 8, 128, 16, "bf16", 2700)
+    return retention_workload("retention", 4, 3, 125, 20, 60, 32, 8, 128, 16, "bf16", 1700)
 
 def workload(cfg: str, small: bool = False, block_size: Optional[int] = None,
              prompt_len: Optional[int] = None, placement: str = "random") -> Workload:

@@ -258,3 +258,32 @@ def test_a_freed_prompt_loses_its_tail_before_its_head():
     bm.free_seq(other)
     _, cached = bm.new_seq_cached(toks)
     assert cached == 4 and bm.evictable() == 0
+
+
+@pytest.mark.parametrize("small", [True, False])
+def test_retention_waves_match_oracle(small):
+    """The two-wave retention workload, phase by phase: identical slots and
+    tables, the designed prefix hits, and the first prompt keeping exactly
+    the blocks the fresh prompt did not evict (its tail went first)."""
+    wl = inputs.retention(small)
+    m = oracle.OracleBlockManager(wl.num_blocks, wl.block_size, wl.free_order)
+    bm = pa.BlockManager(wl.num_blocks, wl.block_size, wl.free_order)
+    op0 = 0
+    for ops, rows in wl.extra["phases"]:
+        script = wl.script[op0:op0 + ops]
+        r = oracle.run_script(0, wl.block_size, None, script, manager=m)
+        slots, pairs = bm.apply_script(script)
+        np.testing.assert_array_equal(slots, r["slots"])
+        assert len(slots) == rows and len(pairs) == 0 and len(r["pairs"]) == 0
+        assert bm.evictable() == len(m.evictable)
+        assert bm.cache_stats() == (len(m.cached), m.hits, m.lookups)
+        op0 += ops
+    assert op0 == len(wl.script)
+    live = wl.extra["live"]
+    tables, lens = bm.export(live, wl.max_blocks_per_seq)
+    np.testing.assert_array_equal(tables, oracle.pad_tables([m.tables[s] for s in live], wl.max_blocks_per_seq))
+    np.testing.assert_array_equal(lens, wl.seq_lens)
+    # the last phase: the fresh request freed, then the first prompt's request
+    first_len = len(wl.script[op0 - 1 - len(live)][1])
+    cached = int((slots[:first_len] < 0).sum())
+    assert cached == wl.extra["cached_tokens_first_prompt"] and slots[cached] >= 0
