@@ -398,13 +398,16 @@ pa_status_t pa_bm_cache_stats(const pa_bm_t *bm, int32_t *cached_blocks_out, int
                               int64_t *lookups_out);
 
 /* Retention of prefix-cached blocks (off by default; the eviction of the
- * hands-on exercise of [PidokuInfra 10] section 10 A).  On: a registered
- * block whose refcount reaches 0 stays registered as evictable instead of
- * returning to the free list; a later prompt that hits it revives it; an
- * allocation takes free blocks first and then evicts the least recently
- * released evictable blocks, one at a time onto the free stack (the hash
- * entry is dropped).  Evictable blocks count as free in pa_bm_stats.  Off:
- * evictable blocks become free, oldest first.  Never fails for a valid bm. */
+ * hands-on exercise of "10 PagedAttention" (PidokuInfra), section 10 A).  On:
+ * a registered block whose refcount reaches 0 stays registered as evictable
+ * instead of returning to the free list; a later prompt that hits it revives
+ * it; an allocation takes free blocks first and then evicts the least
+ * recently released evictable blocks, one at a time onto the free stack (the
+ * hash entry is dropped).  The blocks one pa_bm_free_seq releases count as
+ * released from the sequence's last block to its first, so a prompt loses
+ * its tail before its head (prefix matching stops at the first miss).
+ * Evictable blocks count as free in pa_bm_stats.  Off: evictable blocks
+ * become free, oldest first.  Never fails for a valid bm. */
 pa_status_t pa_bm_set_prefix_retention(pa_bm_t *bm, int32_t on);
 
 /* Number of evictable (retained, refcount 0) blocks. */
