@@ -14,7 +14,7 @@ import os
 import numpy as np
 
 from .build import build_oracle
-from .block_manager import OracleBlockManager, pad_tables, run_script
+from .block_manager import OracleBlockManager, pad_tables, run_script, sampling_memory
 
 F32 = 0
 BF16 = 1

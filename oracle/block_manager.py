@@ -309,6 +309,29 @@ def run_script(num_blocks, block_size, free_order, script, manager=None):
     }
 
 
+
+def sampling_memory(prompt_len, gen_lens, block_size):
+    """Parallel sampling with and without sharing ([PidokuInfra 10] section
+    10 E, on the sharing of section 5): blocks held after every sample has
+    generated its tokens, when the samples fork one prompt sequence (each
+    appending in turn) and when each holds its own prompt.  Returns
+    (shared_blocks, unshared_blocks, copies)."""
+    n = len(gen_lens)
+    pool = sum(-(-(prompt_len + g) // block_size) for g in gen_lens) + 1
+    m = OracleBlockManager(pool, block_size)
+    root = m.new_sequence(prompt_len)
+    seqs = [root] + [m.fork(root) for _ in range(n - 1)]
+    copies = 0
+    for seq, g in zip(seqs, gen_lens):
+        for _ in range(g):
+            copies += m.append_token(seq)[1] is not None
+    u = OracleBlockManager(pool, block_size)
+    for g in gen_lens:
+        seq = u.new_sequence(prompt_len)
+        for _ in range(g):
+            u.append_token(seq)
+    return m.stats()[1], u.stats()[1], copies
+
 def pad_tables(tables, max_blocks):
     """Tables as an int32 [num_seqs, max_blocks] array, unused entries -1."""
     import numpy as np

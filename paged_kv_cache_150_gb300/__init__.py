@@ -457,6 +457,39 @@ class BlockManager:
         return slots, np.asarray(pairs, dtype=np.int32).reshape(-1, 2)
 
 
+
+def sampling_memory(prompt_len, gen_lens, block_size=16):
+    """Parallel sampling of len(gen_lens) completions from one prompt, with and
+    without block sharing (hands-on exercise E of "10 PagedAttention"
+    (PidokuInfra); the sharing of its section 5 "Copy-on-write sharing").
+
+    Shared: one sequence holds the prompt, the other samples fork it, and
+    each sample in turn appends its generated tokens (a write into a shared,
+    partly filled block copies it first).  Unshared: every sample holds its
+    own copy of the prompt.  Returns the blocks each way holds at the end,
+    the fraction sharing saves and the copy-on-write copies it made."""
+    gen_lens = [int(g) for g in gen_lens]
+    B = int(block_size)
+    n = len(gen_lens)
+    if n == 0 or prompt_len < 0 or min(gen_lens) < 0:
+        raise ValueError("need at least one sample and non-negative lengths")
+    pool = sum(-(-(prompt_len + g) // B) for g in gen_lens) + 1
+    shared = BlockManager(pool, B)
+    root = shared.new_seq(prompt_len)
+    seqs = [root] + [shared.fork(root) for _ in range(n - 1)]
+    copies = 0
+    for seq, g in zip(seqs, gen_lens):
+        if g:
+            copies += shared.append_tokens(seq, g)[1] is not None
+    alone = BlockManager(pool, B)
+    for g in gen_lens:
+        seq = alone.new_seq(prompt_len)
+        if g:
+            alone.append_tokens(seq, g)
+    used_shared, used_alone = shared.stats()[1], alone.stats()[1]
+    return {"shared_blocks": used_shared, "unshared_blocks": used_alone,
+            "saved_fraction": 1.0 - used_shared / used_alone if used_alone else 0.0, "copies": copies}
+
 def simulate(policy, arrival_step, prompt_len, output_len, total_slots, block_size=16, max_new_tokens=2048,
              max_steps=10 ** 7):
     """Run the host allocation simulator (pa_sim_run): policy "contiguous"
@@ -480,5 +513,5 @@ __all__ = [
     "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_workspace_bytes", "pa_decode_no_alloc",
     "pa_decode_default_splits", "pa_decode_launch_count", "pa_get_device_error", "pa_selftest_wait_timeout",
     "pa_split_range", "pa_split_owner",
-    "BlockManager", "PagedAttentionError", "simulate", "version",
+    "BlockManager", "PagedAttentionError", "sampling_memory", "simulate", "version",
 ]

@@ -287,3 +287,14 @@ def test_retention_waves_match_oracle(small):
     first_len = len(wl.script[op0 - 1 - len(live)][1])
     cached = int((slots[:first_len] < 0).sum())
     assert cached == wl.extra["cached_tokens_first_prompt"] and slots[cached] >= 0
+
+
+def test_sampling_memory_matches_oracle():
+    rng = np.random.default_rng(12)
+    cases = [(48, [16] * 4, 16), (2000, [1, 256, 100, 37], 16), (2008, [5, 0, 9, 300], 16), (0, [3, 3], 4)]
+    for _ in range(30):
+        B = int(rng.choice([1, 8, 16, 32]))
+        cases.append((int(rng.integers(0, 400)), [int(x) for x in rng.integers(0, 90, size=int(rng.integers(1, 6)))], B))
+    for P, gens, B in cases:
+        got = pa.sampling_memory(P, gens, B)
+        assert (got["shared_blocks"], got["unshared_blocks"], got["copies"]) == oracle.sampling_memory(P, gens, B)
