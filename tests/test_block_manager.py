@@ -184,12 +184,14 @@ def test_beam_search_manager_matches_oracle(small):
         assert bm.stats() == m.stats()
 
 
-def test_prefix_retention_matches_oracle_under_pool_pressure():
+@pytest.mark.parametrize("seed", [11, 12, 13, 14])
+def test_prefix_retention_matches_oracle_under_pool_pressure(seed):
     """Retention on, a pool small enough that allocations evict: the C++
     manager and the oracle model agree on every hit, table, free count,
-    cache counter and evictable count, through frees, appends, failed
-    allocations (no state change) and switching retention off."""
-    rng = np.random.default_rng(11)
+    cache counter and evictable count, through forks, appends with
+    copy-on-write, frees, failed allocations (no state change) and switching
+    retention off."""
+    rng = np.random.default_rng(seed)
     order = rng.permutation(16).astype(np.int32)
     bm = pa.BlockManager(16, 8, order)
     m = oracle.OracleBlockManager(16, 8, order)
@@ -197,7 +199,7 @@ def test_prefix_retention_matches_oracle_under_pool_pressure():
     m.set_retention(True)
     prompts = [rng.integers(0, 30, size=int(rng.integers(16, 70))).tolist() for _ in range(5)]
     live = []
-    failures = most_evictable = evicted = 0
+    failures = most_evictable = evicted = forks = copies = 0
     for step in range(150):
         if step == 120:  # retention off: evictable blocks become free, oldest first
             bm.set_prefix_retention(False)
@@ -217,10 +219,22 @@ def test_prefix_retention_matches_oracle_under_pool_pressure():
             assert bm.block_table(got[0]) == m.tables[want[0]]
             # registered blocks only go away by eviction while retention is on
             evicted += step < 120 and len(m.cached) < registered
-        if live and rng.random() < 0.5:  # some growth of a live sequence
+        if live and rng.random() < 0.25:  # a fork shares every block, cached ones included
+            parent = live[int(rng.integers(0, len(live)))]
+            child = m.fork(parent)
+            assert bm.fork(parent) == child
+            live.append(child)
+            forks += 1
+        if live and rng.random() < 0.6:  # growth of a live sequence, copying a shared partial block
             s = live[int(rng.integers(0, len(live)))]
-            if m.append_token(s) is not None:
-                bm.append_tokens(s, 1)
+            want = m.append_token(s)
+            if want is None:
+                with pytest.raises(pa.PagedAttentionError):
+                    bm.append_tokens(s, 1)
+            else:
+                slots, pair = bm.append_tokens(s, 1)
+                assert (int(slots[0]), pair) == want
+                copies += pair is not None
         while len(live) > 4 or (live and rng.random() < 0.3):
             victim = live.pop(int(rng.integers(0, len(live))))
             bm.free_seq(victim)
@@ -229,7 +243,7 @@ def test_prefix_retention_matches_oracle_under_pool_pressure():
         assert bm.cache_stats() == (len(m.cached), m.hits, m.lookups)
         assert bm.evictable() == len(m.evictable)
         most_evictable = max(most_evictable, len(m.evictable))
-    assert failures > 0 and m.hits > 0 and most_evictable > 0 and evicted > 0
+    assert failures > 0 and m.hits > 0 and most_evictable > 0 and evicted > 0 and forks > 0 and copies > 0
 
 
 def test_retained_prompt_is_hit_again_after_its_sequence_is_freed():
