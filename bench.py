@@ -648,11 +648,13 @@ def run_reference(args, rank, world):
     # one step = a bounded sample of (sequence, KV head) groups, sized so the
     # whole run stays within a few minutes
     budget_s = 150.0
-    t0 = time.perf_counter()
-    oracle.decode(host["q"], kc, vc, tables, r["lens"], wl.scale,
-                  pairs=[(0, j) for j in range(G)], num_threads=threads)
-    t_group = time.perf_counter() - t0
+    for _ in range(2):  # the second call is timed: the first also faults in the caches' pages
+        t0 = time.perf_counter()
+        oracle.decode(host["q"], kc, vc, tables, r["lens"], wl.scale,
+                      pairs=[(0, j) for j in range(G)], num_threads=threads)
+        t_group = time.perf_counter() - t0
     per_step = max(1, min(len(groups_all), int(budget_s / max(args.steps + args.warmup, 1) / max(t_group, 1e-6))))
+    used = min(threads, per_step * G)  # the oracle's threads split the step's (sequence, head) pairs
     times, nbytes = [], 0
     for i in range(args.warmup + args.steps):
         gs = [groups_all[(i * per_step + j) % len(groups_all)] for j in range(per_step)]
@@ -671,8 +673,9 @@ def run_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": describe(wl), "kv_bytes_per_step": wl.kv_bytes_read(),
                    "per_step_sample": "%d (sequence, KV head) groups, all query heads" % per_step},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                         "sample": "%d groups per step of %d" % (per_step, len(groups_all))},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
+                         "sample": "%d groups (%d sequence-head pairs) per step of %d groups; %d host threads"
+                                   % (per_step, per_step * G, len(groups_all), threads)},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
