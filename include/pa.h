@@ -52,7 +52,8 @@ typedef enum pa_status {
     PA_ERR_DEVICE_BOUNDS = -5,  /* a kernel met an index outside the pool or the table */
     PA_ERR_DEVICE_TIMEOUT = -6, /* a kernel's bounded wait on an mbarrier ran out */
     PA_ERR_WORKSPACE = -7,      /* the decode workspace is smaller than required */
-    PA_ERR_DEVICE_PLAN = -8     /* a shared-prefix plan does not match its decode call */
+    PA_ERR_DEVICE_PLAN = -8,    /* a shared-prefix plan does not match its decode call */
+    PA_ERR_HOST_MEMORY = -9     /* a host allocation failed (host-side calls only) */
 } pa_status_t;
 
 typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1 } pa_dtype_t;
@@ -265,7 +266,8 @@ pa_status_t pa_decode_no_alloc(void *out, const void *q, const void *k_cache, co
  *            device: a plan built from other tables gives wrong results.
  * info       optional (NULL allowed): groups, member sequences, shared blocks.
  * Returns PA_ERR_INVALID_ARG for bad sizes or null pointers, or when a
- * length is outside [0, max_blocks_per_seq * B].
+ * length is outside [0, max_blocks_per_seq * B], and PA_ERR_HOST_MEMORY when
+ * its host scratch cannot be allocated.
  * The tensor-core kernel uses the plan when Hk is a multiple of 4, the launch
  * has at least 2 CTAs and q is 16-byte aligned; otherwise (and in the
  * CUDA-core kernel) the plan is ignored and the call runs without sharing.
@@ -339,7 +341,10 @@ pa_status_t pa_selftest_wait_timeout(int64_t limit_ns, pa_stream_t stream);
  *   refcount drops by one, and the (src, dst) pair is returned for
  *   pa_copy_blocks), so a shared block is never written in place;
  * - the slot of a token is table[pos / B] * B + pos % B (PhysicalIndex).
- * Sequence ids are assigned 0, 1, 2, ... in creation order.
+ * Sequence ids are assigned 0, 1, 2, ... in creation order.  A call that
+ * runs out of host memory returns PA_ERR_HOST_MEMORY; it is the one failure
+ * that may leave a partial change behind, so the handle should then be
+ * destroyed.
  * ---------------------------------------------------------------------- */
 typedef struct pa_bm pa_bm_t;
 
@@ -451,6 +456,8 @@ typedef struct pa_sim_result {
     double utilization;      /* sum_used / sum_held */
 } pa_sim_result_t;
 
+/* Returns PA_ERR_INVALID_ARG for arguments outside the rules above and
+ * PA_ERR_HOST_MEMORY when its host state cannot be allocated. */
 pa_status_t pa_sim_run(const pa_sim_config_t *cfg, const int32_t *arrival_step, const int32_t *prompt_len,
                        const int32_t *output_len, int32_t num_requests, pa_sim_result_t *out);
 

@@ -17,6 +17,7 @@ PA_ERR_DEVICE_BOUNDS = -5
 PA_ERR_DEVICE_TIMEOUT = -6
 PA_ERR_WORKSPACE = -7
 PA_ERR_DEVICE_PLAN = -8
+PA_ERR_HOST_MEMORY = -9
 
 PA_F32 = 0
 PA_BF16 = 1

@@ -109,11 +109,9 @@ struct pa_bm {
     }
 };
 
-extern "C" pa_bm_t *pa_bm_create(int32_t num_blocks, int32_t block_size, const int32_t *free_order) {
-    if (num_blocks < 0 || block_size <= 0) return nullptr;
-    if ((int64_t)num_blocks * block_size >= ((int64_t)1 << 31)) return nullptr;
-    pa_bm *bm = new (std::nothrow) pa_bm();
-    if (!bm) return nullptr;
+// Sizes a new manager and fills its free stack (the caller's order, or ids
+// from num_blocks-1 down to 0); a bad order leaves num_blocks = -1.
+static void fill_new(pa_bm *bm, int32_t num_blocks, int32_t block_size, const int32_t *free_order) {
     bm->num_blocks = num_blocks;
     bm->block_size = block_size;
     bm->ref.assign((size_t)num_blocks, 0);
@@ -123,8 +121,8 @@ extern "C" pa_bm_t *pa_bm_create(int32_t num_blocks, int32_t block_size, const i
         for (int32_t i = 0; i < num_blocks; ++i) {
             const int32_t b = free_order[i];
             if (b < 0 || b >= num_blocks || seen[b]) {
-                delete bm;
-                return nullptr;
+                bm->num_blocks = -1;
+                return;
             }
             seen[b] = 1;
             bm->free.push_back(b);
@@ -132,12 +130,29 @@ extern "C" pa_bm_t *pa_bm_create(int32_t num_blocks, int32_t block_size, const i
     } else {
         for (int32_t b = num_blocks - 1; b >= 0; --b) bm->free.push_back(b);
     }
+}
+
+extern "C" pa_bm_t *pa_bm_create(int32_t num_blocks, int32_t block_size, const int32_t *free_order) {
+    if (num_blocks < 0 || block_size <= 0) return nullptr;
+    if ((int64_t)num_blocks * block_size >= ((int64_t)1 << 31)) return nullptr;
+    pa_bm *bm = new (std::nothrow) pa_bm();
+    if (!bm) return nullptr;
+    try {
+        fill_new(bm, num_blocks, block_size, free_order);
+    } catch (const std::bad_alloc &) {
+        delete bm;
+        return nullptr;
+    }
+    if (bm->num_blocks < 0) {  // a bad free order
+        delete bm;
+        return nullptr;
+    }
     return bm;
 }
 
 extern "C" void pa_bm_destroy(pa_bm_t *bm) { delete bm; }
 
-extern "C" pa_status_t pa_bm_new_seq(pa_bm_t *bm, int32_t num_tokens, int32_t *seq_out) {
+extern "C" pa_status_t pa_bm_new_seq(pa_bm_t *bm, int32_t num_tokens, int32_t *seq_out) try {
     if (!bm || num_tokens < 0 || !seq_out) return PA_ERR_INVALID_ARG;
     const int32_t n = bm->blocks_needed(num_tokens);
     if ((int64_t)n > bm->available()) return PA_ERR_NO_BLOCKS;
@@ -149,9 +164,11 @@ extern "C" pa_status_t pa_bm_new_seq(pa_bm_t *bm, int32_t num_tokens, int32_t *s
     bm->seqs.push_back(std::move(s));
     *seq_out = (int32_t)bm->seqs.size() - 1;
     return PA_OK;
+} catch (const std::bad_alloc &) {
+    return PA_ERR_HOST_MEMORY;
 }
 
-extern "C" pa_status_t pa_bm_fork(pa_bm_t *bm, int32_t parent, int32_t *child_out) {
+extern "C" pa_status_t pa_bm_fork(pa_bm_t *bm, int32_t parent, int32_t *child_out) try {
     if (!bm || !child_out) return PA_ERR_INVALID_ARG;
     const pa_bm::Seq *p = bm->get(parent);
     if (!p) return PA_ERR_INVALID_ARG;
@@ -163,9 +180,11 @@ extern "C" pa_status_t pa_bm_fork(pa_bm_t *bm, int32_t parent, int32_t *child_ou
     bm->seqs.push_back(std::move(c));
     *child_out = (int32_t)bm->seqs.size() - 1;
     return PA_OK;
+} catch (const std::bad_alloc &) {
+    return PA_ERR_HOST_MEMORY;
 }
 
-extern "C" pa_status_t pa_bm_free_seq(pa_bm_t *bm, int32_t seq) {
+extern "C" pa_status_t pa_bm_free_seq(pa_bm_t *bm, int32_t seq) try {
     if (!bm) return PA_ERR_INVALID_ARG;
     pa_bm::Seq *s = bm->get(seq);
     if (!s) return PA_ERR_INVALID_ARG;
@@ -187,10 +206,12 @@ extern "C" pa_status_t pa_bm_free_seq(pa_bm_t *bm, int32_t seq) {
     s->live = false;
     s->len = 0;
     return PA_OK;
+} catch (const std::bad_alloc &) {
+    return PA_ERR_HOST_MEMORY;
 }
 
 extern "C" pa_status_t pa_bm_append_tokens(pa_bm_t *bm, int32_t seq, int32_t count, int32_t *slots_out,
-                                           int32_t *cow_pairs_out, int32_t *num_pairs_out) {
+                                           int32_t *cow_pairs_out, int32_t *num_pairs_out) try {
     if (!bm || count < 0 || (count > 0 && !slots_out)) return PA_ERR_INVALID_ARG;
     pa_bm::Seq *s = bm->get(seq);
     if (!s) return PA_ERR_INVALID_ARG;
@@ -221,6 +242,8 @@ extern "C" pa_status_t pa_bm_append_tokens(pa_bm_t *bm, int32_t seq, int32_t cou
     }
     s->len = pos0 + count;
     return PA_OK;
+} catch (const std::bad_alloc &) {
+    return PA_ERR_HOST_MEMORY;
 }
 
 extern "C" pa_status_t pa_bm_append_token(pa_bm_t *bm, int32_t seq, int32_t *slot_out, int32_t *cow_src,
@@ -322,7 +345,7 @@ uint64_t block_chain_hash(uint64_t parent, const int32_t *tokens, int32_t B) {
 }  // namespace
 
 extern "C" pa_status_t pa_bm_new_seq_cached(pa_bm_t *bm, const int32_t *token_ids, int32_t num_tokens,
-                                            int32_t *seq_out, int32_t *num_cached_tokens_out) {
+                                            int32_t *seq_out, int32_t *num_cached_tokens_out) try {
     if (!bm || num_tokens < 0 || (num_tokens > 0 && !token_ids) || !seq_out) return PA_ERR_INVALID_ARG;
     const int32_t B = bm->block_size;
     const int32_t n_full = num_tokens / B;
@@ -374,6 +397,8 @@ extern "C" pa_status_t pa_bm_new_seq_cached(pa_bm_t *bm, const int32_t *token_id
     *seq_out = (int32_t)bm->seqs.size() - 1;
     if (num_cached_tokens_out) *num_cached_tokens_out = reused * B;
     return PA_OK;
+} catch (const std::bad_alloc &) {
+    return PA_ERR_HOST_MEMORY;
 }
 
 extern "C" pa_status_t pa_bm_slots(const pa_bm_t *bm, int32_t seq, int32_t first_pos, int32_t count,
@@ -385,13 +410,15 @@ extern "C" pa_status_t pa_bm_slots(const pa_bm_t *bm, int32_t seq, int32_t first
     return PA_OK;
 }
 
-extern "C" pa_status_t pa_bm_set_prefix_retention(pa_bm_t *bm, int32_t on) {
+extern "C" pa_status_t pa_bm_set_prefix_retention(pa_bm_t *bm, int32_t on) try {
     if (!bm) return PA_ERR_INVALID_ARG;
     if (on && bm->lru_it.empty()) bm->lru_it.resize((size_t)bm->num_blocks);
     if (!on)  // the evictable blocks become plain free blocks, oldest first
         while (!bm->lru.empty()) bm->evict_oldest();
     bm->retain = on != 0;
     return PA_OK;
+} catch (const std::bad_alloc &) {
+    return PA_ERR_HOST_MEMORY;
 }
 
 extern "C" pa_status_t pa_bm_evictable(const pa_bm_t *bm, int32_t *count_out) {

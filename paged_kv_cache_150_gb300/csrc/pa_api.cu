@@ -62,6 +62,7 @@ extern "C" const char *pa_status_string(pa_status_t status) {
         case PA_ERR_UNSUPPORTED: return "unsupported combination (no kernel variant)";
         case PA_ERR_CUDA: return "CUDA error";
         case PA_ERR_NO_BLOCKS: return "no free KV blocks";
+        case PA_ERR_HOST_MEMORY: return "host memory allocation failed";
         case PA_ERR_DEVICE_BOUNDS: return "kernel met an index outside the pool or table";
         case PA_ERR_DEVICE_TIMEOUT: return "kernel wait timed out";
         case PA_ERR_WORKSPACE: return "workspace too small";

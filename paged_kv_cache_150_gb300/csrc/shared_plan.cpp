@@ -14,6 +14,7 @@
 // at least one position after it (P * B < L), and the group is dropped when
 // P < min_shared_blocks.
 #include <unordered_map>
+#include <new>
 #include <vector>
 
 #include "pa_internal.h"
@@ -29,7 +30,7 @@ extern "C" size_t pa_shared_plan_ints(int32_t num_seqs) {
 extern "C" pa_status_t pa_shared_plan_build(const int32_t *block_tables, int32_t max_blocks_per_seq,
                                             const int32_t *seq_lens, int32_t num_seqs, int32_t block_size,
                                             int32_t num_heads, int32_t num_kv_heads, int32_t min_shared_blocks,
-                                            int32_t *plan, size_t plan_ints, pa_shared_plan_info_t *info) {
+                                            int32_t *plan, size_t plan_ints, pa_shared_plan_info_t *info) try {
     const int32_t N = num_seqs;
     if (N < 0 || !plan || block_size <= 0 || max_blocks_per_seq <= 0 || num_kv_heads <= 0 || num_heads <= 0 ||
         num_heads % num_kv_heads != 0 || min_shared_blocks < 1)
@@ -134,4 +135,6 @@ extern "C" pa_status_t pa_shared_plan_build(const int32_t *block_tables, int32_t
         info->saved_blocks = saved;
     }
     return PA_OK;
+} catch (const std::bad_alloc &) {
+    return PA_ERR_HOST_MEMORY;
 }

@@ -21,6 +21,7 @@
 #include <cstdint>
 #include <deque>
 #include <map>
+#include <new>
 #include <vector>
 
 #include "pa.h"
@@ -71,7 +72,7 @@ struct Intervals {
 
 extern "C" pa_status_t pa_sim_run(const pa_sim_config_t *cfg, const int32_t *arrival_step,
                                   const int32_t *prompt_len, const int32_t *output_len, int32_t num_requests,
-                                  pa_sim_result_t *out) {
+                                  pa_sim_result_t *out) try {
     if (!cfg || !out || num_requests < 0 || (num_requests > 0 && (!arrival_step || !prompt_len || !output_len)))
         return PA_ERR_INVALID_ARG;
     if (cfg->policy != PA_SIM_CONTIGUOUS && cfg->policy != PA_SIM_PAGED) return PA_ERR_INVALID_ARG;
@@ -164,4 +165,6 @@ extern "C" pa_status_t pa_sim_run(const pa_sim_config_t *cfg, const int32_t *arr
     out->utilization = out->sum_held > 0 ? (double)out->sum_used / (double)out->sum_held : 0.0;
     if (bm) pa_bm_destroy(bm);
     return PA_OK;
+} catch (const std::bad_alloc &) {
+    return PA_ERR_HOST_MEMORY;
 }

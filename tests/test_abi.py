@@ -38,6 +38,9 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings_and_version(lib):
     assert lib.pa_status_string(0) == b"ok"
     assert b"workspace" in lib.pa_status_string(-7)
+    names = [lib.pa_status_string(c) for c in range(0, -10, -1)]
+    assert len(set(names)) == 10 and b"unknown status" not in names  # every code, PA_ERR_HOST_MEMORY included
+    assert lib.pa_status_string(-10) == b"unknown status"
     assert b"sm_103a" in lib.pa_version()
 
 
