@@ -289,6 +289,8 @@ def test_retention_waves_match_oracle(small):
         slots, pairs = bm.apply_script(script)
         np.testing.assert_array_equal(slots, r["slots"])
         assert len(slots) == rows and len(pairs) == 0 and len(r["pairs"]) == 0
+        written = slots[slots >= 0]
+        assert len(np.unique(written)) == len(written)  # one cache write per phase stays race-free
         assert bm.evictable() == len(m.evictable)
         assert bm.cache_stats() == (len(m.cached), m.hits, m.lookups)
         op0 += ops
