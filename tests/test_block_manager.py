@@ -34,6 +34,12 @@ def test_manager_matches_oracle_model(cfg, kw):
     slots, pairs = bm.apply_script(wl.script)
     np.testing.assert_array_equal(slots, r["slots"])
     np.testing.assert_array_equal(pairs, r["pairs"])
+    # the step writes every row in one call and copies every pair in another:
+    # distinct written slots, distinct copy destinations, no destination read
+    written = slots[slots >= 0]
+    assert len(np.unique(written)) == len(written)
+    if len(pairs):
+        assert len(np.unique(pairs[:, 1])) == len(pairs) and not set(pairs[:, 1]) & set(pairs[:, 0])
     tables, lens = bm.export(list(range(wl.num_seqs)), wl.max_blocks_per_seq)
     np.testing.assert_array_equal(tables, oracle.pad_tables(r["tables"], wl.max_blocks_per_seq))
     np.testing.assert_array_equal(lens, r["lens"])
