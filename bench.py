@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--workload", default="cfg4-b16",
                     help="headline workload: cfg4-b16 (default), cfg4-b32, cfg2, cfg1, cfg3-p2000, cfg3-p2008, "
-                         "cfg4-b16-split, cfg2-split, prefix")
+                         "cfg4-b16-split, cfg2-split, prefix, cfg0 (tiny fp32)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-write-copy", action="store_true",
@@ -70,10 +70,22 @@ WORKLOADS = {"cfg4-b16": ("cfg4", {"block_size": 16}), "cfg4-b32": ("cfg4", {"bl
              "cfg2-split": ("cfg2", {"layout": "split"}), "prefix": ("prefix", {}),
              "cfg4-b16-contiguous": ("cfg4", {"block_size": 16, "placement": "contiguous"}),
              "cfg3-p2008-shared": ("cfg3", {"prompt_len": 2008, "shared": True}),
-             "prefix-shared": ("prefix", {"shared": True})}
+             "prefix-shared": ("prefix", {"shared": True}), "cfg0": ("cfg0", {})}
 
 
 # ---------------------------------------------------------------- helpers
+def make_workload(cfg, kw):
+    """(workload, cache layout, shared-prefix plan) of a bench name's (cfg,
+    options): "layout" and "shared" choose how the CUDA path runs; the other
+    options go to inputs.workload."""
+    from paged_kv_cache_150_gb300 import inputs
+
+    kw = dict(kw)
+    layout = kw.pop("layout", "row")
+    shared = kw.pop("shared", False)
+    return inputs.workload(cfg, **kw), layout, shared
+
+
 def dist_setup(args):
     import torch
 
@@ -211,10 +223,7 @@ class Step:
         from paged_kv_cache_150_gb300 import inputs
 
         self.pa = pa
-        kw = dict(kw)
-        layout = kw.pop("layout", "row")
-        shared = kw.pop("shared", False)
-        wl = inputs.workload(cfg, **kw)
+        wl, layout, shared = make_workload(cfg, kw)
         wl.seed += seed_offset
         if layout == "split":
             wl.name += "-split"
@@ -555,7 +564,7 @@ def run_ours(args, rank, world):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": step.wl.dtype, "data": "synthetic",
         "config": {"workload": describe(step.wl),
                    "kv_bytes_per_step": step.kv_bytes, "num_seqs": step.wl.num_seqs,
                    "max_seq_len": int(step.wl.seq_lens.max()), "block_size": step.wl.block_size,
@@ -564,7 +573,8 @@ def run_ours(args, rank, world):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tokens_per_s": round(tokens_per_s, 1),
         "hbm_frac": round(value / world / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "decode attention (tensor-core kernel)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "decode attention (%s kernel)" % ("tensor-core" if step.wl.dtype == "bf16" else "CUDA-core"),
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": step.kernel_bytes,
@@ -633,8 +643,7 @@ def run_reference(args, rank, world):
     import oracle
     from paged_kv_cache_150_gb300 import inputs
 
-    cfg, kw = WORKLOADS[args.workload]
-    wl = inputs.workload(cfg, **kw)
+    wl, _, _ = make_workload(*WORKLOADS[args.workload])  # the oracle reads the row layout
     vals = inputs.make_values(wl, device="cpu")
     host = {k: inputs.to_numpy_elems(v).copy() for k, v in vals.items()}
     r = oracle.run_script(wl.num_blocks, wl.block_size, wl.free_order, wl.script)
