@@ -693,14 +693,14 @@ def run_reference(args, rank, world):
 
 def main():
     args = parse()
+    if args.impl == "reference":  # host cores only: rank 0 runs it, other ranks exit without work
+        run_reference(args, int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")))
+        return
     rank, world, _ = dist_setup(args)
-    if args.impl == "reference":
-        run_reference(args, rank, world)
-    else:
-        import __graft_entry__
+    import __graft_entry__
 
-        __graft_entry__.build()
-        run_ours(args, rank, world)
+    __graft_entry__.build()
+    run_ours(args, rank, world)
     if world > 1:
         import torch.distributed as dist
 
