@@ -53,7 +53,7 @@ typedef enum pa_status {
     PA_ERR_DEVICE_TIMEOUT = -6, /* a kernel's bounded wait on an mbarrier ran out */
     PA_ERR_WORKSPACE = -7,      /* the decode workspace is smaller than required */
     PA_ERR_DEVICE_PLAN = -8,    /* a shared-prefix plan does not match its decode call */
-    PA_ERR_HOST_MEMORY = -9     /* a host allocation failed (host-side calls only) */
+    PA_ERR_HOST_MEMORY = -9     /* a host allocation failed (no C++ exception ever leaves a call) */
 } pa_status_t;
 
 typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1 } pa_dtype_t;
@@ -179,11 +179,16 @@ typedef struct pa_decode_opts {
     const int32_t *shared_plan;  /* optional device copy of a pa_shared_plan_build plan (NULL = none) */
     /* Optional HOST copy of seq_lens (num_seqs entries; NULL = none), a hint
      * read on the host during the call.  With it, when some sequence is cut
-     * into 5 or more pieces (long contexts), those sequences are merged by a
+     * into 8 or more pieces (long contexts), those sequences are merged by a
      * second kernel that spreads their merges over the GPU instead of
-     * leaving each to the CTA that finishes last.  Without it, or with any
-     * other values, the results are the same: the device decides per
-     * sequence from seq_lens itself; only which merge path runs changes. */
+     * leaving each to the CTA that finishes last.  The hint only chooses the
+     * merge path; the device decides per sequence from seq_lens itself, so a
+     * missing or wrong hint never gives a wrong result.  The two paths fold
+     * the pieces in different batches (the running maximum is rescaled at
+     * different points), so for sequences cut into 8 or more pieces the
+     * outputs with and without the hint agree to rounding, not bit for bit;
+     * every other output is the same bits either way.  A given call (same
+     * arguments, hint included) always gives the same bits. */
     const int32_t *host_seq_lens;
 } pa_decode_opts_t;
 
@@ -212,7 +217,9 @@ pa_status_t pa_decode(void *out, const void *q, const void *k_cache, const void 
  *
  * - The first call on a device looks up that array's device address (once,
  *   with that device current) and caches it; make this first call before
- *   any stream capture.
+ *   any stream capture.  The cached address belongs to the device's current
+ *   context: if that context changes (after cudaDeviceReset, say), the next
+ *   call looks the address up again.
  * - A shape whose workspace (pa_decode_workspace_bytes with the same
  *   options) exceeds PA_NO_ALLOC_SCRATCH_BYTES returns PA_ERR_WORKSPACE and
  *   launches nothing.

@@ -57,9 +57,21 @@ def _cache_desc(k_cache, v_cache):
                      "V [num_blocks, num_kv_heads, head_dim, block_size], x = 16 / element bytes")
 
 
-def _dev(t, name, dtype=None):
+def _current_device():
+    """Index of torch's current CUDA device: the library enqueues on that
+    device's current stream and looks up its per-device state there."""
+    return _torch().cuda.current_device()
+
+
+def _dev(t, name, dtype=None, device=None):
+    """Device pointer of contiguous CUDA tensor ``t``.  ``device``: the index
+    the tensor must be on (the current device; the library works there, so a
+    tensor on another GPU would be read through a foreign pointer)."""
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
+    if device is not None and t.device.index != device:
+        raise ValueError("%s is on cuda:%s but the current device is cuda:%d: make its device current "
+                         "(torch.cuda.device) before the call" % (name, t.device.index, device))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
     if dtype is not None and t.dtype != dtype:
@@ -90,9 +102,10 @@ def pa_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache):
     for name, t in (("k", k), ("v", v)):
         if t.dtype != k_cache.dtype:
             raise TypeError("%s element type differs from the cache" % name)
+    d = _current_device()
     st = _lib.load().pa_reshape_and_cache(
-        _dev(k, "k"), _dev(v, "v"), _dev(slot_mapping, "slot_mapping", torch.int32), T,
-        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(desc), _stream())
+        _dev(k, "k", device=d), _dev(v, "v", device=d), _dev(slot_mapping, "slot_mapping", torch.int32, d), T,
+        _dev(k_cache, "k_cache", device=d), _dev(v_cache, "v_cache", device=d), ctypes.byref(desc), _stream())
     _lib.check("pa_reshape_and_cache", st)
 
 
@@ -104,16 +117,17 @@ def pa_copy_blocks(k_cache, v_cache, src_dst_pairs):
     P = pairs.shape[0] if pairs.numel() else 0
     if P == 0:
         return
-    st = _lib.load().pa_copy_blocks(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
-                                    ctypes.byref(desc), _dev(pairs, "src_dst_pairs", torch.int32), P,
+    d = _current_device()
+    st = _lib.load().pa_copy_blocks(_dev(k_cache, "k_cache", device=d), _dev(v_cache, "v_cache", device=d),
+                                    ctypes.byref(desc), _dev(pairs, "src_dst_pairs", torch.int32, d), P,
                                     _stream())
     _lib.check("pa_copy_blocks", st)
 
 
-def _opts(num_splits, kernel, events, shared_plan=None):
+def _opts(num_splits, kernel, events, shared_plan=None, device=None):
     o = _lib.DecodeOpts(int(num_splits), _KERNELS[kernel], None, None, None)
     if shared_plan is not None:
-        o.shared_plan = _dev(shared_plan, "shared_plan", _torch().int32).value
+        o.shared_plan = _dev(shared_plan, "shared_plan", _torch().int32, device).value
     if events is not None:
         for e in events:
             if not e.cuda_event:  # torch creates the CUDA event on its first record
@@ -204,7 +218,8 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None, work
         out = torch.empty_like(q)
     elif out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("out must match q")
-    o = _opts(num_splits, kernel, events, shared_plan)
+    d = _current_device()
+    o = _opts(num_splits, kernel, events, shared_plan, d)
     host_lens = _set_host_lens(o, host_seq_lens, N)  # noqa: F841 (alive for the call)
     lib = _lib.load()
     if workspace is None:  # a caller's workspace is checked by the library (PA_ERR_WORKSPACE)
@@ -212,11 +227,11 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None, work
         if need == 0:
             raise PagedAttentionError("pa_decode_workspace_bytes", _lib.PA_ERR_UNSUPPORTED)
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    st = lib.pa_decode(_dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
-                       ctypes.byref(desc), _dev(block_tables, "block_tables", torch.int32),
-                       block_tables.shape[1], _dev(seq_lens, "seq_lens", torch.int32), N, H,
-                       float(scale), _dev(workspace, "workspace"), workspace.numel(),
-                       ctypes.byref(o), _stream())
+    st = lib.pa_decode(_dev(out, "out", device=d), _dev(q, "q", device=d), _dev(k_cache, "k_cache", device=d),
+                       _dev(v_cache, "v_cache", device=d), ctypes.byref(desc),
+                       _dev(block_tables, "block_tables", torch.int32, d), block_tables.shape[1],
+                       _dev(seq_lens, "seq_lens", torch.int32, d), N, H, float(scale),
+                       _dev(workspace, "workspace", device=d), workspace.numel(), ctypes.byref(o), _stream())
     _lib.check("pa_decode", st)
     return out
 
@@ -263,12 +278,14 @@ def pa_decode_no_alloc(q, k_cache, v_cache, block_tables, seq_lens, scale, out, 
         raise ValueError("block_tables must be [num_seqs, max_blocks] and seq_lens [num_seqs]")
     if out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("out must match q")
+    d = _current_device()
     o = _opts(num_splits, kernel, None)
     host_lens = _set_host_lens(o, host_seq_lens, N)  # noqa: F841 (alive for the call)
     st = _lib.load().pa_decode_no_alloc(
-        _dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(desc),
-        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
-        _dev(seq_lens, "seq_lens", torch.int32), N, H, float(scale), ctypes.byref(o), _stream())
+        _dev(out, "out", device=d), _dev(q, "q", device=d), _dev(k_cache, "k_cache", device=d),
+        _dev(v_cache, "v_cache", device=d), ctypes.byref(desc), _dev(block_tables, "block_tables", torch.int32, d),
+        block_tables.shape[1], _dev(seq_lens, "seq_lens", torch.int32, d), N, H, float(scale), ctypes.byref(o),
+        _stream())
     _lib.check("pa_decode_no_alloc", st)
     return out
 

@@ -48,7 +48,6 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
-#include <vector>
 
 #include "pa_internal.h"
 
@@ -112,26 +111,31 @@ constexpr int32_t kLongMergePieces = 8;
 
 // kLongMergePieces if, with these host lengths (clamped as the plan kernel
 // clamps them), some sequence is cut into that many pieces; else 0.  A hint
-// only: the device decides per sequence from its own seq_lens.
+// only: the device decides per sequence from its own seq_lens.  Two passes
+// over the lengths (the total, then a running prefix): nothing is allocated.
 int32_t long_merge_pieces(const int32_t *host_lens, int32_t N, int32_t B, int32_t max_len, int32_t NG, int32_t C) {
-    std::vector<int64_t> cu((size_t)N + 1, 0);
-    for (int32_t i = 0; i < N; ++i) {
+    auto blocks = [&](int32_t i) -> int64_t {
         int32_t L = host_lens[i];
         if (L < 0 || L > max_len) L = 0;
-        cu[(size_t)i + 1] = cu[(size_t)i] + (L + B - 1) / B;
-    }
-    const int64_t Wg = cu[(size_t)N], W = (int64_t)NG * Wg;
+        return (L + B - 1) / B;
+    };
+    int64_t Wg = 0;
+    for (int32_t i = 0; i < N; ++i) Wg += blocks(i);
+    const int64_t W = (int64_t)NG * Wg;
     if (W == 0) return 0;
     const int64_t Ce = std::min<int64_t>(C, W);
+    int64_t cu = 0;  // blocks of the sequences before i
     for (int32_t i = 0; i < N; ++i) {
-        const int64_t nb = cu[(size_t)i + 1] - cu[(size_t)i];
+        const int64_t nb = blocks(i);
         // nb blocks span at most nb * Ce / W + 2 CTAs: most sequences need no exact count
-        if (nb == 0 || nb * Ce < (int64_t)(kLongMergePieces - 2) * W) continue;
-        for (int32_t g = 0; g < NG; ++g) {
-            const int64_t x0 = g * Wg + cu[(size_t)i];
-            if (split_owner(x0 + nb - 1, W, Ce) - split_owner(x0, W, Ce) + 1 >= kLongMergePieces)
-                return kLongMergePieces;
+        if (nb > 0 && nb * Ce >= (int64_t)(kLongMergePieces - 2) * W) {
+            for (int32_t g = 0; g < NG; ++g) {
+                const int64_t x0 = g * Wg + cu;
+                if (split_owner(x0 + nb - 1, W, Ce) - split_owner(x0, W, Ce) + 1 >= kLongMergePieces)
+                    return kLongMergePieces;
+            }
         }
+        cu += nb;
     }
     return 0;
 }
@@ -148,8 +152,9 @@ const void *mma_kernel_ptr(int D, int B, int layout, bool shared) {
 }
 
 // Occupancy-based default split count: one full wave of resident CTAs.  The
-// answer is fixed per (device, kernel, threads, shared memory) and cached: the
-// occupancy query costs about a microsecond of host time per call.
+// answer is fixed per (device, kernel, threads, shared memory) and kept in a
+// fixed table: the occupancy query costs about a microsecond of host time per
+// call.  -1 on failure.
 int default_ctas(const void *fn, int threads, size_t smem) {
     struct Entry {
         int dev;
@@ -158,14 +163,18 @@ int default_ctas(const void *fn, int threads, size_t smem) {
         size_t smem;
         int ctas;
     };
+    constexpr int kEntries = 256;  // distinct (device, kernel, shape) answers kept; later ones are not cached
     static std::mutex mu;
-    static std::vector<Entry> cache;
+    static Entry cache[kEntries];
+    static int used = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     {
         std::lock_guard<std::mutex> lock(mu);
-        for (const Entry &e : cache)
+        for (int i = 0; i < used; ++i) {
+            const Entry &e = cache[i];
             if (e.dev == dev && e.fn == fn && e.threads == threads && e.smem == smem) return e.ctas;
+        }
     }
     const int sms = num_sms();
     if (sms <= 0) return -1;
@@ -176,7 +185,7 @@ int default_ctas(const void *fn, int threads, size_t smem) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess) return -1;
     const int ctas = sms * std::max(per_sm, 1);
     std::lock_guard<std::mutex> lock(mu);
-    if (cache.size() < 1024) cache.push_back(Entry{dev, fn, threads, smem, ctas});
+    if (used < kEntries) cache[used++] = Entry{dev, fn, threads, smem, ctas};
     return ctas;
 }
 
@@ -344,14 +353,16 @@ bool encode_cache_map(CUtensorMap *map, const void *base, const pa_cache_desc_t 
 using namespace pa;
 
 extern "C" size_t pa_decode_workspace_bytes(const pa_cache_desc_t *cache, int32_t num_seqs, int32_t num_heads,
-                                            const pa_decode_opts_t *opts) {
+                                            const pa_decode_opts_t *opts) try {
     DecodePlan p;
     if (make_plan(cache, num_seqs, num_heads, opts, true, &p) != PA_OK) return 0;
     return p.total;
+} catch (...) {
+    return 0;
 }
 
 extern "C" int32_t pa_decode_launch_count(const pa_cache_desc_t *cache, int32_t num_seqs, int32_t num_heads,
-                                          int32_t max_blocks_per_seq, const pa_decode_opts_t *opts) {
+                                          int32_t max_blocks_per_seq, const pa_decode_opts_t *opts) try {
     DecodePlan p;
     const pa_status_t st = make_plan(cache, num_seqs, num_heads, opts, true, &p);
     if (st != PA_OK) return (int32_t)st;
@@ -361,15 +372,19 @@ extern "C" int32_t pa_decode_launch_count(const pa_cache_desc_t *cache, int32_t 
     const int32_t min_pieces =
         call_min_pieces(p, opts, num_seqs, cache->block_size, max_blocks_per_seq * cache->block_size);
     return 2 + (p.shared ? 1 : 0) + (min_pieces > 0 ? 1 : 0);
+} catch (...) {
+    return (int32_t)host_failure();
 }
 
 extern "C" int32_t pa_decode_default_splits(const pa_cache_desc_t *cache, int32_t num_heads,
-                                            const pa_decode_opts_t *opts) {
+                                            const pa_decode_opts_t *opts) try {
     pa_decode_opts_t o = opts ? *opts : pa_decode_opts_t{0, PA_KERNEL_AUTO, nullptr, nullptr, nullptr, nullptr};
     o.num_splits = 0;
     DecodePlan p;
     const pa_status_t st = make_plan(cache, 1, num_heads, &o, true, &p);
     return st == PA_OK ? p.C : (int32_t)st;
+} catch (...) {
+    return (int32_t)host_failure();
 }
 
 extern "C" void pa_split_range(int64_t total_blocks, int32_t num_splits, int32_t c, int64_t *begin,
@@ -386,7 +401,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
                                  const pa_cache_desc_t *cache, const int32_t *block_tables,
                                  int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
                                  int32_t num_heads, float scale, void *workspace, size_t workspace_bytes,
-                                 const pa_decode_opts_t *opts, pa_stream_t stream) {
+                                 const pa_decode_opts_t *opts, pa_stream_t stream) try {
     DecodePlan p;
     pa_status_t st = make_plan(cache, num_seqs, num_heads, opts, true, &p);
     if (st != PA_OK) return st;
@@ -507,46 +522,37 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         return PA_ERR_CUDA;
 
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+} catch (...) {
+    return host_failure();
 }
 
 // ------------------------------------------------------------ no-alloc entry
 // Scratch of pa_decode_no_alloc: a fixed array in the library's device image
 // (one per GPU that loads the library, alive until exit).  Host code must not
 // pass `g_decode_scratch` itself to a kernel: on the host that name is only a
-// stand-in, so its device address is looked up per device below.
+// stand-in, so its device address is looked up per device (symbol_address).
 static __device__ __align__(256) unsigned char g_decode_scratch[PA_NO_ALLOC_SCRATCH_BYTES];
 
 namespace {
-std::mutex g_scratch_mu;
-void *g_scratch_addr[64];
-
-// Device address of g_decode_scratch on the current device, looked up on the
-// first call per device (with that device current) and cached; nullptr on
-// failure.
-void *no_alloc_scratch() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || !ptr) return nullptr;
-        g_scratch_addr[dev] = ptr;
-    }
-    return g_scratch_addr[dev];
-}
+SymbolCache g_scratch_cache;
 }  // namespace
 
 extern "C" pa_status_t pa_decode_no_alloc(void *out, const void *q, const void *k_cache, const void *v_cache,
                                           const pa_cache_desc_t *cache, const int32_t *block_tables,
                                           int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
                                           int32_t num_heads, float scale, const pa_decode_opts_t *opts,
-                                          pa_stream_t stream) {
+                                          pa_stream_t stream) try {
     DecodePlan p;
     const pa_status_t st = make_plan(cache, num_seqs, num_heads, opts, true, &p);
     if (st != PA_OK) return st;
     if (p.total > (size_t)PA_NO_ALLOC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
-    void *scratch = no_alloc_scratch();
+    // Looked up once per device (and again if the device's context changes),
+    // with that device current; host code never hands g_decode_scratch itself
+    // to a kernel.
+    void *scratch = symbol_address(&g_scratch_cache, (const void *)&g_decode_scratch);
     if (!scratch) return PA_ERR_CUDA;
     return pa_decode(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                      num_heads, scale, scratch, (size_t)PA_NO_ALLOC_SCRATCH_BYTES, opts, stream);
+} catch (...) {
+    return host_failure();
 }

@@ -1,6 +1,8 @@
 // Library-wide pieces of the C ABI: status strings, the per-device error word
 // that kernels set when they meet an index outside the pool (or a bounded wait
 // runs out), and cached device queries.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "pa_internal.h"
@@ -21,25 +23,60 @@ __global__ void selftest_wait_kernel(unsigned long long limit_ns, unsigned int *
 }
 
 namespace {
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-unsigned int *g_err_ptr[kMaxDevices];
+SymbolCache g_err_cache;
 int g_sms[kMaxDevices];
+
+// Unique id of the calling thread's current context (cuCtxGetId), or 0 when
+// there is none or the driver does not offer the query.  Both driver entry
+// points are resolved once.
+unsigned long long current_context_id() {
+    using GetCurrentFn = CUresult (*)(CUcontext *);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *a = nullptr, *b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) == cudaSuccess &&
+            qa == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+            qb == cudaDriverEntryPointSuccess) {
+            get_current = (GetCurrentFn)a;
+            get_id = (GetIdFn)b;
+        }
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 }  // namespace
 
-unsigned int *device_error_word() {
+void *symbol_address(SymbolCache *cache, const void *symbol) try {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_err_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
-        g_err_ptr[dev] = (unsigned int *)p;
+    unsigned long long id = current_context_id();
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (id != 0 && cache->ctx_id[dev] == id && cache->addr[dev]) return cache->addr[dev];
     }
-    return g_err_ptr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess || !p) return nullptr;
+    id = current_context_id();  // the lookup makes the device's primary context current
+    std::lock_guard<std::mutex> lock(g_mu);
+    cache->ctx_id[dev] = id;  // 0 (unknown): looked up again next time
+    cache->addr[dev] = p;
+    return p;
+} catch (...) {
+    return nullptr;
 }
 
-int num_sms() {
+unsigned int *device_error_word() { return (unsigned int *)symbol_address(&g_err_cache, (const void *)&g_error_word); }
+
+int num_sms() try {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     std::lock_guard<std::mutex> lock(g_mu);
@@ -49,6 +86,8 @@ int num_sms() {
         g_sms[dev] = n;
     }
     return g_sms[dev];
+} catch (...) {
+    return 0;
 }
 
 }  // namespace pa

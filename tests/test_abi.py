@@ -48,43 +48,59 @@ def _desc(nb=8, bs=16, hk=8, d=128, dt=_lib.PA_BF16):
     return _lib.CacheDesc(nb, bs, hk, d, dt)
 
 
+def _gpu_present():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:  # noqa: BLE001 (no torch or no driver: no GPU)
+        return False
+
+
 def test_host_validation_rejects_bad_arguments_without_a_gpu(lib):
+    """Host checks that come before any CUDA call.  Device pointers are None
+    except where the check under test needs a non-null one; those few cases
+    pass a non-null address that is never dereferenced and therefore run only
+    where no GPU is present (a regressed check then fails to find a device
+    instead of launching)."""
     d = _desc()
-    p = ctypes.c_void_p(0x1000)
     # null pointers / negative sizes / bad descriptors are caught before any CUDA call
-    assert lib.pa_reshape_and_cache(None, p, p, 4, p, p, ctypes.byref(d), None) == _lib.PA_ERR_INVALID_ARG
-    assert lib.pa_reshape_and_cache(p, p, p, -1, p, p, ctypes.byref(d), None) == _lib.PA_ERR_INVALID_ARG
-    assert lib.pa_reshape_and_cache(p, p, p, 0, p, p, ctypes.byref(d), None) == _lib.PA_OK
-    assert lib.pa_copy_blocks(p, p, ctypes.byref(d), p, 0, None) == _lib.PA_OK
-    assert lib.pa_copy_blocks(None, p, ctypes.byref(d), p, 3, None) == _lib.PA_ERR_INVALID_ARG
+    assert lib.pa_reshape_and_cache(None, None, None, 4, None, None, ctypes.byref(d), None) == _lib.PA_ERR_INVALID_ARG
+    assert lib.pa_reshape_and_cache(None, None, None, -1, None, None, ctypes.byref(d), None) == _lib.PA_ERR_INVALID_ARG
+    assert lib.pa_reshape_and_cache(None, None, None, 0, None, None, ctypes.byref(d), None) == _lib.PA_OK
+    assert lib.pa_copy_blocks(None, None, ctypes.byref(d), None, 0, None) == _lib.PA_OK
+    assert lib.pa_copy_blocks(None, None, ctypes.byref(d), None, 3, None) == _lib.PA_ERR_INVALID_ARG
     bad = _desc(dt=7)
-    assert lib.pa_copy_blocks(p, p, ctypes.byref(bad), p, 1, None) == _lib.PA_ERR_INVALID_ARG
+    assert lib.pa_copy_blocks(None, None, ctypes.byref(bad), None, 1, None) == _lib.PA_ERR_INVALID_ARG
     big = _desc(nb=1 << 28, bs=16)
-    assert lib.pa_copy_blocks(p, p, ctypes.byref(big), p, 1, None) == _lib.PA_ERR_INVALID_ARG
+    assert lib.pa_copy_blocks(None, None, ctypes.byref(big), None, 1, None) == _lib.PA_ERR_INVALID_ARG
     o = _lib.DecodeOpts(4, _lib.PA_KERNEL_AUTO, None, None)
-    # H not a multiple of Hk, group above 8, unsupported head_dim
-    assert lib.pa_decode(p, p, p, p, ctypes.byref(d), p, 4, p, 2, 12, 1.0, p, 1 << 20, ctypes.byref(o),
+    # H not a multiple of Hk, group above 8, unsupported head_dim: the plan is made first
+    args = (None, None, None, None)
+    assert lib.pa_decode(*args, ctypes.byref(d), None, 4, None, 2, 12, 1.0, None, 1 << 20, ctypes.byref(o),
                          None) == _lib.PA_ERR_INVALID_ARG
-    assert lib.pa_decode(p, p, p, p, ctypes.byref(d), p, 4, p, 2, 128, 1.0, p, 1 << 20, ctypes.byref(o),
+    assert lib.pa_decode(*args, ctypes.byref(d), None, 4, None, 2, 128, 1.0, None, 1 << 20, ctypes.byref(o),
                          None) == _lib.PA_ERR_UNSUPPORTED
     d96 = _desc(d=96)
-    assert lib.pa_decode(p, p, p, p, ctypes.byref(d96), p, 4, p, 2, 32, 1.0, p, 1 << 20, ctypes.byref(o),
+    assert lib.pa_decode(*args, ctypes.byref(d96), None, 4, None, 2, 32, 1.0, None, 1 << 20, ctypes.byref(o),
                          None) == _lib.PA_ERR_UNSUPPORTED
     # the tensor-core kernel needs bf16 and a block size multiple of 16
     d32 = _desc(dt=_lib.PA_F32, d=64)
     om = _lib.DecodeOpts(4, _lib.PA_KERNEL_MMA, None, None)
-    assert lib.pa_decode(p, p, p, p, ctypes.byref(d32), p, 4, p, 2, 32, 1.0, p, 1 << 20, ctypes.byref(om),
+    assert lib.pa_decode(*args, ctypes.byref(d32), None, 4, None, 2, 32, 1.0, None, 1 << 20, ctypes.byref(om),
                          None) == _lib.PA_ERR_UNSUPPORTED
-    # workspace too small, null workspace, misaligned workspace
+    # null workspace; zero sequences is a no-op
+    assert lib.pa_decode(*args, ctypes.byref(d), None, 4, None, 2, 32, 1.0, None, 1 << 20, ctypes.byref(o),
+                         None) == _lib.PA_ERR_INVALID_ARG
+    assert lib.pa_decode(*args, ctypes.byref(d), None, 4, None, 0, 32, 1.0, None, 1 << 20, ctypes.byref(o),
+                         None) == _lib.PA_OK
+    if _gpu_present():
+        return  # the checks below need non-null device pointers
+    p = ctypes.c_void_p(0x1000)
+    # workspace too small, misaligned workspace
     assert lib.pa_decode(p, p, p, p, ctypes.byref(d), p, 4, p, 2, 32, 1.0, p, 16, ctypes.byref(o),
                          None) == _lib.PA_ERR_WORKSPACE
-    assert lib.pa_decode(p, p, p, p, ctypes.byref(d), p, 4, p, 2, 32, 1.0, None, 1 << 20, ctypes.byref(o),
-                         None) == _lib.PA_ERR_INVALID_ARG
     assert lib.pa_decode(p, p, p, p, ctypes.byref(d), p, 4, p, 2, 32, 1.0, ctypes.c_void_p(0x1010),
                          1 << 20, ctypes.byref(o), None) == _lib.PA_ERR_INVALID_ARG
-    # zero sequences is a no-op
-    assert lib.pa_decode(p, p, p, p, ctypes.byref(d), p, 4, p, 0, 32, 1.0, p, 1 << 20, ctypes.byref(o),
-                         None) == _lib.PA_OK
 
 
 def test_workspace_size_follows_the_split_count(lib):
@@ -217,3 +233,61 @@ def test_a_run_of_blocks_spans_at_most_its_share_plus_two_ctas():
         assert pieces <= nb * Ce / W + 2
         if nb * Ce < 6 * W:
             assert pieces < 8
+
+
+class _FakeCudaTensor:
+    """Just enough of a CUDA tensor for the binding's checks (no GPU needed):
+    it reports a device index and never gets as far as a C call."""
+
+    def __init__(self, shape, dtype, index):
+        import torch
+        self.shape = torch.Size(shape)
+        self.dtype = dtype
+        self.device = torch.device("cuda", index)
+        self.is_cuda = True
+
+    def dim(self):
+        return len(self.shape)
+
+    def numel(self):
+        n = 1
+        for x in self.shape:
+            n *= x
+        return n
+
+    def reshape(self, *shape):
+        return self
+
+    def element_size(self):
+        return 2
+
+    def is_contiguous(self):
+        return True
+
+    def data_ptr(self):
+        raise AssertionError("a tensor on another device reached the C call")
+
+
+def test_tensors_on_another_device_are_refused_before_the_call(monkeypatch):
+    """The library works on the current device (its stream, its error word,
+    its scratch); a tensor on another GPU is refused with ValueError."""
+    import torch
+    monkeypatch.setattr(pa, "_current_device", lambda: 0)
+    bf = torch.bfloat16
+    kc = _FakeCudaTensor((8, 16, 8, 128), bf, 1)
+    vc = _FakeCudaTensor((8, 16, 8, 128), bf, 1)
+    pairs = _FakeCudaTensor((2, 2), torch.int32, 1)
+    with pytest.raises(ValueError, match="current device"):
+        pa.pa_copy_blocks(kc, vc, pairs)
+    k = _FakeCudaTensor((4, 8, 128), bf, 1)
+    slots = _FakeCudaTensor((4,), torch.int32, 1)
+    with pytest.raises(ValueError, match="current device"):
+        pa.pa_reshape_and_cache(k, k, slots, kc, vc)
+    q = _FakeCudaTensor((2, 32, 128), bf, 1)
+    tables = _FakeCudaTensor((2, 4), torch.int32, 1)
+    lens = _FakeCudaTensor((2,), torch.int32, 1)
+    ws = _FakeCudaTensor((1 << 20,), torch.uint8, 1)
+    with pytest.raises(ValueError, match="current device"):
+        pa.pa_decode(q, kc, vc, tables, lens, 0.088, out=q, workspace=ws)
+    with pytest.raises(ValueError, match="current device"):
+        pa.pa_decode_no_alloc(q, kc, vc, tables, lens, 0.088, q)

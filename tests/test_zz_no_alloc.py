@@ -4,11 +4,12 @@ Such callers (a server whose KV pool took nearly all device memory at
 startup, a plugin whose host framework owns the allocator, a loop that cannot
 pay for cudaMalloc's implicit synchronisation) cannot pass pa_decode a
 workspace.  The no-allocation entry point uses a fixed scratch array inside the
-library instead.  This file checks, through the C ABI, that two calls in a row
-give the same output as pa_decode with a caller-provided workspace (within the
-suite's bf16 tolerance), and that a shape too large for the fixed array is
-refused before anything is launched.  It is named so that pytest collects it
-last.
+library instead.  This file checks, through the C ABI, that calls in a row
+give the same bits as pa_decode with a caller-provided workspace and the same
+split (also right after a larger call with more splits has left its counters
+and partials in the shared array), and that a shape too large for the fixed
+array is refused before anything is launched.  It is named so that pytest
+collects it last.
 """
 import ctypes
 
@@ -22,18 +23,36 @@ from _pipeline import TOL, gpu_step, host_values
 pytestmark = pytest.mark.gpu
 
 
+def _no_alloc(g, wl, num_splits=0):
+    out = torch.full_like(g["out"], float("nan"))
+    pa.pa_decode_no_alloc(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale, out,
+                          num_splits=num_splits)
+    assert pa.pa_get_device_error(raise_on_error=False) == 0
+    return out
+
+
 @pytest.mark.parametrize("cfg,kw", [("cfg2", {"small": True}), ("cfg4", {"small": True}), ("cfg0", {})])
-def test_no_alloc_matches_pa_decode_on_two_calls_in_a_row(cfg, kw):
+def test_no_alloc_gives_the_bits_of_pa_decode_on_two_calls_in_a_row(cfg, kw):
     wl = inputs.workload(cfg, **kw)
     dev, _ = host_values(wl, "cpu")
-    g = gpu_step(wl, dev)  # pa_decode with a workspace from the caller
-    ref = g["out"].float()
+    g = gpu_step(wl, dev)  # pa_decode with a workspace from the caller, default split
     for _ in range(2):
-        out = torch.full_like(g["out"], float("nan"))
-        pa.pa_decode_no_alloc(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale, out)
-        assert pa.pa_get_device_error(raise_on_error=False) == 0
-        assert torch.isfinite(out.float()).all()
-        assert (out.float() - ref).abs().max().item() <= TOL[wl.dtype]
+        assert torch.equal(_no_alloc(g, wl), g["out"])
+
+
+def test_no_alloc_after_a_larger_call_with_more_splits():
+    """A 256-sequence batch on 608 CTAs leaves more arrival counters and
+    partials in the shared array than the smaller call after it uses; each
+    call must still match pa_decode bit for bit."""
+    big_wl = inputs.workload("cfg2")
+    big_dev, _ = host_values(big_wl, "cuda")
+    big = gpu_step(big_wl, big_dev, num_splits=608)
+    small_wl = inputs.workload("cfg4", small=True)
+    small_dev, _ = host_values(small_wl, "cpu")
+    small = gpu_step(small_wl, small_dev)
+    for _ in range(2):
+        assert torch.equal(_no_alloc(big, big_wl, num_splits=608), big["out"])
+        assert torch.equal(_no_alloc(small, small_wl), small["out"])
 
 
 def test_no_alloc_refuses_a_shape_beyond_its_scratch():
@@ -41,8 +60,10 @@ def test_no_alloc_refuses_a_shape_beyond_its_scratch():
     opts = _lib.DecodeOpts(0, _lib.PA_KERNEL_AUTO, None, None)
     need = _lib.load().pa_decode_workspace_bytes(ctypes.byref(desc), 8192, 64, ctypes.byref(opts))
     assert need > _lib.PA_NO_ALLOC_SCRATCH_BYTES
-    p = ctypes.c_void_p(0x1000)  # never dereferenced: the size check comes first
-    st = _lib.load().pa_decode_no_alloc(p, p, p, p, ctypes.byref(desc), p, 4, p, 8192, 64, 0.088,
+    # Null device pointers: the size check comes first, and if it ever did
+    # not, pa_decode's null-pointer check would refuse the call before any
+    # launch.
+    st = _lib.load().pa_decode_no_alloc(None, None, None, None, ctypes.byref(desc), None, 4, None, 8192, 64, 0.088,
                                         ctypes.byref(opts), None)
     assert st == _lib.PA_ERR_WORKSPACE
 
