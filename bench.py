@@ -36,7 +36,7 @@ METRIC = "paged decode attention: KV bytes read GB/s (% of GB300 HBM peak), toke
 EXTRA = [("cfg2", {}), ("cfg4", {"block_size": 32}), ("cfg1", {}), ("cfg3", {"prompt_len": 2008}), ("cfg4", {"block_size": 16}),
          ("cfg4", {"block_size": 16, "layout": "split"}), ("cfg2", {"layout": "split"}), ("prefix", {}),
          ("cfg3", {"prompt_len": 2008, "shared": True}), ("prefix", {"shared": True}),
-         ("cfg4", {"block_size": 16, "placement": "contiguous"})]
+         ("cfg4", {"block_size": 16, "placement": "contiguous"}), ("cfg2-f32", {}), ("d256", {})]
 FLUSH_BYTES = 512 << 20  # > 129 MB L2: written between timed steps
 FALLBACK_HBM_GBS = 6800.0
 
@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--workload", default="cfg4-b16",
                     help="headline workload: cfg4-b16 (default), cfg4-b32, cfg2, cfg1, cfg3-p2000, cfg3-p2008, "
-                         "cfg4-b16-split, cfg2-split, prefix, cfg0 (tiny fp32)")
+                         "cfg4-b16-split, cfg2-split, prefix, cfg0 (tiny fp32), cfg2-f32, d256 (head_dim 256)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-write-copy", action="store_true",
@@ -70,20 +70,41 @@ WORKLOADS = {"cfg4-b16": ("cfg4", {"block_size": 16}), "cfg4-b32": ("cfg4", {"bl
              "cfg2-split": ("cfg2", {"layout": "split"}), "prefix": ("prefix", {}),
              "cfg4-b16-contiguous": ("cfg4", {"block_size": 16, "placement": "contiguous"}),
              "cfg3-p2008-shared": ("cfg3", {"prompt_len": 2008, "shared": True}),
-             "prefix-shared": ("prefix", {"shared": True}), "cfg0": ("cfg0", {})}
+             "prefix-shared": ("prefix", {"shared": True}), "cfg0": ("cfg0", {}),
+             "cfg2-f32": ("cfg2-f32", {}), "d256": ("d256", {})}
+# The workloads the 70%-of-HBM goal names (mixed-length GQA batch, long
+# contexts at both block sizes): summarised under "targets" at the end of the
+# line, with every output checked against the oracle when the CPU leg runs.
+TARGETS = ("cfg2", "cfg4-b16", "cfg4-b32")
 
 
 # ---------------------------------------------------------------- helpers
-def make_workload(cfg, kw):
+def make_workload(cfg, kw, seed_offset=0):
     """(workload, cache layout, shared-prefix plan) of a bench name's (cfg,
-    options): "layout" and "shared" choose how the CUDA path runs; the other
-    options go to inputs.workload."""
+    options): "layout" and "shared" choose how the CUDA path runs (and mark
+    the workload's name); the other options go to inputs.workload."""
     from paged_kv_cache_150_gb300 import inputs
 
     kw = dict(kw)
     layout = kw.pop("layout", "row")
     shared = kw.pop("shared", False)
-    return inputs.workload(cfg, **kw), layout, shared
+    wl = inputs.workload(cfg, **kw)
+    wl.seed += seed_offset
+    if layout == "split":
+        wl.name += "-split"
+    if shared:
+        wl.name += "-shared"
+    return wl, layout, shared
+
+
+def bench_config(wl, l2, world):
+    """The line's "config": the same object for both arms."""
+    kv = wl.kv_bytes_read()
+    return {"workload": describe(wl), "kv_bytes_per_step": kv, "num_seqs": wl.num_seqs,
+            "max_seq_len": int(wl.seq_lens.max()), "block_size": wl.block_size,
+            "l2": ("inputs larger than L2: %.2f GB of KV per step vs 129 MB L2, no flush" % (kv / 1e9)
+                   if l2 == "none" else "512 MiB buffer written between timed steps"),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
 def dist_setup(args):
@@ -132,61 +153,185 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """SM clock, power and clock-event (throttle) reasons of this process's GPU,
+    sampled DURING the timed region.  Read-only queries: nothing is set.
+
+    Primary source: NVML through ctypes (the library nvidia-smi reads), polled
+    from a thread every 5 ms, so even a timed region of a few milliseconds gets
+    samples.  Fallback: an nvidia-smi loop started before the region (and
+    allowed to print its first row first, since it needs longer than a short
+    region to start).  The GPU is found by UUID, else by its index in
+    CUDA_VISIBLE_DEVICES, else by the CUDA index; the record says which, and
+    why when nothing could be read."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+    PERIOD_S = 0.005
 
     def __init__(self, device_index):
-        self.proc = None
-        # raw samples: PA_CLOCKS_DIR if set (to keep them), else the temp directory
-        self.path = os.path.join(os.environ.get("PA_CLOCKS_DIR") or tempfile.gettempdir(),
-                                 "pa_clocks_r%d.csv" % os.getpid())
+        self.notes = []
+        self.selectors = []
         try:
             import torch
 
-            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
-            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
-        except Exception:
-            sel = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or "0"
-        self.sel = sel
+            u = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.selectors.append(u if u.startswith("GPU-") else "GPU-" + u)
+        except Exception as e:  # noqa: BLE001
+            self.notes.append("no uuid: %s" % str(e)[:60])
+        vis = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+        if device_index < len(vis):
+            self.selectors.append(vis[device_index])
+        self.selectors.append(str(device_index))
+        self.samples = []  # (sm_mhz, sm_max_mhz, power_w, reasons)
+        self.source, self.selector = None, None
+        self._nvml = self._open_nvml()
 
-    def start(self):
-        try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", self.sel, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
-        except Exception:
-            self.proc = None
+    # ---------------------------------------------------------------- NVML
+    def _open_nvml(self):
+        import ctypes
 
-    def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        self.proc.terminate()
         try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.fh.close()
-        sm, smax, reasons = [], [], set()
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit_v2 failed")
+        except Exception as e:  # noqa: BLE001
+            self.notes.append("nvml unavailable: %s" % str(e)[:60])
+            return None
+        h = ctypes.c_void_p()
+        for sel in self.selectors:
+            if sel.startswith("GPU-") or sel.startswith("MIG-"):
+                rc = lib.nvmlDeviceGetHandleByUUID(sel.encode(), ctypes.byref(h))
+            elif sel.isdigit():
+                rc = lib.nvmlDeviceGetHandleByIndex_v2(int(sel), ctypes.byref(h))
+            else:
+                continue
+            if rc == 0:
+                self.selector = sel
+                break
+            self.notes.append("nvml: no handle for %s (rc %d)" % (sel, rc))
+        else:
+            return None
+        self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self._h = h
+        if self._nvml_sample(lib) is None:
+            self.notes.append("nvml: clock query failed")
+            return None
+        return lib
+
+    def _nvml_sample(self, lib):
+        import ctypes
+
+        sm, smax, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if lib.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(sm)) != 0:  # NVML_CLOCK_SM
+            return None
+        lib.nvmlDeviceGetMaxClockInfo(self._h, 1, ctypes.byref(smax))
+        lib.nvmlDeviceGetPowerUsage(self._h, ctypes.byref(mw))
+        self._reasons_fn(self._h, ctypes.byref(rs))
+        return (float(sm.value), float(smax.value), mw.value / 1e3,
+                [n for bit, n in self.REASONS.items() if rs.value & bit])
+
+    def _poll(self):
+        while not self._stop.is_set():
+            s = self._nvml_sample(self._nvml)
+            if s is not None:
+                self.samples.append(s)
+            self._stop.wait(self.PERIOD_S)
+
+    # ----------------------------------------------------------- nvidia-smi
+    def _start_smi(self):
+        self.path = os.path.join(os.environ.get("PA_CLOCKS_DIR") or tempfile.gettempdir(),
+                                 "pa_clocks_r%d.csv" % os.getpid())
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        for sel in self.selectors:
+            try:
+                probe = subprocess.run(["nvidia-smi", "-i", sel, "--query-gpu=clocks.sm", "--format=csv,noheader"],
+                                       capture_output=True, text=True, timeout=20)
+            except Exception as e:  # noqa: BLE001
+                self.notes.append("nvidia-smi: %s" % str(e)[:60])
+                return
+            if probe.returncode == 0 and probe.stdout.strip():
+                self.selector = sel
+                break
+            self.notes.append("nvidia-smi -i %s: %s" % (sel, (probe.stderr or probe.stdout).strip()[:60]))
+        else:
+            return
+        self.fh = open(self.path, "w")
+        self.proc = subprocess.Popen(["nvidia-smi", "-i", self.selector, "--query-gpu=" + self.FIELDS,
+                                      "--format=csv,noheader,nounits", "-lms", "100"],
+                                     stdout=self.fh, stderr=subprocess.DEVNULL)
+        t0 = time.time()
+        while time.time() - t0 < 10 and self._smi_rows() == 0:  # its first row, before the region opens
+            time.sleep(0.05)
+
+    def _smi_rows(self):
+        try:
+            return sum(1 for line in open(self.path) if line.count(",") >= 7)
+        except OSError:
+            return 0
+
+    def _read_smi(self):
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        out = []
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
+                sm, smax = float(parts[0]), float(parts[1])
+                pw = float(parts[2])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+            out.append((sm, smax, pw, [n for n, v in zip(names, parts[4:8]) if v.lower().startswith("active")]))
+        return out
+
+    # ------------------------------------------------------------------ API
+    def start(self):
+        import threading
+
+        self.samples, self.proc = [], None
+        if self._nvml is not None:
+            self.source = "nvml (every %d ms)" % int(self.PERIOD_S * 1e3)
+            self._stop = threading.Event()
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
+            return
+        try:
+            self._start_smi()
+            if self.proc is not None:
+                self.source = "nvidia-smi (every 100 ms)"
+        except Exception as e:  # noqa: BLE001
+            self.notes.append("nvidia-smi: %s" % str(e)[:60])
+
+    def stop(self):
+        if self.source and self.source.startswith("nvml"):
+            self._stop.set()
+            self._thread.join(timeout=5)
+        elif self.proc is not None:
+            n0 = self._smi_rows()
+            t0 = time.time()
+            while time.time() - t0 < 2 and self._smi_rows() <= n0:  # one row after the region closes
+                time.sleep(0.02)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:  # noqa: BLE001
+                self.proc.kill()
+            self.fh.close()
+            self.samples = self._read_smi()
+        s = self.samples
+        rec = {"sm_mhz": statistics.median(x[0] for x in s) if s else None,
+               "sm_max_mhz": max(x[1] for x in s) if s else None,
+               "reasons": sorted({r for x in s for r in x[3]}), "samples": len(s),
+               "power_w_max": round(max(x[2] for x in s), 1) if s else None,
+               "source": self.source, "gpu": self.selector}
+        if not s:
+            rec["why_none"] = "; ".join(self.notes) or "no sample returned"
+        return rec
 
 
 def source_sha():
@@ -223,12 +368,7 @@ class Step:
         from paged_kv_cache_150_gb300 import inputs
 
         self.pa = pa
-        wl, layout, shared = make_workload(cfg, kw)
-        wl.seed += seed_offset
-        if layout == "split":
-            wl.name += "-split"
-        if shared:
-            wl.name += "-shared"
+        wl, layout, shared = make_workload(cfg, kw, seed_offset)
         self.shared = shared
         self.wl = wl
         self.layout = layout
@@ -565,12 +705,7 @@ def run_ours(args, rank, world):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": step.wl.dtype, "data": "synthetic",
-        "config": {"workload": describe(step.wl),
-                   "kv_bytes_per_step": step.kv_bytes, "num_seqs": step.wl.num_seqs,
-                   "max_seq_len": int(step.wl.seq_lens.max()), "block_size": step.wl.block_size,
-                   "l2": ("inputs larger than L2: %.2f GB of KV per step vs 129 MB L2, no flush" % (step.kv_bytes / 1e9)
-                          if args.l2 == "none" else "512 MiB buffer written between timed steps"),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": bench_config(step.wl, args.l2, world),
         "tokens_per_s": round(tokens_per_s, 1),
         "hbm_frac": round(value / world / peak, 4),
         "roofline": {"bound": "hbm",
@@ -585,6 +720,21 @@ def run_ours(args, rank, world):
         "block_manager_ms": round(step.bm_ms, 3),
         "write_copy": write_copy,
     }
+    targets = {"goal": "pa_decode >= 0.70 of HBM peak; outputs within 2e-2 of the fp64 oracle",
+               "peak_gbs": peak}
+
+    def target(name, st, step_ms, kernel_ms, parity):
+        gbs = st.kernel_bytes / (kernel_ms / 1e3) / 1e9
+        targets[name] = {"hbm_frac": round(st.kv_bytes / (step_ms / 1e3) / 1e9 / peak, 4),
+                         "kernel_gbs": round(gbs, 1), "kernel_frac": round(gbs / peak, 4)}
+        if parity is not None:
+            targets[name].update(parity)
+
+    def full_parity(st, threads):
+        """Every output of the workload against the oracle (CPU leg)."""
+        ref, pairs, dt, nbytes, _ = oracle_baseline(st, 10 ** 9, threads)
+        return {"max_abs_err": float("%.3g" % parity_check(st, ref, pairs)), "outputs_checked": len(pairs)}
+
     if do_cpu:
         import oracle
 
@@ -595,7 +745,13 @@ def run_ours(args, rank, world):
                                 "sample": "%d of %d (sequence, KV head) groups of the workload, all query heads, "
                                           "fp64, %.1f s wall" % (ngroups, step.wl.num_seqs * step.wl.num_kv_heads, dt)}
         line["parity"] = {"max_abs_err": parity_check(step, ref, pairs), "pairs_checked": len(pairs),
-                          "tolerance": 2e-2}
+                          "tolerance": 2e-2 if step.wl.dtype == "bf16" else 1e-5}
+    if args.workload in TARGETS:
+        par = None
+        if do_cpu:
+            par = ({"max_abs_err": float("%.3g" % line["parity"]["max_abs_err"]), "outputs_checked": len(pairs)}
+                   if len(pairs) == step.wl.num_seqs * step.wl.num_q_heads else full_parity(step, threads))
+        target(args.workload, step, ms_per_step, kern_avg_ms, par)
     del step
     torch.cuda.empty_cache()
     if do_cpu:
@@ -607,9 +763,14 @@ def run_ours(args, rank, world):
                 continue
             torch.cuda.empty_cache()
             st = Step(cfg, kw, seed_offset=1000 * rank)
+            tname = next((n for n in TARGETS if WORKLOADS[n] == (cfg, kw)), None)
+            if tname and do_cpu:
+                st.keep_initial_host_copy()
             sm, km, _ = time_steps(st, args.extra_steps, args.warmup, world, flush, kernel_steps=args.extra_steps)
             mean_ms = reduce_max(statistics.mean(sm), world)
             kms = statistics.mean(km)
+            if tname:
+                target(tname, st, mean_ms, kms, full_parity(st, threads) if do_cpu else None)
             extra[st.wl.name] = {"kv_gbs": round(st.kv_bytes / (mean_ms / 1e3) / 1e9, 2),
                                  "ms_per_step": round(mean_ms, 5),
                                  "tokens_per_s": round(st.tokens / (mean_ms / 1e3), 1),
@@ -631,6 +792,7 @@ def run_ours(args, rank, world):
         line["workloads"] = extra
     if rank == 0:
         line["allocation_simulator"] = allocation_simulator()
+        line["targets"] = targets  # last: the end of the line is what a log tail keeps
         print(json.dumps(line), flush=True)
 
 
@@ -643,7 +805,7 @@ def run_reference(args, rank, world):
     import oracle
     from paged_kv_cache_150_gb300 import inputs
 
-    wl, _, _ = make_workload(*WORKLOADS[args.workload])  # the oracle reads the row layout
+    wl, _, _ = make_workload(*WORKLOADS[args.workload])  # the oracle reads the row layout of the same values
     vals = inputs.make_values(wl, device="cpu")
     host = {k: inputs.to_numpy_elems(v).copy() for k, v in vals.items()}
     r = oracle.run_script(wl.num_blocks, wl.block_size, wl.free_order, wl.script)
@@ -680,8 +842,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": describe(wl), "kv_bytes_per_step": wl.kv_bytes_read(),
-                   "per_step_sample": "%d (sequence, KV head) groups, all query heads" % per_step},
+        "config": bench_config(wl, args.l2, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
                          "sample": "%d groups (%d sequence-head pairs) per step of %d groups; %d host threads"
                                    % (per_step, per_step * G, len(groups_all), threads)},

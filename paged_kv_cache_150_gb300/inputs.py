@@ -394,6 +394,22 @@ def workload(cfg: str, small: bool = False, block_size: Optional[int] = None,
         if small:
             return prefix_workload("prefix-small", 2, 3, 200, (1, 40), 32, 8, 128, 16, "bf16", 2600, spare_blocks=8)
         return prefix_workload("prefix", 8, 10, 2000, (16, 512), 32, 8, 128, 16, "bf16", 1600)
+    if cfg in ("cfg2-f32", "d256"):
+        # The mixed-length batch where only the CUDA-core kernel applies: in
+        # fp32 (cfg2's shape), and in bf16 with head_dim 256 (16 query / 8 KV
+        # heads, lengths lognormal around 1024).
+        f32 = cfg == "cfg2-f32"
+        seed = (2700 if small else 1700) + (0 if f32 else 1)
+        rng = np.random.default_rng(seed)
+        n, median = (20, 160.0) if small else ((256, 512.0) if f32 else (128, 1024.0))
+        lens = np.clip(np.rint(np.exp(rng.normal(math.log(median), 1.0, size=n))), 16, 8192).astype(np.int32)
+        if small:
+            lens = np.concatenate([[1, 15, 16, 17, 33], lens]).astype(np.int32)
+        H, D = (32, 128) if f32 else (16, 256)
+        return decode_workload(cfg + ("-small" if small else ""), lens, H, 8, D, 16, "f32" if f32 else "bf16", seed,
+                               pool_factor=1.1, rng=rng,
+                               note="mixed lengths, lognormal(median %d, sigma 1), %s" %
+                                    (int(median), "fp32" if f32 else "head_dim 256"))
     k = int(cfg[-1])
     seed = (2500 if small else 1500) + k
     rng = np.random.default_rng(seed)

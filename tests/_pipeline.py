@@ -75,15 +75,3 @@ def max_abs_err(out_dev, ref, pairs=None):
         return float(np.abs(out - ref).max())
     idx = np.asarray(pairs)
     return float(np.abs(out[idx[:, 0], idx[:, 1]] - ref[idx[:, 0], idx[:, 1]]).max())
-
-
-def sample_pairs(wl, n, seed=0):
-    """Random (seq, head) pairs plus every head of the shortest and longest sequence."""
-    rng = np.random.default_rng(seed)
-    H = wl.num_q_heads
-    seqs = rng.integers(0, wl.num_seqs, size=n)
-    heads = rng.integers(0, H, size=n)
-    pairs = set(zip(seqs.tolist(), heads.tolist()))
-    for s in (int(np.argmin(wl.seq_lens)), int(np.argmax(wl.seq_lens))):
-        pairs.update((s, h) for h in range(H))
-    return sorted(pairs)

@@ -41,3 +41,25 @@ def test_reference_arm_other_ranks_exit_without_work():
     res = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert res.returncode == 0, res.stderr[-2000:]
     assert res.stdout.strip() == ""
+
+
+def test_reference_arm_config_is_the_gpu_arms_config():
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "cfg0",
+           "--steps", "2", "--warmup", "1"]
+    res = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-2000:]
+    d = json.loads(res.stdout.strip().splitlines()[-1])
+    wl, _, _ = bench.make_workload(*bench.WORKLOADS["cfg0"])  # rank 0 of the GPU arm: no seed offset
+    assert d["config"] == json.loads(json.dumps(bench.bench_config(wl, "none", 1)))
+
+
+def test_clock_sampler_says_why_it_has_no_samples():
+    """Without a GPU (here) the sampler neither raises nor invents a clock:
+    its record has no samples and a reason."""
+    s = bench.ClockSampler(0)
+    s.start()
+    rec = s.stop()
+    if rec["samples"] == 0:
+        assert rec["sm_mhz"] is None and rec["why_none"]
+    else:  # a machine with a readable GPU
+        assert rec["sm_mhz"] > 0 and rec["source"]

@@ -1,9 +1,9 @@
 """GPU parity of paged decode attention against the fp64 oracle.
 
 Tolerances (max-abs against the fp64 result): 1e-5 for fp32 inputs, 2e-2 for
-bf16 inputs with fp32 accumulation.  Small cases compare every output; full
-size cases run in the benchmark's launch configuration (automatic kernel
-choice, one wave of CTAs) and compare a sample of (sequence, head) pairs."""
+bf16 inputs with fp32 accumulation.  Every case compares every output, the
+full-size ones in the benchmark's launch configuration (automatic kernel
+choice, one wave of CTAs)."""
 import math
 
 import numpy as np
@@ -13,14 +13,15 @@ import torch
 import oracle
 import paged_kv_cache_150_gb300 as pa
 from paged_kv_cache_150_gb300 import inputs
-from _pipeline import TOL, gpu_step, host_values, max_abs_err, oracle_decode, oracle_step, sample_pairs
+from _pipeline import TOL, gpu_step, host_values, max_abs_err, oracle_decode, oracle_step
 
 pytestmark = pytest.mark.gpu
 
 SMALL = [("cfg0", {}), ("cfg1", {"small": True}), ("cfg2", {"small": True}),
          ("cfg3", {"small": True}), ("cfg3", {"small": True, "prompt_len": 200}),
          ("cfg4", {"small": True}), ("cfg4", {"small": True, "block_size": 32}),
-         ("cfg4", {"small": True, "placement": "contiguous"})]
+         ("cfg4", {"small": True, "placement": "contiguous"}), ("cfg2-f32", {"small": True}),
+         ("d256", {"small": True})]
 
 
 @pytest.mark.parametrize("cfg,kw", SMALL)
@@ -35,19 +36,19 @@ def test_decode_small(cfg, kw, kernel, splits):
     assert err <= TOL[wl.dtype], err
 
 
-FULL = [("cfg1", {}, 64), ("cfg2", {}, 96), ("cfg3", {}, 48), ("cfg3", {"prompt_len": 2008}, 48),
-        ("cfg4", {}, 24), ("cfg4", {"block_size": 32}, 24), ("cfg4", {"placement": "contiguous"}, 24)]
+FULL = [("cfg1", {}), ("cfg2", {}), ("cfg3", {}), ("cfg3", {"prompt_len": 2008}),
+        ("cfg4", {}), ("cfg4", {"block_size": 32}), ("cfg4", {"placement": "contiguous"}), ("cfg2-f32", {}),
+        ("d256", {})]
 
 
-@pytest.mark.parametrize("cfg,kw,nsample", FULL)
-def test_decode_full_size_sampled(cfg, kw, nsample):
+@pytest.mark.parametrize("cfg,kw", FULL)
+def test_decode_full_size_every_output(cfg, kw):
     wl = inputs.workload(cfg, **kw)
     dev, host = host_values(wl, "cuda")
     r = oracle_step(wl, host)
     g = gpu_step(wl, dev)
-    pairs = sample_pairs(wl, nsample)
-    ref = oracle_decode(wl, host, r, pairs=pairs)
-    err = max_abs_err(g["out"], ref, pairs)
+    ref = oracle_decode(wl, host, r)
+    err = max_abs_err(g["out"], ref)
     assert err <= TOL[wl.dtype], err
     assert torch.isfinite(g["out"].float()).all()
 
@@ -194,8 +195,7 @@ def test_many_sequences_prefix_sums_in_global_memory(kernel, num_seqs):
     dev, host = host_values(wl, "cuda")
     r = oracle_step(wl, host)
     g = gpu_step(wl, dev, kernel=kernel)
-    pairs = sample_pairs(wl, 400)
-    assert max_abs_err(g["out"], oracle_decode(wl, host, r, pairs=pairs), pairs) <= TOL["bf16"]
+    assert max_abs_err(g["out"], oracle_decode(wl, host, r)) <= TOL["bf16"]
     assert (g["out"][::97] == 0).all()
 
 
@@ -211,9 +211,7 @@ def test_one_long_sequence_merged_from_every_cta(kernel):
     dev, host = host_values(wl, "cuda")
     r = oracle_step(wl, host)
     g = gpu_step(wl, dev, kernel=kernel)
-    pairs = [(0, h) for h in range(0, 64, 7)] + [(0, 63), (1, 3), (2, 63), (3, 10), (3, 32)]
-    ref = oracle_decode(wl, host, r, pairs=pairs)
-    assert max_abs_err(g["out"], ref, pairs) <= TOL["bf16"]
+    assert max_abs_err(g["out"], oracle_decode(wl, host, r)) <= TOL["bf16"]
     assert torch.isfinite(g["out"].float()).all()
 
 
@@ -265,9 +263,7 @@ def test_long_context_merge_kernel_whatever_the_host_hint(kernel, hint):
     hints = {"exact": "exact", "zeros": np.zeros(len(lens), np.int32),
              "all-long": np.full(len(lens), wl.max_blocks_per_seq * wl.block_size, np.int32)}
     g = gpu_step(wl, dev, kernel=kernel, host_lens=hints[hint])
-    pairs = [(0, h) for h in range(0, 64, 5)] + [(1, 0), (2, 63), (3, 31), (4, 7), (5, 0)]
-    ref = oracle_decode(wl, host, r, pairs=pairs[:-1])
-    assert max_abs_err(g["out"], ref, pairs[:-1]) <= TOL["bf16"]
+    assert max_abs_err(g["out"], oracle_decode(wl, host, r)) <= TOL["bf16"]
     assert (g["out"][5] == 0).all()
     assert torch.isfinite(g["out"].float()).all()
 
@@ -279,8 +275,7 @@ def test_long_context_merge_full_size_with_host_lengths():
     dev, host = host_values(wl, "cuda")
     r = oracle_step(wl, host)
     g = gpu_step(wl, dev, host_lens="exact")
-    pairs = sample_pairs(wl, 24)
-    assert max_abs_err(g["out"], oracle_decode(wl, host, r, pairs=pairs), pairs) <= TOL["bf16"]
+    assert max_abs_err(g["out"], oracle_decode(wl, host, r)) <= TOL["bf16"]
 
 
 def test_host_hint_leaves_short_sequences_bit_identical():
@@ -328,7 +323,32 @@ def test_long_merge_among_many_short_sequences():
     dev, host = host_values(wl, "cuda")
     r = oracle_step(wl, host)
     g = gpu_step(wl, dev, host_lens="exact")
-    pairs = sample_pairs(wl, 200) + [(250, h) for h in range(32)]
-    ref = oracle_decode(wl, host, r, pairs=pairs)
-    assert max_abs_err(g["out"], ref, pairs) <= TOL["bf16"]
+    assert max_abs_err(g["out"], oracle_decode(wl, host, r)) <= TOL["bf16"]
     assert (g["out"][::41] == 0).all()
+
+
+@pytest.mark.parametrize("cfg,kw,kernel,layout", [
+    ("cfg0", {}, "auto", "row"), ("cfg1", {"small": True}, "auto", "row"), ("cfg2", {"small": True}, "auto", "row"),
+    ("cfg2", {"small": True}, "simt", "row"), ("cfg4", {"small": True, "block_size": 32}, "auto", "row"),
+    ("cfg2", {"small": True}, "auto", "split"), ("cfg2", {}, "auto", "row"), ("cfg4", {}, "auto", "row")])
+def test_relabelled_physical_blocks_give_the_same_bits(cfg, kw, kernel, layout):
+    """A block table may point at any physical blocks ("10 PagedAttention"
+    (PidokuInfra), section 4 PhysicalIndex; "PagedAttention" (tokentrails),
+    step 3: the same attention as over contiguous memory).  Moving every
+    block's contents to a new physical id and rewriting the tables to match
+    must not change a single bit of the output: the work split and the
+    order of the arithmetic depend only on the lengths, never on where the
+    blocks sit in the pool."""
+    wl = inputs.workload(cfg, **kw)
+    dev, _ = host_values(wl, "cuda", layout=layout)
+    g = gpu_step(wl, dev, kernel=kernel)
+    perm = torch.from_numpy(np.random.default_rng(71).permutation(wl.num_blocks)).cuda()  # new id of block b
+    k2, v2 = torch.empty_like(g["k_cache"]), torch.empty_like(g["v_cache"])
+    k2[perm] = g["k_cache"]
+    v2[perm] = g["v_cache"]
+    t = g["tables"]
+    t2 = torch.where(t >= 0, perm[t.clamp(min=0).long()].to(torch.int32), t)
+    assert not torch.equal(t2, t)
+    out2 = pa.pa_decode(g["q"], k2, v2, t2, g["lens"], wl.scale, kernel=kernel)
+    assert pa.pa_get_device_error(raise_on_error=False) == 0
+    assert torch.equal(out2, g["out"])

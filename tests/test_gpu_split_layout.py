@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from paged_kv_cache_150_gb300 import inputs
-from _pipeline import TOL, gpu_step, host_values, max_abs_err, oracle_decode, oracle_step, sample_pairs
+from _pipeline import TOL, gpu_step, host_values, max_abs_err, oracle_decode, oracle_step
 
 pytestmark = pytest.mark.gpu
 
@@ -30,16 +30,15 @@ def test_split_layout_step_matches_oracle(cfg, kw, kernel, splits):
     assert max_abs_err(g["out"], ref) <= TOL[wl.dtype]
 
 
-@pytest.mark.parametrize("cfg,kw,nsample", [("cfg2", {}, 96), ("cfg4", {}, 24), ("cfg3", {"prompt_len": 2008}, 48)])
-def test_split_layout_full_size(cfg, kw, nsample):
+@pytest.mark.parametrize("cfg,kw", [("cfg2", {}), ("cfg4", {}), ("cfg3", {"prompt_len": 2008})])
+def test_split_layout_full_size(cfg, kw):
     wl = inputs.workload(cfg, **kw)
     dev, host = host_values(wl, "cuda", layout="split")
     r = oracle_step(wl, host)
     g = gpu_step(wl, dev)
     assert np.array_equal(inputs.to_numpy_elems(g["k_cache"]), r["k_cache"])
     assert np.array_equal(inputs.to_numpy_elems(g["v_cache"]), r["v_cache"])
-    pairs = sample_pairs(wl, nsample)
-    assert max_abs_err(g["out"], oracle_decode(wl, host, r, pairs=pairs), pairs) <= TOL[wl.dtype]
+    assert max_abs_err(g["out"], oracle_decode(wl, host, r)) <= TOL[wl.dtype]
 
 
 def test_split_and_row_layouts_agree():

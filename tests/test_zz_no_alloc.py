@@ -87,5 +87,4 @@ def test_no_alloc_with_the_host_lengths_matches_pa_decode():
     assert pa.pa_get_device_error(raise_on_error=False) == 0
     assert torch.equal(out, g["out"])
     r = oracle_step(wl, host)
-    pairs = [(0, h) for h in range(0, 64, 9)] + [(3, 5), (4, 60)]
-    assert max_abs_err(out, oracle_decode(wl, host, r, pairs=pairs), pairs) <= TOL["bf16"]
+    assert max_abs_err(out, oracle_decode(wl, host, r)) <= TOL["bf16"]
