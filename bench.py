@@ -658,6 +658,14 @@ def parity_check(step, ref, pairs):
     return float(np.abs(out[idx[:, 0], idx[:, 1]] - ref[idx[:, 0], idx[:, 1]]).max())
 
 
+def uses_mma(wl):
+    """Whether pa_decode's automatic choice is the tensor-core kernel (bf16,
+    head_dim 64 or 128, block size 16 or 32, at most 8 query heads per KV
+    head); else it runs the CUDA-core kernel."""
+    G = wl.num_q_heads // wl.num_kv_heads
+    return wl.dtype == "bf16" and wl.head_dim in (64, 128) and wl.block_size in (16, 32) and G <= 8
+
+
 def workload_name(step):
     return step.wl.name
 
@@ -709,7 +717,7 @@ def run_ours(args, rank, world):
         "tokens_per_s": round(tokens_per_s, 1),
         "hbm_frac": round(value / world / peak, 4),
         "roofline": {"bound": "hbm",
-                     "kernel": "decode attention (%s kernel)" % ("tensor-core" if step.wl.dtype == "bf16" else "CUDA-core"),
+                     "kernel": "decode attention (%s kernel)" % ("tensor-core" if uses_mma(step.wl) else "CUDA-core"),
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": step.kernel_bytes,
