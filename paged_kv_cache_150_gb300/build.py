@@ -15,9 +15,10 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBRARY = os.path.join(HERE, "libpa.so")
 # decode.cu comes first among the slow units so that it starts first.
-SOURCES = ["decode_mma_shared.cu", "decode_mma_plain.cu", "decode_simt.cu", "decode.cu", "pa_api.cu", "cache_ops.cu",
-           "block_manager.cpp", "simulator.cpp", "shared_plan.cpp"]
-HEADERS = ["pa_common.cuh", "pa_internal.h", "decode_kernels.h", "decode_merge.cuh", "decode_plan.cuh", "decode_simt.cuh", "decode_mma.cuh"]
+SOURCES = ["decode_mma_shared.cu", "decode_mma_plain.cu", "decode_fma.cu", "decode_simt.cu", "decode.cu", "pa_api.cu",
+           "cache_ops.cu", "block_manager.cpp", "simulator.cpp", "shared_plan.cpp"]
+HEADERS = ["pa_common.cuh", "pa_internal.h", "decode_kernels.h", "decode_merge.cuh", "decode_plan.cuh", "decode_simt.cuh",
+           "decode_mma.cuh", "decode_fma.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

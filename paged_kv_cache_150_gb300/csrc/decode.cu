@@ -54,6 +54,7 @@
 #include "decode_kernels.h"
 #include "decode_merge.cuh"
 #include "decode_plan.cuh"
+#include "decode_fma.cuh"  // FmaSmem, fma_lanes_per_token (host side)
 
 namespace pa {
 
@@ -62,6 +63,8 @@ namespace {
 
 struct DecodePlan {
     int kernel;    // PA_KERNEL_SIMT or PA_KERNEL_MMA
+    bool fma;      // CUDA-core: the TMA-staged kernel (decode_fma_kernel), not the per-token one
+    int stages;    // decode_fma_kernel: ring stages
     int NH;        // KV heads per CTA (consumer warps)
     int NG;        // head groups = Hk / NH
     int HPG;       // query heads per group = NH * G
@@ -94,14 +97,48 @@ bool simt_supported(const pa_cache_desc_t *c, int G) {
     return d_ok && G >= 1 && G <= 8;
 }
 
+// The TMA-staged CUDA-core kernel covers the row layout for D whose rows are
+// whole 128-byte lines (fp32 64 and 128, bf16 64, 128 and 256), G <= 8 and any
+// block size whose ring fits shared memory (fma_shape).
+constexpr size_t kFmaStageCap = 32 * 1024;  // K + V bytes of one ring stage, NH chosen to fit
+constexpr size_t kFmaRingTarget = 64 * 1024;
+constexpr size_t kFmaSmemMax = 200 * 1024;
+
+// NH (KV heads per CTA), stages and shared memory of decode_fma_kernel for
+// this shape; false if its ring does not fit.
+bool fma_shape(const pa_cache_desc_t *c, int G, int *NH, int *stages, size_t *smem) {
+    if (c->layout != PA_LAYOUT_ROW || G < 1 || G > 8 || c->block_size > 256) return false;
+    const bool d_ok = c->dtype == PA_F32 ? (c->head_dim == 64 || c->head_dim == 128)
+                                         : (c->head_dim == 64 || c->head_dim == 128 || c->head_dim == 256);
+    if (!d_ok) return false;
+    const int eb = dtype_bytes(c->dtype), line = 128 / eb, D = c->head_dim, B = c->block_size;
+    int nh = 1;
+    for (int d = std::min(c->num_kv_heads, kMmaMaxHeads); d >= 1; --d) {
+        if (c->num_kv_heads % d == 0 && 2 * (size_t)FmaSmem::box_bytes(d, D, B, line) <= kFmaStageCap) {
+            nh = d;
+            break;
+        }
+    }
+    const size_t stage = 2 * (size_t)FmaSmem::box_bytes(nh, D, B, line);
+    const int st = (int)std::max<size_t>(2, std::min<size_t>(8, kFmaRingTarget / stage));
+    const int gm = fma_gmax(G);
+    const size_t bytes = FmaSmem::bytes(st, nh, D, B, line, gm, fma_lanes_per_token(B));
+    if (bytes > kFmaSmemMax) return false;
+    *NH = nh;
+    *stages = st;
+    *smem = bytes;
+    return true;
+}
+
 // kMmaStages stages of NH head slabs of K and of V (the shared-prefix CTAs
-// use the same ring with NH = kPlanHeads), mbarriers after the tiles, with
-// shared prefixes the query rows of the shared-prefix warps (QRows, 256
-// bytes after the tiles); 1024 bytes to align the base.
+// cut the same ring bytes, NH = kPlanWarps, into their own stages),
+// mbarriers after the tiles, with shared prefixes the query rows of the
+// shared-prefix warps (QRows, 256 bytes after the tiles); 1024 bytes to align
+// the base.
 size_t mma_smem_bytes(int D, int B, int NH, bool shared) {
     const size_t slab = (size_t)(D / 64) * B * 128;
     size_t bytes = (size_t)kMmaStages * 2 * NH * slab + 2 * (size_t)kMmaStages * sizeof(uint64_t) + 1024;
-    if (shared) bytes += 256 + (size_t)kPlanHeads * kPlanRows * (D * 2 + 16);  // QRows of the shared-prefix warps
+    if (shared) bytes += 256 + (size_t)kPlanWarps * kPlanWarpRows * (D * 2 + 16);  // QRows of the shared-prefix warps
     return bytes;
 }
 
@@ -208,10 +245,14 @@ pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_d
     }
     p->kernel = kernel;
     p->shared = false;
-    if (kernel == PA_KERNEL_MMA) {
+    p->fma = false;
+    p->stages = 0;
+    if (kernel == PA_KERNEL_SIMT && fma_shape(c, G, &p->NH, &p->stages, &p->smem)) {
+        p->fma = true;
+    } else if (kernel == PA_KERNEL_MMA) {
         p->NH = largest_divisor_at_most(c->num_kv_heads, kMmaMaxHeads);
         // Shared-prefix CTAs use 4 consumer warps: the launch shape must match.
-        p->shared = opts && opts->shared_plan && p->NH == kPlanHeads;
+        p->shared = opts && opts->shared_plan && p->NH == kPlanWarps;
         p->smem = mma_smem_bytes(c->head_dim, c->block_size, p->NH, p->shared);
     } else {
         p->NH = largest_divisor_at_most(c->num_kv_heads, 8);
@@ -219,13 +260,14 @@ pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_d
     }
     p->NG = c->num_kv_heads / p->NH;
     p->HPG = p->NH * G;
-    const int threads = kernel == PA_KERNEL_MMA ? (p->NH + 1) * 32 : p->NH * 32;
+    const int threads = kernel == PA_KERNEL_MMA || p->fma ? (p->NH + 1) * 32 : p->NH * 32;
     const int C_given = opts ? opts->num_splits : 0;
     int C = C_given;
     if (C == 0) {
         if (!need_default_splits) return PA_ERR_INVALID_ARG;
         const void *fn = kernel == PA_KERNEL_MMA ? mma_kernel_ptr(c->head_dim, c->block_size, c->layout, p->shared)
-                                                 : simt_kernel_ptr(c->dtype, c->head_dim, G, c->layout);
+                         : p->fma             ? fma_kernel_ptr(c->dtype, c->head_dim, G)
+                                              : simt_kernel_ptr(c->dtype, c->head_dim, G, c->layout);
         C = default_ctas(fn, threads, p->smem);
         if (C <= 0) return PA_ERR_CUDA;
     }
@@ -315,7 +357,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 4-D maps over one bf16 cache (both use 128-byte rows of 64 elements).
+// 4-D maps over one cache (128-byte rows: 64 bf16 or 32 fp32 elements); NH
+// heads per box (the own-block CTAs' NH, or 1 for the shared-prefix CTAs).
+// The split layout is bf16 only (tensor-core kernel).
 // Row layout: {64, NB*B, D/64, Hk} with byte strides {Hk*D*2, 128, D*2}, box
 // {64, B, D/64, NH}, 128-byte swizzle -> shared [head][half][token][64].
 // Split layout (K [NB, Hk, D/8, B, 8] or V [NB, Hk, D, B]): each (block, head)
@@ -328,6 +372,8 @@ bool encode_cache_map(CUtensorMap *map, const void *base, const pa_cache_desc_t 
     const int D = c->head_dim;
     const int B = c->block_size;
     const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const int eb = dtype_bytes(c->dtype), line = 128 / eb;
+    const CUtensorMapDataType et = c->dtype == PA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUresult r;
     if (c->layout == PA_LAYOUT_SPLIT) {
         cuuint64_t dims[4] = {64, (cuuint64_t)D * B / 64, (cuuint64_t)c->num_kv_heads, (cuuint64_t)c->num_blocks};
@@ -337,10 +383,11 @@ bool encode_cache_map(CUtensorMap *map, const void *base, const pa_cache_desc_t 
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
-        cuuint64_t dims[4] = {64, (cuuint64_t)c->num_blocks * B, (cuuint64_t)(D / 64), (cuuint64_t)c->num_kv_heads};
-        cuuint64_t strides[3] = {(cuuint64_t)c->num_kv_heads * D * 2, 128, (cuuint64_t)D * 2};
-        cuuint32_t box[4] = {64, (cuuint32_t)B, (cuuint32_t)(D / 64), (cuuint32_t)NH};
-        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+        cuuint64_t dims[4] = {(cuuint64_t)line, (cuuint64_t)c->num_blocks * B, (cuuint64_t)(D / line),
+                              (cuuint64_t)c->num_kv_heads};
+        cuuint64_t strides[3] = {(cuuint64_t)c->num_kv_heads * D * eb, 128, (cuuint64_t)D * eb};
+        cuuint32_t box[4] = {(cuuint32_t)line, (cuuint32_t)B, (cuuint32_t)(D / line), (cuuint32_t)NH};
+        r = fn(map, et, 4, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
@@ -471,9 +518,16 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         return PA_ERR_CUDA;
     if (p.kernel == PA_KERNEL_MMA) {
         if (((uintptr_t)k_cache | (uintptr_t)v_cache) % 16 != 0) return PA_ERR_INVALID_ARG;
-        CUtensorMap tmk, tmv;
+        CUtensorMap tmk, tmv, tmk1, tmv1;  // NH-head boxes; one-head boxes for the shared-prefix CTAs
         if (!encode_cache_map(&tmk, k_cache, cache, p.NH) || !encode_cache_map(&tmv, v_cache, cache, p.NH))
             return PA_ERR_CUDA;
+        if (p.shared) {
+            if (!encode_cache_map(&tmk1, k_cache, cache, 1) || !encode_cache_map(&tmv1, v_cache, cache, 1))
+                return PA_ERR_CUDA;
+        } else {
+            tmk1 = tmk;
+            tmv1 = tmv;
+        }
         const void *fn = mma_kernel_ptr(cache->head_dim, cache->block_size, cache->layout, p.shared);
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
             return PA_ERR_CUDA;
@@ -485,7 +539,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         float sl = scale_log2;
         int32_t local_cu = p.local_cu ? 1 : 0;
         int32_t min_pieces = call_min_pieces(p, opts, num_seqs, cache->block_size, max_len);
-        void *args[] = {&tmk, &tmv, &qb, &ob, &block_tables, &mb, &lens_ws, &cu, &Nv, &Hv, &Hk,
+        void *args[] = {&tmk, &tmv, &tmk1, &tmv1, &qb, &ob, &block_tables, &mb, &lens_ws, &cu, &Nv, &Hv, &Hk,
                         &Gv, &NB, &NHv, &sl, &Cv, &ml, &acc, &cnt, &start_seq, &err, &sh, &seq_lens, &local_cu,
                         &min_pieces};
         if (launch_pdl(fn, grid, block, args, p.smem, s) != cudaSuccess) return PA_ERR_CUDA;
@@ -507,6 +561,23 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
                                                      : (const void *)shared_merge_kernel<64>;
             if (launch_pdl(mfn, mgrid, mblock, margs, 0, s) != cudaSuccess) return PA_ERR_CUDA;
         }
+    } else if (p.fma) {
+        if (((uintptr_t)k_cache | (uintptr_t)v_cache) % 16 != 0) return PA_ERR_INVALID_ARG;
+        CUtensorMap tmk, tmv;
+        if (!encode_cache_map(&tmk, k_cache, cache, p.NH) || !encode_cache_map(&tmv, v_cache, cache, p.NH))
+            return PA_ERR_CUDA;
+        const void *fn = fma_kernel_ptr(cache->dtype, cache->head_dim, G);
+        if (!fn) return PA_ERR_UNSUPPORTED;
+        if (p.smem > 48 * 1024 &&
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
+            return PA_ERR_CUDA;
+        const dim3 grid(p.C), block((p.NH + 1) * 32);
+        int32_t NB = cache->num_blocks, Hk = cache->num_kv_heads, NHv = p.NH, Cv = p.C, St = p.stages;
+        int32_t Nv = num_seqs, Hv = num_heads, Gv = G, mb = max_blocks_per_seq, Bv = cache->block_size;
+        float sl = scale_log2;
+        void *args[] = {&tmk, &tmv, &q, &out, &block_tables, &mb, &lens_ws, &cu, &Nv, &Hv, &Hk, &Gv, &Bv, &NB,
+                        &NHv, &St, &sl, &Cv, &ml, &acc, &cnt, &start_seq, &err};
+        if (launch_pdl(fn, grid, block, args, p.smem, s) != cudaSuccess) return PA_ERR_CUDA;
     } else {
         const void *fn = simt_kernel_ptr(cache->dtype, cache->head_dim, G, cache->layout);
         if (!fn) return PA_ERR_UNSUPPORTED;

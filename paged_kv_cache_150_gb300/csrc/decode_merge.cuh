@@ -148,8 +148,8 @@ __device__ __forceinline__ PieceRange own_range(const float2 *ml, const float *a
 __device__ __forceinline__ PieceRange no_range() { return PieceRange{nullptr, nullptr, 0, 0, 0, 0, -1}; }
 
 // The shared-prefix part of a launch, as the merge needs it: the shared
-// split is the flattened (head group hg of kPlanHeads heads, virtual
-// sequence, block) list of Ws entries cut over Ce_s CTAs.
+// split is the flattened (stage head group hg of plan_stage_heads(R) KV
+// heads, virtual sequence, block) list of Ws entries cut over Ce_s CTAs.
 struct SharedView {
     PlanView pv;
     const int32_t *skip;
@@ -166,26 +166,27 @@ __device__ __forceinline__ SharedView shared_view(const int32_t *plan, const int
     sv.skip = skip;
     sv.ml_s = ml_s;
     sv.acc_s = acc_s;
-    sv.Ws = (int64_t)(Hk / kPlanHeads) * sv.pv.cu_s[sv.pv.V];
+    sv.Ws = (int64_t)(Hk / plan_stage_heads(sv.pv.R)) * sv.pv.cu_s[sv.pv.V];
     sv.Ce_s = (int32_t)(sv.Ws < (int64_t)Cs ? sv.Ws : (int64_t)Cs);
     return sv;
 }
 
 // Pieces of the shared prefix of sequence seq for KV head kvh (none when the
 // sequence is computed without sharing): the virtual sequence v that holds
-// its G query rows, in slots c + hg * V + v, rows (kvh % 4) * 16 + row % 16.
+// its G query rows, in slots c + hg * V + v (hg = kvh / heads per stage),
+// rows (kvh % heads per stage) * R + row % R.
 __device__ __forceinline__ PieceRange shared_range(const SharedView &sv, int32_t seq, int32_t kvh, int32_t G) {
     if (sv.skip[seq] <= 0) return no_range();
     const PlanView &pv = sv.pv;
-    const int32_t hg = kvh / kPlanHeads;
+    const int32_t R = pv.R, nhb = plan_stage_heads(R);
+    const int32_t hg = kvh / nhb;
     const int32_t grp = pv.seq_group[seq];
     const int32_t row0 = pv.seq_member[seq] * G;
-    const int32_t v = pv.group_vbase[grp] + row0 / kPlanRows;
+    const int32_t v = pv.group_vbase[grp] + row0 / R;
     const int64_t xs = (int64_t)hg * pv.cu_s[pv.V] + pv.cu_s[v];
     const int32_t P = pv.cu_s[v + 1] - pv.cu_s[v];
-    return PieceRange{sv.ml_s, sv.acc_s, (int64_t)hg * pv.V + v, kPlanSlotRows,
-                      (kvh - hg * kPlanHeads) * kPlanRows + row0 % kPlanRows, split_owner(xs, sv.Ws, sv.Ce_s),
-                      split_owner(xs + P - 1, sv.Ws, sv.Ce_s)};
+    return PieceRange{sv.ml_s, sv.acc_s, (int64_t)hg * pv.V + v, kPlanSlotRows, (kvh - hg * nhb) * R + row0 % R,
+                      split_owner(xs, sv.Ws, sv.Ce_s), split_owner(xs + P - 1, sv.Ws, sv.Ce_s)};
 }
 
 // After a warp published a piece of (sequence seq, KV head kvh): count the

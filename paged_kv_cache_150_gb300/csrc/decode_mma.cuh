@@ -1,7 +1,7 @@
 // TMA + tensor-core decode kernel (instantiated in decode_mma_plain.cu and
 // decode_mma_shared.cu).
 //
-// TMA tiles of (block, 4 KV heads) through an mbarrier ring, mma.sync for
+// TMA tiles of (block, up to 4 KV heads) through an mbarrier ring, mma.sync for
 // S^T = K Q^T and O^T += V^T P^T; own-block CTAs and, with a plan,
 // shared-prefix CTAs in one launch.
 #pragma once
@@ -108,7 +108,7 @@ __device__ __forceinline__ void mma_block(uint32_t kslab, uint32_t vslab, int32_
 template <int D>
 struct QRows {
     static constexpr int kRowBytes = D * 2 + 16;
-    static constexpr int kBytes = kPlanRows * kRowBytes;
+    static constexpr int kBytes = kPlanWarpRows * kRowBytes;
 };
 
 // The same as mma_block for NT 8-column tiles of query rows (NT * 8 rows) that
@@ -127,9 +127,13 @@ __device__ __forceinline__ void mma_block_tiles(uint32_t kslab, uint32_t vslab, 
     const uint32_t qrow = qsm + (uint32_t)(((mi >> 1) * 8 + rr) * QRows<D>::kRowBytes + (mi & 1) * 16);
 #pragma unroll
     for (int mt = 0; mt < B / 16; ++mt) {
-        float sacc[NT][4];
+        // Two accumulators per tile (even and odd k-steps), summed at the end:
+        // the dependent MMA chain is half as long.
+        float sacc[NT][2][4];
 #pragma unroll
-        for (int t = 0; t < NT; ++t) sacc[t][0] = sacc[t][1] = sacc[t][2] = sacc[t][3] = 0.f;
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) sacc[t][h][0] = sacc[t][h][1] = sacc[t][h][2] = sacc[t][h][3] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < KT; ++kk) {
             const int tk = mt * 16 + rr + (mi & 1) * 8;
@@ -140,14 +144,16 @@ __device__ __forceinline__ void mma_block_tiles(uint32_t kslab, uint32_t vslab, 
             else
                 ldmatrix_x4(kslab + (uint32_t)(((d >> 3) * B + tk) * 16), a0, a1, a2, a3);
             ldmatrix_x4(qrow + (uint32_t)(kk * 32), b00, b01, b10, b11);
-            mma_bf16_16816(sacc[0], a0, a1, a2, a3, b00, b01);
-            mma_bf16_16816(sacc[1], a0, a1, a2, a3, b10, b11);
+            mma_bf16_16816(sacc[0][kk & 1], a0, a1, a2, a3, b00, b01);
+            mma_bf16_16816(sacc[1][kk & 1], a0, a1, a2, a3, b10, b11);
         }
         uint32_t pb0[NT], pb1[NT];
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-            const float x0 = sacc[t][0] * scale_log2, x1 = sacc[t][1] * scale_log2;
-            const float x2 = sacc[t][2] * scale_log2, x3 = sacc[t][3] * scale_log2;
+            const float x0 = (sacc[t][0][0] + sacc[t][1][0]) * scale_log2;
+            const float x1 = (sacc[t][0][1] + sacc[t][1][1]) * scale_log2;
+            const float x2 = (sacc[t][0][2] + sacc[t][1][2]) * scale_log2;
+            const float x3 = (sacc[t][0][3] + sacc[t][1][3]) * scale_log2;
             float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
@@ -162,12 +168,16 @@ __device__ __forceinline__ void mma_block_tiles(uint32_t kslab, uint32_t vslab, 
             l[t][1] = l[t][1] * al1 + (p1 + p3);
             m[t][0] = mn0;
             m[t][1] = mn1;
+            // Rescale only when some row's running maximum moved (a factor of
+            // exactly 1 changes nothing): after the first blocks it rarely does.
+            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-            for (int dm = 0; dm < KT; ++dm) {
-                o[t][dm][0] *= al0;
-                o[t][dm][1] *= al1;
-                o[t][dm][2] *= al0;
-                o[t][dm][3] *= al1;
+                for (int dm = 0; dm < KT; ++dm) {
+                    o[t][dm][0] *= al0;
+                    o[t][dm][1] *= al1;
+                    o[t][dm][2] *= al0;
+                    o[t][dm][3] *= al1;
+                }
             }
             pb0[t] = movmatrix_trans(pack_bf16x2(p0, p1));
             pb1[t] = movmatrix_trans(pack_bf16x2(p2, p3));
@@ -190,30 +200,36 @@ __device__ __forceinline__ void mma_block_tiles(uint32_t kslab, uint32_t vslab, 
     }
 }
 
-// A CTA of the shared-prefix part.  Its range of the flattened (head group
-// hg, virtual sequence v, block) list: W_s = (Hk / 4) * cu_s[V] entries cut
-// over Ce_s CTAs.  The ring, its stages and the TMA box of 4 KV heads are the
-// own-block CTAs'.  Each block of a group's prefix is read once (the table of
-// the group's first member) and warp w applies head hg * 4 + w to the pass's
-// 16 query rows (member m = row / G, query head h = kvh * G + row % G), as
-// two 8-column MMA tiles.  A piece's partial goes to slot c + hg * V + v;
-// shared_merge_kernel merges the members' pieces after the launch.
+// A CTA of the shared-prefix part.  Its range of the flattened (stage head
+// group hg, virtual sequence v, block) list: W_s = (Hk / nhb) * cu_s[V]
+// entries cut over Ce_s CTAs, nhb = plan_stage_heads(R) KV heads per stage.
+// The ring has the own-block CTAs' bytes, cut into 2, 4 or 8 stages of nhb
+// one-head TMA boxes of K and of V (tmk1 / tmv1).  Each block of a group's
+// prefix is read once per pass (the table of the group's first member), and
+// warp w applies head hg * nhb + w / (R / 16) of the stage to its 16 query
+// rows of the pass (member m = row / G, query head h = kvh * G + row % G), as
+// two 8-column MMA tiles; a warp whose rows are all past the group's rows
+// only keeps the ring's phases.  A piece's partial goes to slot
+// c + hg * V + v, rows w * 16 .. + 15; shared_merge_kernel merges the
+// members' pieces after the launch.
 template <int D, int B, int LAYOUT>
-__device__ __forceinline__ void shared_prefix_cta(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMap *tmv,
+__device__ __forceinline__ void shared_prefix_cta(uint8_t *smem, const CUtensorMap *tmk1, const CUtensorMap *tmv1,
                                                   const __nv_bfloat16 *__restrict__ q,
                                                   const int32_t *__restrict__ tables, int32_t max_blocks, int32_t H,
                                                   int32_t G, int32_t NB, float scale_log2, int32_t Hk, int32_t Cs,
                                                   const SharedArgs &sh, unsigned int *__restrict__ err) {
     using Tile = MmaTile<D, B>;
-    constexpr int S = Tile::kStages;
     constexpr int KT = D / 16;
-    constexpr int NT = kPlanRows / 8;  // MMA tiles per warp
-    constexpr uint32_t tile_bytes = kPlanHeads * Tile::kSlabBytes, stage_bytes = 2 * tile_bytes;
-    uint64_t *full = (uint64_t *)(smem + S * stage_bytes);
-    uint64_t *empty = full + S;
-    uint8_t *qbuf = smem + S * stage_bytes + 256;  // QRows of each consumer warp
+    constexpr int NT = kPlanWarpRows / 8;  // MMA tiles per warp
+    constexpr uint32_t ring_bytes = (uint32_t)Tile::kStages * 2 * kPlanWarps * Tile::kSlabBytes;
     const SharedView sv = shared_view(sh.plan, sh.skip, sh.ml_s, sh.acc_s, Hk, Cs);
     const PlanView &pv = sv.pv;
+    const int32_t R = pv.R, nhb = plan_stage_heads(R), wph = R / kPlanWarpRows;
+    const uint32_t tile_bytes = (uint32_t)nhb * Tile::kSlabBytes, stage_bytes = 2 * tile_bytes;
+    const int S = (int)(ring_bytes / stage_bytes);  // 2, 4 or 8 stages
+    uint64_t *full = (uint64_t *)(smem + ring_bytes);
+    uint64_t *empty = full + S;                     // 2 * S <= 16 barriers in the 256 bytes after the ring
+    uint8_t *qbuf = smem + ring_bytes + 256;        // QRows of each consumer warp
     const int32_t c = blockIdx.x;
     if (c >= sv.Ce_s) return;
     const int64_t lo = split_begin(c, sv.Ws, sv.Ce_s), hi = split_begin(c + 1, sv.Ws, sv.Ce_s);
@@ -222,21 +238,20 @@ __device__ __forceinline__ void shared_prefix_cta(uint8_t *smem, const CUtensorM
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-#pragma unroll
-        for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), (uint32_t)kPlanHeads);
+        for (int st = 0; st < S; ++st) {
+            mbar_init(smem_u32(&full[st]), 1);
+            mbar_init(smem_u32(&empty[st]), (uint32_t)kPlanWarps);
         }
         fence_mbarrier_init();
     }
     __syncthreads();
 
-    if (warp == kPlanHeads) {
+    if (warp == kPlanWarps) {
         // ------------------------------------------------------- producer
         if (lane == 0) {
-            prefetch_tmap(tmk);
-            prefetch_tmap(tmv);
-            const uint64_t kv_policy = l2_policy_evict_first();  // each shared block is read once
+            prefetch_tmap(tmk1);
+            prefetch_tmap(tmv1);
+            const uint64_t kv_policy = l2_policy_evict_first();  // a pass streams each shared block once
             BlockCursor cur, ahead;
             cur.init_at(lo, sh.start_s[c], pv.cu_s, V);
             ahead.init_at(lo, sh.start_s[c], pv.cu_s, V);
@@ -263,7 +278,7 @@ __device__ __forceinline__ void shared_prefix_cta(uint8_t *smem, const CUtensorM
             }
             int64_t issued = 0;
             for (; issued < n; ++issued) {
-                const int s = (int)(issued % S);
+                const int st = (int)(issued % S);
                 const uint32_t ph = (uint32_t)((issued / S) & 1);
                 int32_t phys = ring[0];
 #pragma unroll
@@ -276,7 +291,7 @@ __device__ __forceinline__ void shared_prefix_cta(uint8_t *smem, const CUtensorM
                     ring[PD - 1] = tables[ahead_row + ahead.blk];
                     ahead.advance(pv.cu_s, V);
                 }
-                if (issued >= S && !mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u)) {
+                if (issued >= S && !mbar_wait_bounded(smem_u32(&empty[st]), ph ^ 1u)) {
                     atomicOr(err, kErrTimeout);
                     break;
                 }
@@ -284,15 +299,19 @@ __device__ __forceinline__ void shared_prefix_cta(uint8_t *smem, const CUtensorM
                     atomicOr(err, kErrBounds);
                     phys = NB;
                 }
-                const uint32_t fb = smem_u32(&full[s]);
-                const uint32_t dst = smem_u32(smem + (size_t)s * stage_bytes);
+                const uint32_t fb = smem_u32(&full[st]);
+                const uint32_t dst = smem_u32(smem + (size_t)st * stage_bytes);
                 mbar_arrive_expect_tx(fb, stage_bytes);
-                if (LAYOUT == PA_LAYOUT_ROW) {
-                    tma_load_4d_hint(dst, tmk, fb, 0, phys * B, 0, cur.g * kPlanHeads, kv_policy);
-                    tma_load_4d_hint(dst + tile_bytes, tmv, fb, 0, phys * B, 0, cur.g * kPlanHeads, kv_policy);
-                } else {
-                    tma_load_4d_hint(dst, tmk, fb, 0, 0, cur.g * kPlanHeads, phys, kv_policy);
-                    tma_load_4d_hint(dst + tile_bytes, tmv, fb, 0, 0, cur.g * kPlanHeads, phys, kv_policy);
+                for (int32_t h = 0; h < nhb; ++h) {  // nhb one-head boxes land as one nhb-head box would
+                    const int32_t head = cur.g * nhb + h;
+                    const uint32_t off = (uint32_t)h * Tile::kSlabBytes;
+                    if (LAYOUT == PA_LAYOUT_ROW) {
+                        tma_load_4d_hint(dst + off, tmk1, fb, 0, phys * B, 0, head, kv_policy);
+                        tma_load_4d_hint(dst + tile_bytes + off, tmv1, fb, 0, phys * B, 0, head, kv_policy);
+                    } else {
+                        tma_load_4d_hint(dst + off, tmk1, fb, 0, 0, head, phys, kv_policy);
+                        tma_load_4d_hint(dst + tile_bytes + off, tmv1, fb, 0, 0, head, phys, kv_policy);
+                    }
                 }
                 cur.advance(pv.cu_s, V);
             }
@@ -305,88 +324,106 @@ __device__ __forceinline__ void shared_prefix_cta(uint8_t *smem, const CUtensorM
 
     // ----------------------------------------------------------- consumers
     const int r = lane >> 2, cq = lane & 3;
+    const int hb = warp / wph, sub = warp - hb * wph;  // this warp's head in the stage, rows of the pass
     uint8_t *qw = qbuf + warp * QRows<D>::kBytes;
     float o[NT][KT][4];
     float mm[NT][2], ll[NT][2];
     BlockCursor cur;
     cur.init_at(lo, sh.start_s[c], pv.cu_s, V);
-    bool seg_start = true;
+    bool seg_start = true, active = false;
     int32_t grp = 0, rows = 0, row_base = 0;
     for (int64_t it = 0; it < n; ++it) {
-        const int s = (int)(it % S);
+        const int st = (int)(it % S);
         const uint32_t ph = (uint32_t)((it / S) & 1);
-        const int32_t kvh = cur.g * kPlanHeads + warp, v = cur.seq;
+        const int32_t kvh = cur.g * nhb + hb, v = cur.seq;
         if (seg_start) {
             grp = pv.vgroup[v];
             rows = (pv.group_begin[grp + 1] - pv.group_begin[grp]) * G;
-            row_base = (v - pv.group_vbase[grp]) * kPlanRows;
-            // The pass's 16 query rows of this warp's head into shared memory
-            // (zeros past the group's rows): row i = member i / G, head i % G.
-            __syncwarp();  // the previous segment's reads of qw are done
-            constexpr int kChunks = D / 8;  // 16-byte pieces of a row
-            for (int e = lane; e < kPlanRows * kChunks; e += 32) {
-                const int i = e / kChunks, ch = e - i * kChunks;
-                const int32_t gr = row_base + i;
-                uint4 val = make_uint4(0u, 0u, 0u, 0u);
-                if (gr < rows) {
-                    const int32_t m = gr / G;
-                    const int32_t seq = pv.members[pv.group_begin[grp] + m];
-                    const __nv_bfloat16 *qp = q + ((int64_t)seq * H + (int64_t)kvh * G + (gr - m * G)) * D;
-                    val = *reinterpret_cast<const uint4 *>(qp + ch * 8);  // q is 16-byte aligned with a plan
+            row_base = (v - pv.group_vbase[grp]) * R + sub * kPlanWarpRows;  // this warp's first row
+            active = row_base < rows;
+            if (active) {
+                // The warp's 16 query rows of its head into shared memory
+                // (zeros past the group's rows): row i = member i / G, head i % G.
+                // Lane i < 16 looks up row i's sequence; every load of the
+                // rows is then issued at once (one round trip, not one per row).
+                __syncwarp();  // the previous segment's reads of qw are done
+                int32_t row_seq = -1;
+                if (lane < kPlanWarpRows && row_base + lane < rows)
+                    row_seq = pv.members[pv.group_begin[grp] + (row_base + lane) / G];
+                constexpr int kChunks = D / 8;  // 16-byte pieces of a row
+                uint4 val[kPlanWarpRows * kChunks / 32];
+#pragma unroll
+                for (int k = 0; k < kPlanWarpRows * kChunks / 32; ++k) {
+                    const int e = lane + 32 * k, i = e / kChunks, ch = e - i * kChunks;
+                    const int32_t seq = __shfl_sync(0xffffffffu, row_seq, i);
+                    const int32_t gr = row_base + i;
+                    val[k] = make_uint4(0u, 0u, 0u, 0u);
+                    if (seq >= 0) {  // q is 16-byte aligned with a plan
+                        const __nv_bfloat16 *qp = q + ((int64_t)seq * H + (int64_t)kvh * G + gr % G) * D;
+                        val[k] = *reinterpret_cast<const uint4 *>(qp + ch * 8);
+                    }
                 }
-                *reinterpret_cast<uint4 *>(qw + i * QRows<D>::kRowBytes + ch * 16) = val;
-            }
-            __syncwarp();
 #pragma unroll
-            for (int t = 0; t < NT; ++t) {
+                for (int k = 0; k < kPlanWarpRows * kChunks / 32; ++k) {
+                    const int e = lane + 32 * k, i = e / kChunks, ch = e - i * kChunks;
+                    *reinterpret_cast<uint4 *>(qw + i * QRows<D>::kRowBytes + ch * 16) = val[k];
+                }
+                __syncwarp();
 #pragma unroll
-                for (int kk = 0; kk < KT; ++kk)
+                for (int t = 0; t < NT; ++t) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) o[t][kk][e] = 0.f;
-                mm[t][0] = mm[t][1] = -INFINITY;
-                ll[t][0] = ll[t][1] = 0.f;
+                    for (int kk = 0; kk < KT; ++kk)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) o[t][kk][e] = 0.f;
+                    mm[t][0] = mm[t][1] = -INFINITY;
+                    ll[t][0] = ll[t][1] = 0.f;
+                }
             }
             seg_start = false;
         }
-        const bool ok = mbar_wait_bounded(smem_u32(&full[s]), ph);
+        const bool ok = mbar_wait_bounded(smem_u32(&full[st]), ph);
         if (!__all_sync(0xffffffffu, ok)) {
             if (lane == 0) atomicOr(err, kErrTimeout);
             return;
         }
-        const uint32_t kslab = smem_u32(smem + (size_t)s * stage_bytes) + (uint32_t)warp * Tile::kSlabBytes;
-        mma_block_tiles<D, B, LAYOUT, NT>(kslab, kslab + tile_bytes, smem_u32(qw), scale_log2, o, mm, ll, lane);
+        if (active) {
+            const uint32_t kslab = smem_u32(smem + (size_t)st * stage_bytes) + (uint32_t)hb * Tile::kSlabBytes;
+            mma_block_tiles<D, B, LAYOUT, NT>(kslab, kslab + tile_bytes, smem_u32(qw), scale_log2, o, mm, ll, lane);
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
 
         if (cur.blk == cur.nb - 1 || it + 1 == n) {
-            const int64_t slot = partial_slot(c, cur.g * V + v);
-            const int64_t wrow = slot * kPlanSlotRows + warp * kPlanRows;  // this warp's 16 rows
-            const int h0 = 2 * cq, h1 = 2 * cq + 1;
+            if (active) {
+                const int64_t slot = partial_slot(c, cur.g * V + v);
+                const int64_t wrow = slot * kPlanSlotRows + warp * kPlanWarpRows;  // this warp's 16 rows
+                const int h0 = 2 * cq, h1 = 2 * cq + 1;
 #pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                float lt0 = ll[t][0], lt1 = ll[t][1];
+                for (int t = 0; t < NT; ++t) {
+                    float lt0 = ll[t][0], lt1 = ll[t][1];
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    lt0 += __shfl_xor_sync(0xffffffffu, lt0, off);
-                    lt1 += __shfl_xor_sync(0xffffffffu, lt1, off);
-                }
-                const bool v0 = row_base + t * 8 + h0 < rows, v1 = row_base + t * 8 + h1 < rows;
-                float *ab = sh.acc_s + (wrow + t * 8) * D;
-#pragma unroll
-                for (int dm = 0; dm < KT; ++dm) {
-                    const int d = dm * 16 + r;
-                    if (v0) {
-                        ab[h0 * D + d] = o[t][dm][0];
-                        ab[h0 * D + d + 8] = o[t][dm][2];
+                    for (int off = 4; off < 32; off <<= 1) {
+                        lt0 += __shfl_xor_sync(0xffffffffu, lt0, off);
+                        lt1 += __shfl_xor_sync(0xffffffffu, lt1, off);
                     }
-                    if (v1) {
-                        ab[h1 * D + d] = o[t][dm][1];
-                        ab[h1 * D + d + 8] = o[t][dm][3];
+                    const bool v0 = row_base + t * 8 + h0 < rows, v1 = row_base + t * 8 + h1 < rows;
+                    float *ab = sh.acc_s + (wrow + t * 8) * D;
+#pragma unroll
+                    for (int dm = 0; dm < KT; ++dm) {
+                        const int d = dm * 16 + r;
+                        if (v0) {
+                            ab[h0 * D + d] = o[t][dm][0];
+                            ab[h0 * D + d + 8] = o[t][dm][2];
+                        }
+                        if (v1) {
+                            ab[h1 * D + d] = o[t][dm][1];
+                            ab[h1 * D + d + 8] = o[t][dm][3];
+                        }
                     }
-                }
-                if (r == 0) {
-                    if (v0) sh.ml_s[wrow + t * 8 + h0] = make_float2(mm[t][0], lt0);
-                    if (v1) sh.ml_s[wrow + t * 8 + h1] = make_float2(mm[t][1], lt1);
+                    if (r == 0) {
+                        if (v0) sh.ml_s[wrow + t * 8 + h0] = make_float2(mm[t][0], lt0);
+                        if (v1) sh.ml_s[wrow + t * 8 + h1] = make_float2(mm[t][1], lt1);
+                    }
                 }
             }
             seg_start = true;
@@ -735,10 +772,12 @@ __device__ __forceinline__ void local_prefix_sums(const int32_t *__restrict__ se
 // The attention launch.  Without a plan (kShared = false) every CTA is an
 // own-block CTA.  With one, the plan kernel gives CTAs [0, Cs) to the shared
 // prefixes and the rest to the sequences' own blocks; both kinds run at once
-// and meet only at the arrival counters.
+// and meet only at the arrival counters.  tmk / tmv hold NH-head boxes (the
+// own-block CTAs'), tmk1 / tmv1 one-head boxes (the shared-prefix CTAs').
 template <int D, int B, int LAYOUT, bool kShared>
 __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+    const __grid_constant__ CUtensorMap tmk1, const __grid_constant__ CUtensorMap tmv1,
     const __nv_bfloat16 *__restrict__ q, __nv_bfloat16 *__restrict__ out,
     const int32_t *__restrict__ tables, int32_t max_blocks, const int32_t *__restrict__ lens,
     const int32_t *__restrict__ cu, int32_t N, int32_t H, int32_t Hk, int32_t G, int32_t NB,
@@ -771,7 +810,7 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
     if (kShared || min_pieces > 0) grid_launch_dependents();
     const int32_t Cs = kShared ? sh.ctl[0] : 0;
     if (kShared && (int32_t)blockIdx.x < Cs)
-        shared_prefix_cta<D, B, LAYOUT>(smem, &tmk, &tmv, q, tables, max_blocks, H, G, NB, scale_log2, Hk, Cs, sh,
+        shared_prefix_cta<D, B, LAYOUT>(smem, &tmk1, &tmv1, q, tables, max_blocks, H, G, NB, scale_log2, Hk, Cs, sh,
                                         err);
     else
         own_block_cta<D, B, LAYOUT, kShared>(smem, &tmk, &tmv, q, out, tables, max_blocks, lens_p, cu_p, N, H, G,

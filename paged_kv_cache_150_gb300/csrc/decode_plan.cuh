@@ -11,17 +11,17 @@ namespace pa {
 
 // ---------------------------------------------------------------- plan kernel
 // Checks a shared-prefix plan's words against the call (sizes, heads per KV
-// head, block size, and every index it holds), so that a bad plan can only
-// switch sharing off, never send a kernel out of bounds.  Block-wide; every
-// thread returns the verdict.
-__device__ bool plan_valid(const int32_t *__restrict__ w, int32_t N, int32_t G, int32_t B, int32_t max_blocks,
-                           int *s_flag, int *s_count) {
+// head, block size, rows per pass, and every index it holds), so that a bad
+// plan can only switch sharing off, never send a kernel out of bounds.
+// Block-wide; every thread returns the verdict.
+__device__ bool plan_valid(const int32_t *__restrict__ w, int32_t N, int32_t G, int32_t B, int32_t Hk,
+                           int32_t max_blocks, int *s_flag, int *s_count) {
     if (threadIdx.x == 0) {
         const int32_t groups = w[4], M = w[5], V = w[6];
         const int32_t R = w[7];
         bool ok = w[0] == kPlanMagic && w[1] == N && w[2] == G && w[3] == B && groups >= 0 && groups <= N &&
-                  M >= 0 && M <= N && V >= 0 && V <= N && R == kPlanRows && G <= 8 && 8 % G == 0 &&
-                  PlanView::words(N, groups, M, V) <= 7 * (int64_t)N + 16;
+                  M >= 0 && M <= N && V >= 0 && V <= N && plan_rows_ok(R) && Hk % plan_stage_heads(R) == 0 &&
+                  G <= 8 && 8 % G == 0 && PlanView::words(N, groups, M, V) <= 7 * (int64_t)N + 16;
         if (ok) {
             const PlanView pv = PlanView::at(w);
             ok = pv.group_begin[0] == 0 && pv.group_begin[groups] == M && pv.group_vbase[0] == 0 &&
@@ -37,7 +37,7 @@ __device__ bool plan_valid(const int32_t *__restrict__ w, int32_t N, int32_t G, 
     for (int32_t g = threadIdx.x; g < pv.groups; g += blockDim.x) {
         const int32_t S = pv.group_begin[g + 1] - pv.group_begin[g];
         const int32_t passes = pv.group_vbase[g + 1] - pv.group_vbase[g];
-        ok = ok && S >= 1 && passes == (S * G + kPlanRows - 1) / kPlanRows && pv.group_prefix[g] >= 1 &&
+        ok = ok && S >= 1 && passes == (S * G + pv.R - 1) / pv.R && pv.group_prefix[g] >= 1 &&
              pv.group_prefix[g] <= max_blocks;
     }
     // From here group_begin and group_vbase are increasing from 0 to M and V,
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
         plan = plan_sm;
     }
     // A shared-prefix plan that does not match the call switches sharing off.
-    const bool plan_ok = plan && plan_valid(plan, N, G, B, max_len / B, &s_flag, &s_count);
+    const bool plan_ok = plan && plan_valid(plan, N, G, B, Hk, max_len / B, &s_flag, &s_count);
     if (plan && !plan_ok && threadIdx.x == 0) atomicOr(err, kErrPlan);
     const PlanView pv = plan_ok ? PlanView::at(plan) : PlanView{};
     for (int32_t base = 0; base < N; base += blockDim.x) {
@@ -172,13 +172,17 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
     if (threadIdx.x == 0) {
         cu[N] = carry;
         if (cu_in_smem) cu_s[N] = carry;
-        // CTAs for the shared prefixes, in proportion to the bytes they read
-        // (a shared unit is one KV head of a block, an own unit NH heads).
+        // CTAs for the shared prefixes, in proportion to the stages each side
+        // streams (a shared-prefix stage holds plan_stage_heads(R) KV heads,
+        // an own-block stage NH).  Measured on the prefix workload: a stage
+        // takes about the same time on either side, whatever the heads in it,
+        // since its consumers' work (16 query rows per warp), not its bytes,
+        // sets it.
         int32_t cs = 0;
         if (plan_ok) {
-            const int64_t Ws = (int64_t)Hk * pv.cu_s[pv.V], Wo = (int64_t)NG * carry * NH;
+            const double Ws = (double)(Hk / plan_stage_heads(pv.R)) * pv.cu_s[pv.V], Wo = (double)NG * carry;
             if (Ws > 0) {
-                const double share = (double)Ws / (double)(Ws + Wo);
+                const double share = Ws / (Ws + Wo);
                 cs = (int32_t)((double)C * share + 0.5);
                 cs = cs < 1 ? 1 : (cs > C - 1 ? C - 1 : cs);
             }
@@ -206,10 +210,11 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
         }
         start_seq[c] = lo;
     }
-    // The same for the shared-prefix CTAs over the virtual sequences.
+    // The same for the shared-prefix CTAs over the virtual sequences (the
+    // list's outer index is the stage's KV heads, plan_stage_heads(R) of them).
     if (s_cs > 0) {
         const int32_t Wv = pv.cu_s[pv.V];
-        const int64_t Ws = (int64_t)(Hk / kPlanHeads) * Wv;
+        const int64_t Ws = (int64_t)(Hk / plan_stage_heads(pv.R)) * Wv;
         const int32_t Ce_s = (int32_t)(Ws < (int64_t)s_cs ? Ws : (int64_t)s_cs);
         for (int32_t c = threadIdx.x; c < Ce_s; c += blockDim.x) {
             const int32_t r = (int32_t)(split_begin(c, Ws, Ce_s) % Wv);

@@ -64,17 +64,24 @@ __host__ __device__ __forceinline__ int64_t partial_slot(int32_t c, int32_t sp) 
 //   seq_group[N]  seq_member[N]  group_prefix[groups]  group_vbase[groups + 1]
 //   group_begin[groups + 1]  members[members]  vgroup[V]  cu_s[V + 1]
 // A group's sharers contribute G query rows each (member m: rows m*G ..
-// m*G + G - 1); the rows are cut into passes of R = kPlanRows, and each pass
-// is one "virtual sequence" v over the group's P shared blocks (cu_s = prefix
-// sums of P over virtual sequences).  A stage of a shared-prefix CTA holds
-// kPlanHeads KV heads, one per consumer warp, and each warp applies it to the
-// pass's 16 rows of its head (two 8-column MMA tiles).  G divides 8, so a
+// m*G + G - 1); the rows are cut into passes of R (16, 32 or 64, one value
+// per plan), and each pass is one "virtual sequence" v over the group's P
+// shared blocks (cu_s = prefix sums of P over virtual sequences).  A
+// shared-prefix CTA has kPlanWarps consumer warps of kPlanWarpRows rows each:
+// a stage holds kPlanSlotRows / R KV heads (1-head TMA boxes side by side),
+// and warp w applies head w / (R / 16) of the stage to rows
+// (w % (R / 16)) * 16 .. + 15 of the pass (two 8-column MMA tiles).  So one
+// streamed tile serves up to 64 query rows of its KV head.  G divides 8, so a
 // member's rows never straddle an MMA tile or a pass.
 constexpr int32_t kPlanMagic = 0x50415350;
 constexpr int kPlanHeader = 8;
-constexpr int kPlanRows = 16;                            // query rows per pass
-constexpr int kPlanHeads = 4;                            // KV heads per shared-prefix stage
-constexpr int kPlanSlotRows = kPlanHeads * kPlanRows;    // rows of one shared-prefix partial slot
+constexpr int kPlanWarps = 4;                               // consumer warps of a shared-prefix CTA
+constexpr int kPlanWarpRows = 16;                           // query rows of one consumer warp
+constexpr int kPlanSlotRows = kPlanWarps * kPlanWarpRows;   // rows of one shared-prefix partial slot
+
+// Rows per pass R that a plan may carry, and the KV heads of a stage for it.
+__host__ __device__ __forceinline__ bool plan_rows_ok(int32_t R) { return R == 16 || R == 32 || R == 64; }
+__host__ __device__ __forceinline__ int32_t plan_stage_heads(int32_t R) { return kPlanSlotRows / R; }
 
 struct PlanView {
     const int32_t *seq_group, *seq_member, *group_prefix, *group_vbase, *group_begin, *members, *vgroup, *cu_s;

@@ -13,8 +13,9 @@
 // leading blocks equal in every member's table, cut so that each member keeps
 // at least one position after it (P * B < L), and the group is dropped when
 // P < min_shared_blocks.
-#include <unordered_map>
+#include <algorithm>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 #include "pa_internal.h"
@@ -82,7 +83,13 @@ extern "C" pa_status_t pa_shared_plan_build(const int32_t *block_tables, int32_t
     }
 
     const int32_t NGr = (int32_t)groups.size();
-    const int32_t R = kPlanRows;  // query rows per pass
+    // Rows per pass: the smallest of 16, 32, 64 that holds the largest
+    // group's rows (64 for larger groups, which then take several passes).
+    // Fewer KV heads per stage for larger R, so one streamed tile serves all
+    // of a pass's rows.
+    int32_t max_rows = 0;
+    for (const auto &g : groups) max_rows = std::max(max_rows, (int32_t)g.members.size() * G);
+    const int32_t R = max_rows <= 16 ? 16 : (max_rows <= 32 ? 32 : 64);
     int32_t M = 0, V = 0;
     for (const auto &g : groups) {
         M += (int32_t)g.members.size();

@@ -16,15 +16,18 @@ from _pipeline import TOL, gpu_step, host_values, max_abs_err, oracle_decode, or
 
 pytestmark = pytest.mark.gpu
 
-# (name, prompts, prompt_len, samples, max_append, H, Hk, D, B)
+# (name, prompts, prompt_len, samples, max_append, H, Hk, D, B).  Rows per KV
+# head = samples x query heads per KV head; the plan's rows per pass R is the
+# smallest of 16, 32, 64 holding them (4, 2 or 1 KV heads per stage).
 SAMPLING = [
-    ("g4-s4", 6, 200, 4, 40, 32, 8, 128, 16),     # the parallel-sampling shape, reduced
-    ("g8-s4", 4, 150, 4, 30, 64, 8, 128, 16),     # 8 query heads per KV head: one member per warp
-    ("g1-s40", 2, 90, 40, 20, 32, 32, 128, 16),   # one query head per KV head, 40 sharers: three passes of 16
-    ("g2-b32", 3, 300, 5, 70, 16, 8, 128, 32),    # block size 32
-    ("g4-d64", 3, 120, 6, 25, 32, 8, 64, 16),     # head_dim 64
-    ("g4-s9-b32", 3, 64, 9, 10, 16, 4, 64, 32),   # 36 rows: three passes, head_dim 64, block 32
-    ("g2-s4", 3, 80, 4, 12, 16, 8, 128, 16),      # 8 rows: one pass, the second MMA tile empty
+    ("g4-s4", 6, 200, 4, 40, 32, 8, 128, 16),     # the parallel-sampling shape, reduced: 16 rows, R 16
+    ("g8-s4", 4, 150, 4, 30, 64, 8, 128, 16),     # 8 query heads per KV head: 32 rows, R 32 (2 heads per stage)
+    ("g1-s40", 2, 90, 40, 20, 32, 32, 128, 16),   # one query head per KV head, 40 sharers: R 64, one warp idle
+    ("g2-b32", 3, 300, 5, 70, 16, 8, 128, 32),    # block size 32: 10 rows, R 16
+    ("g4-d64", 3, 120, 6, 25, 32, 8, 64, 16),     # head_dim 64: 24 rows, R 32
+    ("g4-s9-b32", 3, 64, 9, 10, 16, 4, 64, 32),   # 36 rows, R 64, head_dim 64, block 32
+    ("g2-s4", 3, 80, 4, 12, 16, 8, 128, 16),      # 8 rows: R 16, the second MMA tile empty
+    ("g8-s9", 2, 120, 9, 20, 64, 8, 128, 16),     # 72 rows: R 64, two passes, the second on one warp
 ]
 
 
