@@ -565,8 +565,7 @@ def time_write_copy(step, iters, peak):
     if npairs:
         calls["block_copy"] = (lambda: pa.pa_copy_blocks(v["k_cache"], v["v_cache"], step.pairs),
                                2 * 2 * npairs * wl.block_size * row + 8 * npairs, npairs)
-    out = {}
-    for name, (fn, nbytes, units) in calls.items():
+    def median_us(fn):
         for _ in range(3):
             fn()
         ev = _events(iters)
@@ -576,12 +575,23 @@ def time_write_copy(step, iters, peak):
             fn()
             ev[i][1].record()
         torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
+
+    # The same timing around a kernel that does nothing: what one launch
+    # between two events costs on this machine whatever it moves (about 4 us).
+    floor_us = median_us(lambda: torch.cuda._sleep(0)) if hasattr(torch.cuda, "_sleep") else None
+    out = {}
+    for name, (fn, nbytes, units) in calls.items():
+        us = median_us(fn)
         pa.pa_get_device_error()
-        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
-        gbs = nbytes / (ms / 1e3) / 1e9
-        out[name] = {"us": round(ms * 1e3, 2), "bytes_read_written": nbytes,
+        gbs = nbytes / (us / 1e6) / 1e9
+        out[name] = {"us": round(us, 2), "bytes_read_written": nbytes,
                      ("rows" if name == "cache_write" else "pairs"): units,
                      "gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4)}
+        if floor_us is not None:
+            out[name]["empty_launch_us"] = round(floor_us, 2)
+            if us > floor_us:  # bandwidth of the time the call takes beyond an empty launch
+                out[name]["gbs_above_empty_launch"] = round(nbytes / ((us - floor_us) / 1e6) / 1e9, 1)
     del flush
     return out
 
