@@ -61,26 +61,34 @@ __device__ __forceinline__ void mma_block(uint32_t kslab, uint32_t vslab, int32_
         const float x2 = tb < L ? sacc[2] * scale_log2 : -INFINITY;
         const float x3 = tb < L ? sacc[3] * scale_log2 : -INFINITY;
         float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+        // Lazy maximum: the column maxima (shuffles over the 8 lanes of a
+        // column) and the rescale only when some score passes the running
+        // maximum by more than kLazyMaxSlack (always on a segment's first
+        // tokens, where the maximum is -inf).
+        if (__any_sync(0xffffffffu, mx0 > m0 + kLazyMaxSlack || mx1 > m1 + kLazyMaxSlack)) {
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float al0 = ex2_approx(m0 - mn0), al1 = ex2_approx(m1 - mn1);
-        const float p0 = ex2_approx(x0 - mn0), p1 = ex2_approx(x1 - mn1);
-        const float p2 = ex2_approx(x2 - mn0), p3 = ex2_approx(x3 - mn1);
-        l0 = l0 * al0 + (p0 + p2);
-        l1 = l1 * al1 + (p1 + p3);
-        m0 = mn0;
-        m1 = mn1;
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float al0 = ex2_approx(m0 - mn0), al1 = ex2_approx(m1 - mn1);
+            l0 *= al0;
+            l1 *= al1;
+            m0 = mn0;
+            m1 = mn1;
 #pragma unroll
-        for (int dm = 0; dm < KT; ++dm) {
-            o[dm][0] *= al0;
-            o[dm][1] *= al1;
-            o[dm][2] *= al0;
-            o[dm][3] *= al1;
+            for (int dm = 0; dm < KT; ++dm) {
+                o[dm][0] *= al0;
+                o[dm][1] *= al1;
+                o[dm][2] *= al0;
+                o[dm][3] *= al1;
+            }
         }
+        const float p0 = ex2_approx(x0 - m0), p1 = ex2_approx(x1 - m1);
+        const float p2 = ex2_approx(x2 - m0), p3 = ex2_approx(x3 - m1);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
         // P^T as the B operand: transpose the two 8x8 bf16 quadrants.
         const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
         const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
@@ -155,22 +163,20 @@ __device__ __forceinline__ void mma_block_tiles(uint32_t kslab, uint32_t vslab, 
             const float x2 = (sacc[t][0][2] + sacc[t][1][2]) * scale_log2;
             const float x3 = (sacc[t][0][3] + sacc[t][1][3]) * scale_log2;
             float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+            // Lazy maximum, as in mma_block: shuffles and rescale only when a
+            // score passes the running maximum by more than kLazyMaxSlack.
+            if (__any_sync(0xffffffffu, mx0 > m[t][0] + kLazyMaxSlack || mx1 > m[t][1] + kLazyMaxSlack)) {
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-            }
-            const float mn0 = fmaxf(m[t][0], mx0), mn1 = fmaxf(m[t][1], mx1);
-            const float al0 = ex2_approx(m[t][0] - mn0), al1 = ex2_approx(m[t][1] - mn1);
-            const float p0 = ex2_approx(x0 - mn0), p1 = ex2_approx(x1 - mn1);
-            const float p2 = ex2_approx(x2 - mn0), p3 = ex2_approx(x3 - mn1);
-            l[t][0] = l[t][0] * al0 + (p0 + p2);
-            l[t][1] = l[t][1] * al1 + (p1 + p3);
-            m[t][0] = mn0;
-            m[t][1] = mn1;
-            // Rescale only when some row's running maximum moved (a factor of
-            // exactly 1 changes nothing): after the first blocks it rarely does.
-            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                const float mn0 = fmaxf(m[t][0], mx0), mn1 = fmaxf(m[t][1], mx1);
+                const float al0 = ex2_approx(m[t][0] - mn0), al1 = ex2_approx(m[t][1] - mn1);
+                l[t][0] *= al0;
+                l[t][1] *= al1;
+                m[t][0] = mn0;
+                m[t][1] = mn1;
 #pragma unroll
                 for (int dm = 0; dm < KT; ++dm) {
                     o[t][dm][0] *= al0;
@@ -179,6 +185,10 @@ __device__ __forceinline__ void mma_block_tiles(uint32_t kslab, uint32_t vslab, 
                     o[t][dm][3] *= al1;
                 }
             }
+            const float p0 = ex2_approx(x0 - m[t][0]), p1 = ex2_approx(x1 - m[t][1]);
+            const float p2 = ex2_approx(x2 - m[t][0]), p3 = ex2_approx(x3 - m[t][1]);
+            l[t][0] += p0 + p2;
+            l[t][1] += p1 + p3;
             pb0[t] = movmatrix_trans(pack_bf16x2(p0, p1));
             pb1[t] = movmatrix_trans(pack_bf16x2(p2, p3));
         }

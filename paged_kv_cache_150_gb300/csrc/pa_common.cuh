@@ -35,6 +35,12 @@ constexpr int kTablePrefetch = 4;
 // on GB300 against 3-4 stages and 8 heads per CTA: deeper rings (192 KiB per
 // SM) were 2-3% slower on every workload.
 constexpr int kMmaStages = 2;
+// Online softmax with a lazy running maximum (log2 units): the column-wide
+// maximum is recomputed (shuffles) and the accumulators rescaled only when a
+// score exceeds the running maximum by more than this, so between updates the
+// probabilities 2^(s - m) stay at most 2^8.  The result is the same softmax:
+// numerator and denominator carry the same subtracted constant.
+constexpr float kLazyMaxSlack = 8.f;
 constexpr int kMmaMaxHeads = 4;
 // Sequences (+ 1) whose block-count prefix sums a tensor-core CTA computes in
 // its own shared memory (16 KiB) instead of waiting for the plan kernel's.
