@@ -58,6 +58,10 @@ SHAPES = [  # (dtype, H, Hk, D, B)
     ("bf16", 8, 8, 128, 16), ("bf16", 16, 8, 128, 16), ("bf16", 32, 8, 128, 32), ("bf16", 64, 8, 128, 32),
     ("bf16", 8, 1, 128, 16), ("bf16", 6, 2, 64, 16), ("bf16", 12, 4, 64, 32), ("bf16", 8, 8, 256, 16),
     ("bf16", 4, 4, 128, 8), ("f32", 8, 2, 128, 16), ("f32", 4, 4, 64, 4), ("f32", 3, 1, 64, 5),
+    # block sizes without a tensor-core instance: the TMA-staged CUDA-core kernel (a ring of 2 to 8
+    # stages), and fp32 blocks of 128 tokens, whose ring does not fit, on the per-token kernel
+    ("bf16", 8, 8, 64, 1), ("f32", 32, 8, 64, 7), ("bf16", 16, 8, 256, 64), ("f32", 8, 2, 128, 64),
+    ("f32", 16, 2, 128, 128),
 ]
 
 
