@@ -167,8 +167,10 @@ pa_status_t pa_copy_blocks(void *k_cache, void *v_cache, const pa_cache_desc_t *
  * ---------------------------------------------------------------------- */
 typedef enum pa_kernel {
     PA_KERNEL_AUTO = 0, /* tensor-core kernel when it applies, else the CUDA-core one */
-    PA_KERNEL_SIMT = 1, /* CUDA-core kernel (fp32 and bf16) */
-    PA_KERNEL_MMA = 2   /* TMA + tensor-core kernel (bf16, D % 64 == 0, B % 16 == 0) */
+    PA_KERNEL_SIMT = 1, /* CUDA-core kernel (fp32 and bf16): blocks staged by TMA in the row layout
+                           when the ring fits (D 64/128, bf16 also 256, block sizes up to 256),
+                           else one token at a time */
+    PA_KERNEL_MMA = 2   /* TMA + tensor-core kernel (bf16, D 64 or 128, B 16 or 32) */
 } pa_kernel_t;
 
 typedef struct pa_decode_opts {
