@@ -62,6 +62,8 @@ SHAPES = [  # (dtype, H, Hk, D, B)
     # stages), and fp32 blocks of 128 tokens, whose ring does not fit, on the per-token kernel
     ("bf16", 8, 8, 64, 1), ("f32", 32, 8, 64, 7), ("bf16", 16, 8, 256, 64), ("f32", 8, 2, 128, 64),
     ("f32", 16, 2, 128, 128),
+    # eight query heads per KV head on the CUDA-core kernel (its largest accumulator sets)
+    ("f32", 16, 2, 64, 16), ("f32", 16, 2, 128, 16), ("bf16", 16, 2, 256, 16), ("f32", 7, 1, 128, 32),
 ]
 
 
