@@ -74,7 +74,7 @@ struct DecodePlan {
     size_t smem;   // dynamic shared memory of the attention kernel
     // workspace layout (byte offsets)
     size_t off_lens, off_cu, off_cnt, off_start, off_ml, off_acc;
-    size_t off_skip, off_ctl, off_start_s, off_ml_s, off_acc_s;  // shared-prefix part
+    size_t off_skip, off_ctl, off_start_s, off_rowseq, off_ml_s, off_acc_s;  // shared-prefix part
     size_t total;
 };
 
@@ -306,7 +306,7 @@ pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_d
     off = align256(off + sizeof(float2) * slots * p->HPG);
     p->off_acc = off;
     off = align256(off + sizeof(float) * slots * p->HPG * c->head_dim);
-    p->off_skip = p->off_ctl = p->off_start_s = p->off_ml_s = p->off_acc_s = 0;
+    p->off_skip = p->off_ctl = p->off_start_s = p->off_rowseq = p->off_ml_s = p->off_acc_s = 0;
     if (p->shared) {
         // virtual sequences V <= N (checked on the device), so at most
         // C + Hk * N shared-prefix slots of kPlanSlotRows query rows
@@ -317,6 +317,8 @@ pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_d
         off = align256(off + sizeof(int32_t) * 8);
         p->off_start_s = off;
         off = align256(off + sizeof(int32_t) * (size_t)C);
+        p->off_rowseq = off;  // V <= N virtual sequences of R <= kPlanSlotRows rows
+        off = align256(off + sizeof(int32_t) * (size_t)std::max(N, 1) * kPlanSlotRows);
         p->off_ml_s = off;
         off = align256(off + sizeof(float2) * slots_s * kPlanSlotRows);
         p->off_acc_s = off;
@@ -491,6 +493,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         sh.skip = (const int32_t *)(ws + p.off_skip);
         sh.ctl = (const int32_t *)(ws + p.off_ctl);
         sh.start_s = (const int32_t *)(ws + p.off_start_s);
+        sh.rowseq = (const int32_t *)(ws + p.off_rowseq);
         sh.ml_s = (float2 *)(ws + p.off_ml_s);
         sh.acc_s = (float *)(ws + p.off_acc_s);
     }
@@ -500,6 +503,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         void *outp = out;
         const int32_t *planp = sh.plan;
         int32_t *skipp = (int32_t *)sh.skip, *ctlp = (int32_t *)sh.ctl, *start_sp = (int32_t *)sh.start_s;
+        int32_t *rowseqp = (int32_t *)sh.rowseq;
         // the plan's words in shared memory when they fit (at most 96 KiB)
         const size_t plan_bytes = sizeof(int32_t) * (7 * (size_t)num_seqs + 16);
         int32_t in_smem = p.shared && plan_bytes <= 96 * 1024 ? 1 : 0;
@@ -510,7 +514,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
             cudaFuncSetAttribute(pfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem) != cudaSuccess)
             return PA_ERR_CUDA;
         void *pargs[] = {&seq_lens, &Nv, &Bv, &ml_v, &HDv, &lens_ws, &cu, &cnt, &nc, &outp, &NGv, &Cv, &start_seq,
-                         &err, &planp, &Gv, &Hkv, &NHv, &skipp, &ctlp, &start_sp, &in_smem};
+                         &err, &planp, &Gv, &Hkv, &NHv, &skipp, &ctlp, &start_sp, &rowseqp, &in_smem};
         if (launch_pdl(pfn, dim3(1), dim3(1024), pargs, psmem, s) != cudaSuccess) return PA_ERR_CUDA;
     }
 

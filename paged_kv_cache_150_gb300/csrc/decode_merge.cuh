@@ -224,6 +224,8 @@ struct SharedArgs {
     const int32_t *skip;   // [N] shared blocks of each sequence, 0 = none (plan kernel)
     const int32_t *ctl;    // ctl[0]: CTAs given to shared prefixes (plan kernel)
     const int32_t *start_s;
+    const int32_t *rowseq; // [V][R] sequence of each query row of each virtual sequence, -1 past
+                           // the group's rows (plan kernel)
     float2 *ml_s;          // shared-prefix pieces: [slot][kPlanSlotRows] (m, l)
     float *acc_s;          //                       [slot][kPlanSlotRows][D]
 };

@@ -341,35 +341,34 @@ __device__ __forceinline__ void shared_prefix_cta(uint8_t *smem, const CUtensorM
     BlockCursor cur;
     cur.init_at(lo, sh.start_s[c], pv.cu_s, V);
     bool seg_start = true, active = false;
-    int32_t grp = 0, rows = 0, row_base = 0;
+    uint32_t row_valid = 0;  // bit i: this warp's row i of the pass belongs to a member
     for (int64_t it = 0; it < n; ++it) {
         const int st = (int)(it % S);
         const uint32_t ph = (uint32_t)((it / S) & 1);
         const int32_t kvh = cur.g * nhb + hb, v = cur.seq;
         if (seg_start) {
-            grp = pv.vgroup[v];
-            rows = (pv.group_begin[grp + 1] - pv.group_begin[grp]) * G;
-            row_base = (v - pv.group_vbase[grp]) * R + sub * kPlanWarpRows;  // this warp's first row
-            active = row_base < rows;
+            // This warp's rows of the pass: sub * 16 .. + 15 (member row / G,
+            // query head row % G); lane i < 16 loads row i's sequence from the
+            // plan kernel's table, then every load of the rows is issued at
+            // once: two round trips per segment.
+            int32_t row_seq = -1;
+            if (lane < kPlanWarpRows) row_seq = sh.rowseq[(int64_t)v * R + sub * kPlanWarpRows + lane];
+            row_valid = __ballot_sync(0xffffffffu, row_seq >= 0) & ((1u << kPlanWarpRows) - 1u);
+            active = row_valid != 0;
             if (active) {
                 // The warp's 16 query rows of its head into shared memory
-                // (zeros past the group's rows): row i = member i / G, head i % G.
-                // Lane i < 16 looks up row i's sequence; every load of the
-                // rows is then issued at once (one round trip, not one per row).
+                // (zeros for rows past the group's).
                 __syncwarp();  // the previous segment's reads of qw are done
-                int32_t row_seq = -1;
-                if (lane < kPlanWarpRows && row_base + lane < rows)
-                    row_seq = pv.members[pv.group_begin[grp] + (row_base + lane) / G];
                 constexpr int kChunks = D / 8;  // 16-byte pieces of a row
                 uint4 val[kPlanWarpRows * kChunks / 32];
 #pragma unroll
                 for (int k = 0; k < kPlanWarpRows * kChunks / 32; ++k) {
                     const int e = lane + 32 * k, i = e / kChunks, ch = e - i * kChunks;
                     const int32_t seq = __shfl_sync(0xffffffffu, row_seq, i);
-                    const int32_t gr = row_base + i;
                     val[k] = make_uint4(0u, 0u, 0u, 0u);
-                    if (seq >= 0) {  // q is 16-byte aligned with a plan
-                        const __nv_bfloat16 *qp = q + ((int64_t)seq * H + (int64_t)kvh * G + gr % G) * D;
+                    if (seq >= 0) {  // q is 16-byte aligned with a plan; passes start on a member
+                        const int hq = (sub * kPlanWarpRows + i) % G;
+                        const __nv_bfloat16 *qp = q + ((int64_t)seq * H + (int64_t)kvh * G + hq) * D;
                         val[k] = *reinterpret_cast<const uint4 *>(qp + ch * 8);
                     }
                 }
@@ -416,7 +415,7 @@ __device__ __forceinline__ void shared_prefix_cta(uint8_t *smem, const CUtensorM
                         lt0 += __shfl_xor_sync(0xffffffffu, lt0, off);
                         lt1 += __shfl_xor_sync(0xffffffffu, lt1, off);
                     }
-                    const bool v0 = row_base + t * 8 + h0 < rows, v1 = row_base + t * 8 + h1 < rows;
+                    const bool v0 = (row_valid >> (t * 8 + h0)) & 1u, v1 = (row_valid >> (t * 8 + h1)) & 1u;
                     float *ab = sh.acc_s + (wrow + t * 8) * D;
 #pragma unroll
                     for (int dm = 0; dm < KT; ++dm) {

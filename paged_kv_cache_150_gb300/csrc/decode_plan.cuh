@@ -81,7 +81,8 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
                                                            const int32_t *__restrict__ plan, int32_t G,
                                                            int32_t Hk, int32_t NH, int32_t *__restrict__ skip,
                                                            int32_t *__restrict__ ctl,
-                                                           int32_t *__restrict__ start_s, int32_t plan_in_smem) {
+                                                           int32_t *__restrict__ start_s,
+                                                           int32_t *__restrict__ rowseq, int32_t plan_in_smem) {
     grid_dependency_wait();     // inputs written by earlier work on the stream
     grid_launch_dependents();   // the attention kernel may become resident now
     constexpr int32_t kSmemCu = 2048;  // prefix sums kept in shared memory for the start search
@@ -227,6 +228,16 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
                     hi = mid - 1;
             }
             start_s[c] = lo;
+        }
+        // The sequence of every query row of every virtual sequence (-1 past
+        // its group's rows), so that a shared-prefix warp finds its rows'
+        // sequences with one load instead of a chain through the plan.
+        const int32_t R = pv.R;
+        for (int32_t e = threadIdx.x; e < pv.V * R; e += blockDim.x) {
+            const int32_t v = e / R, r = e - v * R;
+            const int32_t grp = pv.vgroup[v], gb = pv.group_begin[grp];
+            const int32_t row = (v - pv.group_vbase[grp]) * R + r;
+            rowseq[e] = row < (pv.group_begin[grp + 1] - gb) * G ? pv.members[gb + row / G] : -1;
         }
     }
 }
