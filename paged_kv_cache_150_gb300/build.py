@@ -18,7 +18,7 @@ LIBRARY = os.path.join(HERE, "libpa.so")
 SOURCES = ["decode_mma_shared.cu", "decode_mma_plain.cu", "decode_fma.cu", "decode_simt.cu", "decode.cu", "pa_api.cu",
            "cache_ops.cu", "block_manager.cpp", "simulator.cpp", "shared_plan.cpp"]
 HEADERS = ["pa_common.cuh", "pa_internal.h", "decode_kernels.h", "decode_merge.cuh", "decode_plan.cuh", "decode_simt.cuh",
-           "decode_mma.cuh", "decode_fma.cuh"]
+           "decode_mma.cuh", "decode_tc.cuh", "decode_fma.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

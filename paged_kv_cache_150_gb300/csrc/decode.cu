@@ -70,6 +70,7 @@ struct DecodePlan {
     int HPG;       // query heads per group = NH * G
     int C;         // persistent CTAs
     bool shared;   // a shared-prefix plan is used
+    bool tc;       // its 64-row passes may run on tcgen05 (row layout; the CTAs' tensor memory fits an SM)
     bool local_cu; // tensor-core CTAs compute the prefix sums themselves (kLocalCuMax)
     size_t smem;   // dynamic shared memory of the attention kernel
     // workspace layout (byte offsets)
@@ -130,17 +131,24 @@ bool fma_shape(const pa_cache_desc_t *c, int G, int *NH, int *stages, size_t *sm
     return true;
 }
 
-// kMmaStages stages of NH head slabs of K and of V (the shared-prefix CTAs
-// cut the same ring bytes, NH = kPlanWarps, into their own stages),
-// mbarriers after the tiles, with shared prefixes the query rows of the
-// shared-prefix warps (QRows, 256 bytes after the tiles); 1024 bytes to align
-// the base.
+// kMmaStages stages of NH head slabs of K and of V, mbarriers after the
+// tiles; with a shared-prefix plan two halves of shared_half_bytes (each the
+// largest of the own-block, mma.sync and tcgen05 shared-prefix maps); 1024
+// bytes to align the base.
 size_t mma_smem_bytes(int D, int B, int NH, bool shared) {
     const size_t slab = (size_t)(D / 64) * B * 128;
-    size_t bytes = (size_t)kMmaStages * 2 * NH * slab + 2 * (size_t)kMmaStages * sizeof(uint64_t) + 1024;
-    if (shared) bytes += 256 + (size_t)kPlanWarps * kPlanWarpRows * (D * 2 + 16);  // QRows of the shared-prefix warps
-    return bytes;
+    if (shared) return (size_t)shared_halves(D, B) * shared_half_bytes(D, B) + 1024;  // halves (NH = kPlanWarps)
+    return (size_t)kMmaStages * 2 * NH * slab + 2 * (size_t)kMmaStages * sizeof(uint64_t) + 1024;
 }
+
+// Logical CTAs per CTA of the tensor-core launch (halves with a plan).
+int mma_halves(int D, int B, bool shared) { return shared ? shared_halves(D, B) : 1; }
+// Threads of a tensor-core attention CTA: NH consumer warps and a producer
+// per half.
+int mma_threads(int NH, int halves) { return (NH + 1) * 32 * halves; }
+
+// Tensor-memory columns a tcgen05 shared-prefix CTA allocates (TcSmem::kCols).
+int tc_tmem_cols(int D) { return D == 128 ? 256 : 128; }
 
 // Pieces from which a (sequence, KV head) is merged by long_merge_kernel
 // rather than by the CTA whose piece arrives last.
@@ -260,7 +268,9 @@ pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_d
     }
     p->NG = c->num_kv_heads / p->NH;
     p->HPG = p->NH * G;
-    const int threads = kernel == PA_KERNEL_MMA || p->fma ? (p->NH + 1) * 32 : p->NH * 32;
+    const int threads = kernel == PA_KERNEL_MMA ? mma_threads(p->NH, mma_halves(c->head_dim, c->block_size, p->shared))
+                        : p->fma                ? (p->NH + 1) * 32
+                                                : p->NH * 32;
     const int C_given = opts ? opts->num_splits : 0;
     int C = C_given;
     if (C == 0) {
@@ -270,11 +280,23 @@ pa_status_t make_plan(const pa_cache_desc_t *c, int32_t N, int32_t H, const pa_d
                                               : simt_kernel_ptr(c->dtype, c->head_dim, G, c->layout);
         C = default_ctas(fn, threads, p->smem);
         if (C <= 0) return PA_ERR_CUDA;
+        C *= kernel == PA_KERNEL_MMA ? mma_halves(c->head_dim, c->block_size, p->shared) : 1;  // logical CTAs
     }
     p->C = C;
     if (p->shared && C < 2) {  // shared prefixes need a CTA of each kind
         p->shared = false;
         p->smem = mma_smem_bytes(c->head_dim, c->block_size, p->NH, false);
+    }
+    // tcgen05 shared-prefix halves allocate tensor memory; both halves of
+    // every CTA of the launch that can be resident on one SM must find their
+    // columns (512 per SM), so that an allocation never waits on a CTA of
+    // the same launch.
+    p->tc = false;
+    if (p->shared && c->layout == PA_LAYOUT_ROW) {
+        const void *fn = mma_kernel_ptr(c->head_dim, c->block_size, c->layout, true);
+        const int all = default_ctas(fn, threads, p->smem), sms = num_sms();
+        const int halves = mma_halves(c->head_dim, c->block_size, true);
+        if (all > 0 && sms > 0) p->tc = (all / sms) * halves * tc_tmem_cols(c->head_dim) <= 512;
     }
     // Without a plan, tensor-core CTAs keep their own prefix sums when they
     // fit and the room for them leaves as many CTAs resident per SM (checked
@@ -368,7 +390,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // slab is D*B contiguous elements, viewed as {64, D*B/64, Hk, NB} with strides
 // {128, D*B*2, Hk*D*B*2}, box {64, D*B/64, NH, 1}, no swizzle -> the slab's
 // own byte order in shared memory.
-bool encode_cache_map(CUtensorMap *map, const void *base, const pa_cache_desc_t *c, int NH) {
+bool encode_cache_map(CUtensorMap *map, const void *base, const pa_cache_desc_t *c, int NH, bool one_panel = false) {
     auto fn = encode_fn();
     if (!fn) return false;
     const int D = c->head_dim;
@@ -388,7 +410,7 @@ bool encode_cache_map(CUtensorMap *map, const void *base, const pa_cache_desc_t 
         cuuint64_t dims[4] = {(cuuint64_t)line, (cuuint64_t)c->num_blocks * B, (cuuint64_t)(D / line),
                               (cuuint64_t)c->num_kv_heads};
         cuuint64_t strides[3] = {(cuuint64_t)c->num_kv_heads * D * eb, 128, (cuuint64_t)D * eb};
-        cuuint32_t box[4] = {(cuuint32_t)line, (cuuint32_t)B, (cuuint32_t)(D / line), (cuuint32_t)NH};
+        cuuint32_t box[4] = {(cuuint32_t)line, (cuuint32_t)B, one_panel ? 1u : (cuuint32_t)(D / line), (cuuint32_t)NH};
         r = fn(map, et, 4, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -467,6 +489,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
     if (((uintptr_t)q | (uintptr_t)out) % (size_t)(eb * 2) != 0) return PA_ERR_INVALID_ARG;
     if (p.shared && (uintptr_t)q % 16 != 0) {  // shared-prefix warps read q rows in 16-byte pieces
         p.shared = false;
+        p.tc = false;
         p.smem = mma_smem_bytes(cache->head_dim, cache->block_size, p.NH, false);
     }
     unsigned int *err = device_error_word();
@@ -496,10 +519,11 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         sh.rowseq = (const int32_t *)(ws + p.off_rowseq);
         sh.ml_s = (float2 *)(ws + p.off_ml_s);
         sh.acc_s = (float *)(ws + p.off_acc_s);
+        sh.tc = p.tc ? 1 : 0;
     }
     {
         int32_t Nv = num_seqs, Bv = cache->block_size, ml_v = max_len, HDv = HD, nc = ncnt, NGv = p.NG, Cv = p.C;
-        int32_t Gv = G, Hkv = cache->num_kv_heads, NHv = p.NH;
+        int32_t Gv = G, Hkv = cache->num_kv_heads, NHv = p.NH, tcv = sh.tc;
         void *outp = out;
         const int32_t *planp = sh.plan;
         int32_t *skipp = (int32_t *)sh.skip, *ctlp = (int32_t *)sh.ctl, *start_sp = (int32_t *)sh.start_s;
@@ -514,7 +538,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
             cudaFuncSetAttribute(pfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem) != cudaSuccess)
             return PA_ERR_CUDA;
         void *pargs[] = {&seq_lens, &Nv, &Bv, &ml_v, &HDv, &lens_ws, &cu, &cnt, &nc, &outp, &NGv, &Cv, &start_seq,
-                         &err, &planp, &Gv, &Hkv, &NHv, &skipp, &ctlp, &start_sp, &rowseqp, &in_smem};
+                         &err, &planp, &Gv, &Hkv, &NHv, &skipp, &ctlp, &start_sp, &rowseqp, &in_smem, &tcv};
         if (launch_pdl(pfn, dim3(1), dim3(1024), pargs, psmem, s) != cudaSuccess) return PA_ERR_CUDA;
     }
 
@@ -522,7 +546,9 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         return PA_ERR_CUDA;
     if (p.kernel == PA_KERNEL_MMA) {
         if (((uintptr_t)k_cache | (uintptr_t)v_cache) % 16 != 0) return PA_ERR_INVALID_ARG;
-        CUtensorMap tmk, tmv, tmk1, tmv1;  // NH-head boxes; one-head boxes for the shared-prefix CTAs
+        // NH-head boxes; one-head boxes for the mma.sync shared-prefix CTAs;
+        // one-head, one-panel boxes for the tcgen05 ones
+        CUtensorMap tmk, tmv, tmk1, tmv1, tmkp, tmvp;
         if (!encode_cache_map(&tmk, k_cache, cache, p.NH) || !encode_cache_map(&tmv, v_cache, cache, p.NH))
             return PA_ERR_CUDA;
         if (p.shared) {
@@ -532,10 +558,19 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
             tmk1 = tmk;
             tmv1 = tmv;
         }
+        if (p.tc) {
+            if (!encode_cache_map(&tmkp, k_cache, cache, 1, true) || !encode_cache_map(&tmvp, v_cache, cache, 1, true))
+                return PA_ERR_CUDA;
+        } else {
+            tmkp = tmk1;
+            tmvp = tmv1;
+        }
         const void *fn = mma_kernel_ptr(cache->head_dim, cache->block_size, cache->layout, p.shared);
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
             return PA_ERR_CUDA;
-        const dim3 grid(p.C), block((p.NH + 1) * 32);
+        // with a plan, shared_halves logical CTAs (halves) per CTA
+        const int halves = mma_halves(cache->head_dim, cache->block_size, p.shared);
+        const dim3 grid((p.C + halves - 1) / halves), block(mma_threads(p.NH, halves));
         const __nv_bfloat16 *qb = (const __nv_bfloat16 *)q;
         __nv_bfloat16 *ob = (__nv_bfloat16 *)out;
         int32_t NB = cache->num_blocks, Hk = cache->num_kv_heads, NHv = p.NH, Cv = p.C;
@@ -543,7 +578,7 @@ extern "C" pa_status_t pa_decode(void *out, const void *q, const void *k_cache, 
         float sl = scale_log2;
         int32_t local_cu = p.local_cu ? 1 : 0;
         int32_t min_pieces = call_min_pieces(p, opts, num_seqs, cache->block_size, max_len);
-        void *args[] = {&tmk, &tmv, &tmk1, &tmv1, &qb, &ob, &block_tables, &mb, &lens_ws, &cu, &Nv, &Hv, &Hk,
+        void *args[] = {&tmk, &tmv, &tmk1, &tmv1, &tmkp, &tmvp, &qb, &ob, &block_tables, &mb, &lens_ws, &cu, &Nv, &Hv, &Hk,
                         &Gv, &NB, &NHv, &sl, &Cv, &ml, &acc, &cnt, &start_seq, &err, &sh, &seq_lens, &local_cu,
                         &min_pieces};
         if (launch_pdl(fn, grid, block, args, p.smem, s) != cudaSuccess) return PA_ERR_CUDA;

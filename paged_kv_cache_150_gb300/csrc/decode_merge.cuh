@@ -228,6 +228,7 @@ struct SharedArgs {
                            // the group's rows (plan kernel)
     float2 *ml_s;          // shared-prefix pieces: [slot][kPlanSlotRows] (m, l)
     float *acc_s;          //                       [slot][kPlanSlotRows][D]
+    int32_t tc;            // 1: plans of 64 rows per pass run on tcgen05 (decode_tc.cuh)
 };
 
 // Single-pass merge (after the tensor-core kernel's block loop and in

@@ -23,6 +23,15 @@ struct MmaTile {
     static constexpr int kStages = kMmaStages;
 };
 
+// Barrier of one CTA, or of one half of a two-half CTA (named barrier
+// 1 + half over its 32 * (kMmaMaxHeads + 1) threads; 0: the whole CTA).
+__device__ __forceinline__ void cta_sync(uint32_t bar) {
+    if (bar == 0)
+        __syncthreads();
+    else
+        asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(32 * (kMmaMaxHeads + 1)) : "memory");
+}
+
 __device__ __forceinline__ uint32_t swz_addr(uint32_t slab, int line, int chunk) {
     return slab + (uint32_t)line * 128u + ((uint32_t)(chunk ^ (line & 7)) << 4);
 }
@@ -210,6 +219,92 @@ __device__ __forceinline__ void mma_block_tiles(uint32_t kslab, uint32_t vslab, 
     }
 }
 
+// The TMA producer of a shared-prefix CTA (one thread): its range [lo, lo + n)
+// of the flattened (stage head group, virtual sequence, block) list through a
+// ring of S stages of stage_bytes, nhb one-head boxes of K then of V per
+// stage (tile_bytes each).  Each block is read through the table row of its
+// group's first member.
+template <int D, int B, int LAYOUT>
+__device__ __forceinline__ void shared_prefix_producer(uint8_t *smem, uint64_t *full, uint64_t *empty, int S,
+                                                       uint32_t stage_bytes, uint32_t tile_bytes, int32_t nhb,
+                                                       const CUtensorMap *tmk1, const CUtensorMap *tmv1,
+                                                       const int32_t *__restrict__ tables, int32_t max_blocks,
+                                                       int32_t NB, const PlanView &pv, const SharedArgs &sh,
+                                                       int32_t c, int64_t lo, int64_t n,
+                                                       unsigned int *__restrict__ err) {
+    using Tile = MmaTile<D, B>;
+    const int32_t V = pv.V;
+    prefetch_tmap(tmk1);
+    prefetch_tmap(tmv1);
+    const uint64_t kv_policy = l2_policy_evict_first();  // a pass streams each shared block once
+    BlockCursor cur, ahead;
+    cur.init_at(lo, sh.start_s[c], pv.cu_s, V);
+    ahead.init_at(lo, sh.start_s[c], pv.cu_s, V);
+    // table row of a virtual sequence: its group's first member
+    auto rep_row = [&](int32_t v) {
+        return (int64_t)pv.members[pv.group_begin[pv.vgroup[v]]] * max_blocks;
+    };
+    int32_t ahead_v = ahead.seq;
+    int64_t ahead_row = rep_row(ahead_v);
+    constexpr int PD = kTablePrefetch;
+    int32_t ring[PD];
+#pragma unroll
+    for (int j = 0; j < PD; ++j) {
+        if (j < n) {
+            if (ahead.seq != ahead_v) {
+                ahead_v = ahead.seq;
+                ahead_row = rep_row(ahead_v);
+            }
+            ring[j] = tables[ahead_row + ahead.blk];
+            ahead.advance(pv.cu_s, V);
+        } else {
+            ring[j] = 0;
+        }
+    }
+    int64_t issued = 0;
+    for (; issued < n; ++issued) {
+        const int st = (int)(issued % S);
+        const uint32_t ph = (uint32_t)((issued / S) & 1);
+        int32_t phys = ring[0];
+#pragma unroll
+        for (int j = 0; j + 1 < PD; ++j) ring[j] = ring[j + 1];
+        if (issued + PD < n) {
+            if (ahead.seq != ahead_v) {
+                ahead_v = ahead.seq;
+                ahead_row = rep_row(ahead_v);
+            }
+            ring[PD - 1] = tables[ahead_row + ahead.blk];
+            ahead.advance(pv.cu_s, V);
+        }
+        if (issued >= S && !mbar_wait_bounded(smem_u32(&empty[st]), ph ^ 1u)) {
+            atomicOr(err, kErrTimeout);
+            break;
+        }
+        if (phys < 0 || phys >= NB) {  // read zeros: the box lies past the pool
+            atomicOr(err, kErrBounds);
+            phys = NB;
+        }
+        const uint32_t fb = smem_u32(&full[st]);
+        const uint32_t dst = smem_u32(smem + (size_t)st * stage_bytes);
+        mbar_arrive_expect_tx(fb, stage_bytes);
+        for (int32_t h = 0; h < nhb; ++h) {  // nhb one-head boxes land as one nhb-head box would
+            const int32_t head = cur.g * nhb + h;
+            const uint32_t off = (uint32_t)h * Tile::kSlabBytes;
+            if (LAYOUT == PA_LAYOUT_ROW) {
+                tma_load_4d_hint(dst + off, tmk1, fb, 0, phys * B, 0, head, kv_policy);
+                tma_load_4d_hint(dst + tile_bytes + off, tmv1, fb, 0, phys * B, 0, head, kv_policy);
+            } else {
+                tma_load_4d_hint(dst + off, tmk1, fb, 0, 0, head, phys, kv_policy);
+                tma_load_4d_hint(dst + tile_bytes + off, tmv1, fb, 0, 0, head, phys, kv_policy);
+            }
+        }
+        cur.advance(pv.cu_s, V);
+    }
+    // Let every copy still in flight land before the CTA may exit.
+    for (int64_t j = issued > S ? issued - S : 0; j < issued; ++j)
+        mbar_wait_bounded(smem_u32(&full[j % S]), (uint32_t)((j / S) & 1));
+}
+
 // A CTA of the shared-prefix part.  Its range of the flattened (stage head
 // group hg, virtual sequence v, block) list: W_s = (Hk / nhb) * cu_s[V]
 // entries cut over Ce_s CTAs, nhb = plan_stage_heads(R) KV heads per stage.
@@ -227,7 +322,8 @@ __device__ __forceinline__ void shared_prefix_cta(uint8_t *smem, const CUtensorM
                                                   const __nv_bfloat16 *__restrict__ q,
                                                   const int32_t *__restrict__ tables, int32_t max_blocks, int32_t H,
                                                   int32_t G, int32_t NB, float scale_log2, int32_t Hk, int32_t Cs,
-                                                  const SharedArgs &sh, unsigned int *__restrict__ err) {
+                                                  const SharedArgs &sh, unsigned int *__restrict__ err, int32_t cta,
+                                                  int tid, uint32_t bar) {
     using Tile = MmaTile<D, B>;
     constexpr int KT = D / 16;
     constexpr int NT = kPlanWarpRows / 8;  // MMA tiles per warp
@@ -240,95 +336,27 @@ __device__ __forceinline__ void shared_prefix_cta(uint8_t *smem, const CUtensorM
     uint64_t *full = (uint64_t *)(smem + ring_bytes);
     uint64_t *empty = full + S;                     // 2 * S <= 16 barriers in the 256 bytes after the ring
     uint8_t *qbuf = smem + ring_bytes + 256;        // QRows of each consumer warp
-    const int32_t c = blockIdx.x;
+    const int32_t c = cta;
     if (c >= sv.Ce_s) return;
     const int64_t lo = split_begin(c, sv.Ws, sv.Ce_s), hi = split_begin(c + 1, sv.Ws, sv.Ce_s);
     const int64_t n = hi - lo;
     const int32_t V = pv.V;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = tid >> 5, lane = tid & 31;
 
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         for (int st = 0; st < S; ++st) {
             mbar_init(smem_u32(&full[st]), 1);
             mbar_init(smem_u32(&empty[st]), (uint32_t)kPlanWarps);
         }
         fence_mbarrier_init();
     }
-    __syncthreads();
+    cta_sync(bar);
 
     if (warp == kPlanWarps) {
         // ------------------------------------------------------- producer
-        if (lane == 0) {
-            prefetch_tmap(tmk1);
-            prefetch_tmap(tmv1);
-            const uint64_t kv_policy = l2_policy_evict_first();  // a pass streams each shared block once
-            BlockCursor cur, ahead;
-            cur.init_at(lo, sh.start_s[c], pv.cu_s, V);
-            ahead.init_at(lo, sh.start_s[c], pv.cu_s, V);
-            // table row of a virtual sequence: its group's first member
-            auto rep_row = [&](int32_t v) {
-                return (int64_t)pv.members[pv.group_begin[pv.vgroup[v]]] * max_blocks;
-            };
-            int32_t ahead_v = ahead.seq;
-            int64_t ahead_row = rep_row(ahead_v);
-            constexpr int PD = kTablePrefetch;
-            int32_t ring[PD];
-#pragma unroll
-            for (int j = 0; j < PD; ++j) {
-                if (j < n) {
-                    if (ahead.seq != ahead_v) {
-                        ahead_v = ahead.seq;
-                        ahead_row = rep_row(ahead_v);
-                    }
-                    ring[j] = tables[ahead_row + ahead.blk];
-                    ahead.advance(pv.cu_s, V);
-                } else {
-                    ring[j] = 0;
-                }
-            }
-            int64_t issued = 0;
-            for (; issued < n; ++issued) {
-                const int st = (int)(issued % S);
-                const uint32_t ph = (uint32_t)((issued / S) & 1);
-                int32_t phys = ring[0];
-#pragma unroll
-                for (int j = 0; j + 1 < PD; ++j) ring[j] = ring[j + 1];
-                if (issued + PD < n) {
-                    if (ahead.seq != ahead_v) {
-                        ahead_v = ahead.seq;
-                        ahead_row = rep_row(ahead_v);
-                    }
-                    ring[PD - 1] = tables[ahead_row + ahead.blk];
-                    ahead.advance(pv.cu_s, V);
-                }
-                if (issued >= S && !mbar_wait_bounded(smem_u32(&empty[st]), ph ^ 1u)) {
-                    atomicOr(err, kErrTimeout);
-                    break;
-                }
-                if (phys < 0 || phys >= NB) {  // read zeros: the box lies past the pool
-                    atomicOr(err, kErrBounds);
-                    phys = NB;
-                }
-                const uint32_t fb = smem_u32(&full[st]);
-                const uint32_t dst = smem_u32(smem + (size_t)st * stage_bytes);
-                mbar_arrive_expect_tx(fb, stage_bytes);
-                for (int32_t h = 0; h < nhb; ++h) {  // nhb one-head boxes land as one nhb-head box would
-                    const int32_t head = cur.g * nhb + h;
-                    const uint32_t off = (uint32_t)h * Tile::kSlabBytes;
-                    if (LAYOUT == PA_LAYOUT_ROW) {
-                        tma_load_4d_hint(dst + off, tmk1, fb, 0, phys * B, 0, head, kv_policy);
-                        tma_load_4d_hint(dst + tile_bytes + off, tmv1, fb, 0, phys * B, 0, head, kv_policy);
-                    } else {
-                        tma_load_4d_hint(dst + off, tmk1, fb, 0, 0, head, phys, kv_policy);
-                        tma_load_4d_hint(dst + tile_bytes + off, tmv1, fb, 0, 0, head, phys, kv_policy);
-                    }
-                }
-                cur.advance(pv.cu_s, V);
-            }
-            // Let every copy still in flight land before the CTA may exit.
-            for (int64_t j = issued > S ? issued - S : 0; j < issued; ++j)
-                mbar_wait_bounded(smem_u32(&full[j % S]), (uint32_t)((j / S) & 1));
-        }
+        if (lane == 0)
+            shared_prefix_producer<D, B, LAYOUT>(smem, full, empty, S, stage_bytes, tile_bytes, nhb, tmk1, tmv1, tables,
+                                                 max_blocks, NB, pv, sh, c, lo, n, err);
         return;
     }
 
@@ -455,7 +483,8 @@ __device__ __forceinline__ void own_block_cta(
     const int32_t *__restrict__ lens, const int32_t *cu, int32_t N, int32_t H, int32_t G, int32_t NB,
     int32_t NH, float scale_log2, float2 *__restrict__ ml_ws, float *__restrict__ acc_ws,
     unsigned int *__restrict__ counters, const int32_t *__restrict__ start_seq, int32_t Hk, int32_t C,
-    int32_t Cs, const SharedArgs &sh, unsigned int *__restrict__ err, int32_t min_pieces) {
+    int32_t Cs, const SharedArgs &sh, unsigned int *__restrict__ err, int32_t min_pieces, int32_t cta, int tid,
+    uint32_t bar) {
     using Tile = MmaTile<D, B>;
     constexpr int S = Tile::kStages;
     constexpr int KT = D / 16;  // k-steps of q.k and m-tiles of O^T
@@ -466,18 +495,20 @@ __device__ __forceinline__ void own_block_cta(
     const int32_t *skip = kShared && Cs > 0 ? sh.skip : nullptr;  // nullptr without shared prefixes
     const int64_t W = (int64_t)(Hk / NH) * cu[N];
     const int32_t Ce = (int32_t)(W < (int64_t)(C - Cs) ? W : (int64_t)(C - Cs));  // no CTA with an empty range
-    const int32_t c = (int32_t)blockIdx.x - Cs;
+    const int32_t c = cta - Cs;
     if (c >= Ce) return;
     const int64_t lo = split_begin(c, W, Ce), hi = split_begin(c + 1, W, Ce);
     const int64_t n = hi - lo;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = tid >> 5, lane = tid & 31;
     // Sequences whose merge falls to a consumer warp, done after its block
     // loop where the loop's registers are free for the pieces' loads.  Only
     // the first and the last segment of a range are pieces: at most two.
-    __shared__ int32_t pending[kMmaMaxHeads][2];
-    if (threadIdx.x < 2 * kMmaMaxHeads) pending[threadIdx.x >> 1][threadIdx.x & 1] = -1;
+    // One table per half of a two-half CTA.
+    __shared__ int32_t pending_tab[kShared ? 2 : 1][kMmaMaxHeads][2];
+    int32_t(&pending)[kMmaMaxHeads][2] = pending_tab[kShared && bar == 2 ? 1 : 0];
+    if (tid < 2 * kMmaMaxHeads) pending[tid >> 1][tid & 1] = -1;
 
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
@@ -485,7 +516,7 @@ __device__ __forceinline__ void own_block_cta(
         }
         fence_mbarrier_init();
     }
-    __syncthreads();
+    cta_sync(bar);
 
     if (warp == NH) {
         // ------------------------------------------------------- producer
@@ -778,15 +809,28 @@ __device__ __forceinline__ void local_prefix_sums(const int32_t *__restrict__ se
     __syncthreads();
 }
 
+}  // namespace pa
+
+#include "decode_tc.cuh"  // the tcgen05 shared-prefix CTA
+
+namespace pa {
+
 // The attention launch.  Without a plan (kShared = false) every CTA is an
-// own-block CTA.  With one, the plan kernel gives CTAs [0, Cs) to the shared
-// prefixes and the rest to the sequences' own blocks; both kinds run at once
-// and meet only at the arrival counters.  tmk / tmv hold NH-head boxes (the
-// own-block CTAs'), tmk1 / tmv1 one-head boxes (the shared-prefix CTAs').
+// own-block CTA (two resident per SM at block size 16).  With one, each CTA
+// is shared_halves(D, B) halves of 32 * (kMmaMaxHeads + 1) threads and
+// shared_half_bytes of shared memory, one logical CTA each (halves * blockIdx
+// + half): a kernel that holds tcgen05 instructions is resident once per SM,
+// so two halves keep two logical CTAs per SM where they fit.  The plan kernel gives logical CTAs [0, Cs) to the shared prefixes
+// and the rest to the sequences' own blocks; both kinds run at once and meet
+// only at the arrival counters.  tmk / tmv hold NH-head boxes (the own-block
+// CTAs'), tmk1 / tmv1 one-head boxes (the mma.sync shared-prefix CTAs'),
+// tmkp / tmvp one-head, one-panel boxes (the tcgen05 ones').
 template <int D, int B, int LAYOUT, bool kShared>
-__global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
+__global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1) * (kShared ? shared_halves(D, B) : 1), kShared ? 1 : 2)
+    decode_mma_kernel(
     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
     const __grid_constant__ CUtensorMap tmk1, const __grid_constant__ CUtensorMap tmv1,
+    const __grid_constant__ CUtensorMap tmkp, const __grid_constant__ CUtensorMap tmvp,
     const __nv_bfloat16 *__restrict__ q, __nv_bfloat16 *__restrict__ out,
     const int32_t *__restrict__ tables, int32_t max_blocks, const int32_t *__restrict__ lens,
     const int32_t *__restrict__ cu, int32_t N, int32_t H, int32_t Hk, int32_t G, int32_t NB,
@@ -817,14 +861,32 @@ __global__ void __launch_bounds__(32 * (kMmaMaxHeads + 1), 2) decode_mma_kernel(
     // With a plan or with long sequences, the merge kernel that follows may
     // become resident now and wait for this launch there.
     if (kShared || min_pieces > 0) grid_launch_dependents();
-    const int32_t Cs = kShared ? sh.ctl[0] : 0;
-    if (kShared && (int32_t)blockIdx.x < Cs)
-        shared_prefix_cta<D, B, LAYOUT>(smem, &tmk1, &tmv1, q, tables, max_blocks, H, G, NB, scale_log2, Hk, Cs, sh,
-                                        err);
-    else
-        own_block_cta<D, B, LAYOUT, kShared>(smem, &tmk, &tmv, q, out, tables, max_blocks, lens_p, cu_p, N, H, G,
-                                             NB, NH, scale_log2, ml_ws, acc_ws, counters, start_p, Hk, C, Cs, sh,
-                                             err, kShared ? 0 : min_pieces);
+    if constexpr (kShared) {
+        const int32_t Cs = sh.ctl[0];
+        constexpr int kHalf = 32 * (kMmaMaxHeads + 1);
+        const int half = (int)threadIdx.x / kHalf, tid = (int)threadIdx.x - half * kHalf;
+        const int32_t cta = shared_halves(D, B) * (int32_t)blockIdx.x + half;
+        uint8_t *hs = smem + (size_t)half * shared_half_bytes(D, B);
+        const uint32_t bar = 1u + (uint32_t)half;
+        if (cta < Cs) {
+            bool tc = false;
+            if constexpr (LAYOUT == PA_LAYOUT_ROW) tc = sh.tc != 0 && sh.plan[7] == kPlanSlotRows;
+            if (tc)
+                shared_prefix_cta_tc<D, B>(hs, &tmkp, &tmvp, q, tables, max_blocks, H, G, NB, scale_log2, Hk, Cs, sh,
+                                           err, cta, tid, bar, half);
+            else
+                shared_prefix_cta<D, B, LAYOUT>(hs, &tmk1, &tmv1, q, tables, max_blocks, H, G, NB, scale_log2, Hk,
+                                                Cs, sh, err, cta, tid, bar);
+        } else {
+            own_block_cta<D, B, LAYOUT, true>(hs, &tmk, &tmv, q, out, tables, max_blocks, lens_p, cu_p, N, H, G, NB,
+                                              NH, scale_log2, ml_ws, acc_ws, counters, start_p, Hk, C, Cs, sh, err, 0,
+                                              cta, tid, bar);
+        }
+    } else {
+        own_block_cta<D, B, LAYOUT, false>(smem, &tmk, &tmv, q, out, tables, max_blocks, lens_p, cu_p, N, H, G, NB,
+                                           NH, scale_log2, ml_ws, acc_ws, counters, start_p, Hk, C, 0, sh, err,
+                                           min_pieces, (int32_t)blockIdx.x, (int)threadIdx.x, 0u);
+    }
     // The grid ends after the plan kernel (which also writes the zero output
     // of empty sequences), as a grid that waited at its start does.
     if (local) grid_dependency_wait();

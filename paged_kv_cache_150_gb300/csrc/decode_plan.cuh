@@ -82,7 +82,8 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
                                                            int32_t Hk, int32_t NH, int32_t *__restrict__ skip,
                                                            int32_t *__restrict__ ctl,
                                                            int32_t *__restrict__ start_s,
-                                                           int32_t *__restrict__ rowseq, int32_t plan_in_smem) {
+                                                           int32_t *__restrict__ rowseq, int32_t plan_in_smem,
+                                                           int32_t tc) {
     grid_dependency_wait();     // inputs written by earlier work on the stream
     grid_launch_dependents();   // the attention kernel may become resident now
     constexpr int32_t kSmemCu = 2048;  // prefix sums kept in shared memory for the start search
@@ -175,13 +176,15 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
         if (cu_in_smem) cu_s[N] = carry;
         // CTAs for the shared prefixes, in proportion to the stages each side
         // streams (a shared-prefix stage holds plan_stage_heads(R) KV heads,
-        // an own-block stage NH).  Measured on the prefix workload: a stage
-        // takes about the same time on either side, whatever the heads in it,
-        // since its consumers' work (16 query rows per warp), not its bytes,
-        // sets it.
+        // an own-block stage NH).  Measured on the prefix workload: with
+        // mma.sync consumers a stage takes about the same time on either
+        // side, whatever the heads in it, since its consumers' work (16 query
+        // rows per warp), not its bytes, sets it; a one-head stage of the
+        // tcgen05 CTAs weighs kTcStageWeight of an own-block stage.
         int32_t cs = 0;
         if (plan_ok) {
-            const double Ws = (double)(Hk / plan_stage_heads(pv.R)) * pv.cu_s[pv.V], Wo = (double)NG * carry;
+            const double w = tc && pv.R == kPlanSlotRows ? (double)kTcStageWeight : 1.0;
+            const double Ws = w * (Hk / plan_stage_heads(pv.R)) * pv.cu_s[pv.V], Wo = (double)NG * carry;
             if (Ws > 0) {
                 const double share = Ws / (Ws + Wo);
                 cs = (int32_t)((double)C * share + 0.5);

@@ -85,6 +85,32 @@ constexpr int kPlanWarps = 4;                               // consumer warps of
 constexpr int kPlanWarpRows = 16;                           // query rows of one consumer warp
 constexpr int kPlanSlotRows = kPlanWarps * kPlanWarpRows;   // rows of one shared-prefix partial slot
 
+// Relative cost of a one-head shared-prefix stage on tcgen05 against an
+// own-block stage of the same launch (the CTA split of the plan kernel).
+constexpr float kTcStageWeight = 0.4f;
+
+// Shared memory of one half of a two-half CTA of the shared-plan attention
+// launch (1024-byte multiple): the largest of the own-block map (the ring of
+// kMmaStages stages of kPlanWarps heads, barriers), the mma.sync
+// shared-prefix map (the same ring, 256 bytes of barriers, 16 query rows of
+// D + 8 elements per consumer warp) and the tcgen05 one (64 x 64 bf16
+// probabilities, 64 query rows of D, two rounds of 64 tokens of K and V,
+// barriers).
+__host__ __device__ constexpr uint32_t shared_half_bytes(int D, int B) {
+    const uint32_t slab = (uint32_t)(D / 64) * (uint32_t)B * 128u;
+    const uint32_t ring = (uint32_t)kMmaStages * 2u * (uint32_t)kPlanWarps * slab;
+    const uint32_t own = ring + 2u * (uint32_t)kMmaStages * 8u;
+    const uint32_t mma = ring + 256u + (uint32_t)kPlanWarps * (uint32_t)kPlanWarpRows * (uint32_t)(D * 2 + 16);
+    const uint32_t tc = 64u * 64u * 2u + 64u * (uint32_t)D * 2u + 2u * (2u * 64u * (uint32_t)D * 2u) + 256u;
+    const uint32_t m = own > mma ? (own > tc ? own : tc) : (mma > tc ? mma : tc);
+    return (m + 1023u) & ~1023u;
+}
+// Halves per CTA of the shared-plan launch: two when both fit the 227 KiB a
+// CTA may hold (block size 16, and head_dim 64 at 32), else one.
+__host__ __device__ constexpr int shared_halves(int D, int B) {
+    return 2u * shared_half_bytes(D, B) + 1024u <= 227u * 1024u ? 2 : 1;
+}
+
 // Rows per pass R that a plan may carry, and the KV heads of a stage for it.
 __host__ __device__ __forceinline__ bool plan_rows_ok(int32_t R) { return R == 16 || R == 32 || R == 64; }
 __host__ __device__ __forceinline__ int32_t plan_stage_heads(int32_t R) { return kPlanSlotRows / R; }

@@ -18,7 +18,9 @@ pytestmark = pytest.mark.gpu
 
 # (name, prompts, prompt_len, samples, max_append, H, Hk, D, B).  Rows per KV
 # head = samples x query heads per KV head; the plan's rows per pass R is the
-# smallest of 16, 32, 64 holding them (4, 2 or 1 KV heads per stage).
+# smallest of 16, 32, 64 holding them (4, 2 or 1 KV heads per stage).  Passes
+# of 64 rows in the row layout run on tcgen05 (accumulators in tensor
+# memory), the others on mma.sync.
 SAMPLING = [
     ("g4-s4", 6, 200, 4, 40, 32, 8, 128, 16),     # the parallel-sampling shape, reduced: 16 rows, R 16
     ("g8-s4", 4, 150, 4, 30, 64, 8, 128, 16),     # 8 query heads per KV head: 32 rows, R 32 (2 heads per stage)
@@ -28,6 +30,9 @@ SAMPLING = [
     ("g4-s9-b32", 3, 64, 9, 10, 16, 4, 64, 32),   # 36 rows, R 64, head_dim 64, block 32
     ("g2-s4", 3, 80, 4, 12, 16, 8, 128, 16),      # 8 rows: R 16, the second MMA tile empty
     ("g8-s9", 2, 120, 9, 20, 64, 8, 128, 16),     # 72 rows: R 64, two passes, the second on one warp
+    ("g4-s12-b32", 2, 200, 12, 30, 32, 8, 128, 32),  # 48 rows, R 64, block size 32: rounds of 2 blocks
+    ("g2-s20-d64", 2, 150, 20, 20, 16, 8, 64, 16),  # 40 rows, R 64, head_dim 64
+    ("g1-s64", 1, 700, 64, 9, 8, 8, 128, 16),     # 64 rows, R 64, 43 shared blocks: full rounds and a ragged one
 ]
 
 
@@ -58,12 +63,47 @@ def test_shared_prefix_any_split_count(splits):
     assert max_abs_err(g["out"], ref) <= TOL["bf16"]
 
 
-def test_shared_prefix_split_layout():
-    wl = _sampling(*SAMPLING[0])
+@pytest.mark.parametrize("idx", [0, 2], ids=["R16", "R64"])
+def test_shared_prefix_split_layout(idx):
+    wl = _sampling(*SAMPLING[idx])
     dev, host = host_values(wl, "cpu", layout="split")
     r = oracle_step(wl, host)
     g = gpu_step(wl, dev, shared=True)
     assert max_abs_err(g["out"], oracle_decode(wl, host, r)) <= TOL["bf16"]
+
+
+def _growing_scores(wl, step):
+    """Values whose cached keys grow with their position in the sequence
+    (factor 1 + position / step), so that the scores of later shared blocks
+    pass the running maximum of earlier ones many times over: the online
+    softmax must rescale its accumulators in the middle of a prefix."""
+    vals = inputs.make_values(wl, device="cpu")
+    r = oracle.run_script(wl.num_blocks, wl.block_size, wl.free_order, wl.script)
+    kc = vals["k_cache"].float()
+    seen = set()
+    for table in r["tables"]:
+        for b, blk in enumerate(table):
+            if blk not in seen:
+                seen.add(blk)
+                f = 1.0 + (b * wl.block_size + torch.arange(wl.block_size, dtype=torch.float32)) / step
+                kc[blk] *= f[:, None, None]
+    vals["k_cache"] = kc.to(vals["k_cache"].dtype)
+    dev = {n: v.to("cuda") for n, v in vals.items()}
+    host = {n: inputs.to_numpy_elems(v).copy() for n, v in vals.items()}
+    return dev, host
+
+
+@pytest.mark.parametrize("idx", [0, 2, 10], ids=["R16", "R64", "R64-43-blocks"])
+def test_shared_prefix_scores_growing_along_the_prefix(idx):
+    spec = SAMPLING[idx]
+    wl = _sampling(*spec)
+    dev, host = _growing_scores(wl, 24.0)
+    r = oracle_step(wl, host)
+    ref = oracle_decode(wl, host, r)
+    g = gpu_step(wl, {k: v.clone() for k, v in dev.items()}, shared=True)
+    assert max_abs_err(g["out"], ref) <= TOL["bf16"]
+    plain = gpu_step(wl, dev)
+    assert max_abs_err(plain["out"], ref) <= TOL["bf16"]
 
 
 @pytest.mark.parametrize("cfg,kw", [("cfg3", {"small": True}), ("cfg3", {"small": True, "prompt_len": 200}),
