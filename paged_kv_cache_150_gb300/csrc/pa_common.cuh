@@ -87,7 +87,7 @@ constexpr int kPlanSlotRows = kPlanWarps * kPlanWarpRows;   // rows of one share
 
 // Relative cost of a one-head shared-prefix stage on tcgen05 against an
 // own-block stage of the same launch (the CTA split of the plan kernel).
-constexpr float kTcStageWeight = 0.4f;
+constexpr float kTcStageWeight = 0.6f;
 
 // Shared memory of one half of a two-half CTA of the shared-plan attention
 // launch (1024-byte multiple): the largest of the own-block map (the ring of
