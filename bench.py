@@ -338,7 +338,7 @@ def source_sha():
     h = hashlib.sha256()
     for f in ("decode.cu", "decode_mma_plain.cu", "decode_mma_shared.cu", "decode_simt.cu", "decode_fma.cu",
               "decode_kernels.h", "decode_merge.cuh", "decode_plan.cuh", "decode_simt.cuh", "decode_mma.cuh",
-              "decode_fma.cuh", "pa_common.cuh"):
+              "decode_fma.cuh", "decode_tc.cuh", "pa_common.cuh"):
         h.update(open(os.path.join(ROOT, "paged_kv_cache_150_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
