@@ -280,6 +280,10 @@ pa_status_t pa_decode_no_alloc(void *out, const void *q, const void *k_cache, co
  * The tensor-core kernel uses the plan when Hk is a multiple of 4, the launch
  * has at least 2 CTAs and q is 16-byte aligned; otherwise (and in the
  * CUDA-core kernel) the plan is ignored and the call runs without sharing.
+ * In the row layout, plans of 64 query rows per pass (groups of more than 32
+ * rows) run their shared blocks as tcgen05 MMAs with the accumulators in
+ * tensor memory; such a call's attention CTAs each hold two halves of the
+ * usual size (a kernel with tcgen05 instructions is resident once per SM).
  * ---------------------------------------------------------------------- */
 typedef struct pa_shared_plan_info {
     int32_t num_groups;    /* groups of >= 2 sequences sharing a prefix */
