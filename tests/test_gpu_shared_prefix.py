@@ -53,9 +53,12 @@ def test_shared_prefix_decode_matches_oracle(spec):
     assert (g["out"].float() - plain["out"].float()).abs().max().item() <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("idx", [0, 10], ids=["R16", "R64"])
 @pytest.mark.parametrize("splits", [2, 3, 7, 64, 0])
-def test_shared_prefix_any_split_count(splits):
-    wl = _sampling(*SAMPLING[0])
+def test_shared_prefix_any_split_count(splits, idx):
+    """Any split count: with 64-row passes (tcgen05 halves) odd counts leave
+    a CTA whose halves are of different kinds, or a half with nothing to do."""
+    wl = _sampling(*SAMPLING[idx])
     dev, host = host_values(wl, "cpu")
     r = oracle_step(wl, host)
     ref = oracle_decode(wl, host, r)
