@@ -304,6 +304,17 @@ pa_status_t pa_shared_plan_build(const int32_t *block_tables, int32_t max_blocks
 int32_t pa_decode_default_splits(const pa_cache_desc_t *cache, int32_t num_heads,
                                  const pa_decode_opts_t *opts);
 
+/* 1 when a pa_decode call with these arguments (opts->shared_plan set) runs
+ * the passes of 64 query rows of its shared prefixes as tcgen05 MMAs with the
+ * accumulators in tensor memory, 0 when it would run them on mma.sync (no
+ * plan, the split layout, or a tensor-memory budget that does not fit an
+ * SM), or a negative pa_status_t.  Plans of 16 or 32 rows per pass always
+ * run on mma.sync; the plan's rows per pass are read on the device, so this
+ * host-only query does not look at them ("10 PagedAttention" (PidokuInfra),
+ * section 5 "The relationship to prefix caching").  Launches nothing. */
+int32_t pa_decode_shared_tc(const pa_cache_desc_t *cache, int32_t num_seqs, int32_t num_heads,
+                            const pa_decode_opts_t *opts);
+
 /* Kernels that one pa_decode call with these arguments launches on the
  * current device (its plan kernel, the attention kernel and the merge
  * kernels its options bring in), assuming q is 16-byte aligned; or a

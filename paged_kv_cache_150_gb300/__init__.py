@@ -196,6 +196,18 @@ def pa_decode_default_splits(k_cache, num_heads, kernel="auto"):
     return int(n)
 
 
+def pa_decode_shared_tc(k_cache, num_seqs, num_heads, shared_plan, num_splits=0):
+    """True when pa_decode with this device plan would run its 64-row shared
+    passes on tcgen05 (host-side choice; plans of 16 or 32 rows per pass run
+    on mma.sync whatever this says)."""
+    desc = _cache_desc_from_k(k_cache)
+    o = _opts(num_splits, "auto", None, shared_plan, _current_device())
+    n = _lib.load().pa_decode_shared_tc(ctypes.byref(desc), int(num_seqs), int(num_heads), ctypes.byref(o))
+    if n < 0:
+        raise PagedAttentionError("pa_decode_shared_tc", n)
+    return n == 1
+
+
 def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None, workspace=None,
               num_splits=0, kernel="auto", events=None, shared_plan=None, host_seq_lens=None):
     """Decode attention through block tables; returns ``out`` [N, H, D].
@@ -528,7 +540,7 @@ def version():
 
 __all__ = [
     "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_workspace_bytes", "pa_decode_no_alloc",
-    "pa_decode_default_splits", "pa_decode_launch_count", "pa_get_device_error", "pa_selftest_wait_timeout",
+    "pa_decode_default_splits", "pa_decode_shared_tc", "pa_decode_launch_count", "pa_get_device_error", "pa_selftest_wait_timeout",
     "pa_split_range", "pa_split_owner",
     "BlockManager", "PagedAttentionError", "sampling_memory", "simulate", "version",
 ]

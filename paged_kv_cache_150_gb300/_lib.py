@@ -83,6 +83,7 @@ SIGNATURES = {
     "pa_decode": (_I32, [_P, _P, _P, _P, _DESC, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P,
                          ctypes.c_size_t, _OPTS, _P]),
     "pa_decode_default_splits": (_I32, [_DESC, _I32, _OPTS]),
+    "pa_decode_shared_tc": (_I32, [_DESC, _I32, _I32, _OPTS]),
     "pa_decode_launch_count": (_I32, [_DESC, _I32, _I32, _I32, _OPTS]),
     "pa_decode_no_alloc": (_I32, [_P, _P, _P, _P, _DESC, _P, _I32, _P, _I32, _I32, ctypes.c_float, _OPTS, _P]),
     "pa_split_range": (None, [_I64, _I32, _I32, _PI64, _PI64]),

@@ -447,6 +447,16 @@ extern "C" int32_t pa_decode_launch_count(const pa_cache_desc_t *cache, int32_t 
     return (int32_t)host_failure();
 }
 
+extern "C" int32_t pa_decode_shared_tc(const pa_cache_desc_t *cache, int32_t num_seqs, int32_t num_heads,
+                                       const pa_decode_opts_t *opts) try {
+    DecodePlan p;
+    const pa_status_t st = make_plan(cache, num_seqs, num_heads, opts, true, &p);
+    if (st != PA_OK) return (int32_t)st;
+    return p.shared && p.tc ? 1 : 0;
+} catch (...) {
+    return (int32_t)host_failure();
+}
+
 extern "C" int32_t pa_decode_default_splits(const pa_cache_desc_t *cache, int32_t num_heads,
                                             const pa_decode_opts_t *opts) try {
     pa_decode_opts_t o = opts ? *opts : pa_decode_opts_t{0, PA_KERNEL_AUTO, nullptr, nullptr, nullptr, nullptr};

@@ -252,3 +252,23 @@ def test_shared_prefix_plan_too_large_for_shared_memory():
     g = gpu_step(wl, dev, shared=True)
     assert g["plan_info"]["num_groups"] == 1000
     assert max_abs_err(g["out"], oracle_decode(wl, host, r)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("idx,layout", [(2, "row"), (8, "row"), (9, "row"), (2, "split")],
+                         ids=["d128-b16", "d128-b32", "d64-b16", "split"])
+def test_64_row_passes_choose_tcgen05_in_the_row_layout(idx, layout):
+    """The host chooses the tcgen05 shared-prefix CTAs for plans of 64 rows
+    per pass in the row layout (their tensor memory fits an SM), and the
+    mma.sync ones in the split layout; both give the oracle's attention."""
+    wl = _sampling(*SAMPLING[idx])
+    dev, host = host_values(wl, "cpu", layout=layout)
+    r = oracle_step(wl, host)
+    g = gpu_step(wl, dev, decode=False)
+    lens = g["lens"].cpu().numpy()
+    plan, info = pa.shared_prefix_plan(g["host_tables"], lens, wl.block_size, wl.num_q_heads, wl.num_kv_heads)
+    assert int(plan[7]) == 64
+    plan_d = plan.cuda()
+    assert pa.pa_decode_shared_tc(g["k_cache"], wl.num_seqs, wl.num_q_heads, plan_d) == (layout == "row")
+    out = pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale, shared_plan=plan_d)
+    assert pa.pa_get_device_error(raise_on_error=False) == 0
+    assert max_abs_err(out, oracle_decode(wl, host, r)) <= TOL["bf16"]
