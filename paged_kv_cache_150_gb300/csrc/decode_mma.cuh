@@ -222,8 +222,8 @@ __device__ __forceinline__ void mma_block_tiles(uint32_t kslab, uint32_t vslab, 
 // The TMA producer of a shared-prefix CTA (one thread): its range [lo, lo + n)
 // of the flattened (stage head group, virtual sequence, block) list through a
 // ring of S stages of stage_bytes, nhb one-head boxes of K then of V per
-// stage (tile_bytes each).  Each block is read through the table row of its
-// group's first member.
+// stage (tile_bytes each).  Each block is read through the table row of the
+// sequence of the pass's first query row (a member of the group).
 template <int D, int B, int LAYOUT>
 __device__ __forceinline__ void shared_prefix_producer(uint8_t *smem, uint64_t *full, uint64_t *empty, int S,
                                                        uint32_t stage_bytes, uint32_t tile_bytes, int32_t nhb,
@@ -240,10 +240,10 @@ __device__ __forceinline__ void shared_prefix_producer(uint8_t *smem, uint64_t *
     BlockCursor cur, ahead;
     cur.init_at(lo, sh.start_s[c], pv.cu_s, V);
     ahead.init_at(lo, sh.start_s[c], pv.cu_s, V);
-    // table row of a virtual sequence: its group's first member
-    auto rep_row = [&](int32_t v) {
-        return (int64_t)pv.members[pv.group_begin[pv.vgroup[v]]] * max_blocks;
-    };
+    // table row of a virtual sequence: the sequence of its first query row
+    // (the plan kernel's row table), a member of the group that shares the
+    // prefix: one load rather than the chain through the plan's arrays
+    auto rep_row = [&](int32_t v) { return (int64_t)sh.rowseq[(int64_t)v * pv.R] * max_blocks; };
     int32_t ahead_v = ahead.seq;
     int64_t ahead_row = rep_row(ahead_v);
     constexpr int PD = kTablePrefetch;
@@ -310,7 +310,7 @@ __device__ __forceinline__ void shared_prefix_producer(uint8_t *smem, uint64_t *
 // entries cut over Ce_s CTAs, nhb = plan_stage_heads(R) KV heads per stage.
 // The ring has the own-block CTAs' bytes, cut into 2, 4 or 8 stages of nhb
 // one-head TMA boxes of K and of V (tmk1 / tmv1).  Each block of a group's
-// prefix is read once per pass (the table of the group's first member), and
+// prefix is read once per pass (the table of one of its members), and
 // warp w applies head hg * nhb + w / (R / 16) of the stage to its 16 query
 // rows of the pass (member m = row / G, query head h = kvh * G + row % G), as
 // two 8-column MMA tiles; a warp whose rows are all past the group's rows

@@ -159,7 +159,7 @@ __device__ __forceinline__ int tc_round_blocks(const BlockCursor &cur, int64_t i
 
 // The TMA producer of a tcgen05 shared-prefix CTA (one thread): round r into
 // slot r % 2, each block as 2 * D/64 one-panel boxes (tmkp / tmvp), through
-// the table row of its group's first member.
+// the table row of the sequence of the pass's first query row.
 template <int D, int B>
 __device__ __forceinline__ void shared_prefix_producer_tc(uint8_t *slots, uint64_t *full, uint64_t *empty,
                                                           const CUtensorMap *tmkp, const CUtensorMap *tmvp,
@@ -175,7 +175,8 @@ __device__ __forceinline__ void shared_prefix_producer_tc(uint8_t *slots, uint64
     BlockCursor cur, ahead;
     cur.init_at(lo, sh.start_s[c], pv.cu_s, V);
     ahead = cur;
-    auto rep_row = [&](int32_t v) { return (int64_t)pv.members[pv.group_begin[pv.vgroup[v]]] * max_blocks; };
+    // table row of a virtual sequence: the sequence of its first query row
+    auto rep_row = [&](int32_t v) { return (int64_t)sh.rowseq[(int64_t)v * pv.R] * max_blocks; };
     int32_t ahead_v = ahead.seq;
     int64_t ahead_row = rep_row(ahead_v);
     constexpr int PD = kTablePrefetch;
