@@ -130,9 +130,11 @@ __host__ __device__ constexpr uint32_t tc_idesc_bf16(int M, int N, bool a_mn_maj
 // p at p * kPanel, V panel p at (D/64 + p) * kPanel, token t of the round at
 // line t of each (128-byte lines, 128-byte swizzle, as TMA writes a box of
 // B lines).  So the round's tokens are one operand of N = 64 (S = Q K^T) and
-// of K = 64 (O += P V).  The MMAs are M = 128: rows 64..127 of P read Q's
-// bytes and those of Q's last panel read slot 0; those rows' results land in
-// tensor-memory lanes that are never read.
+// of K = 64 (O += P V).  The MMAs are M = 128: in the first half rows
+// 64..127 of P read Q's bytes and those of Q's last panel read slot 0; the
+// second half's descriptors start 8 KiB before P and Q, so its rows 0..63
+// read the bytes before them.  Those rows' results land in tensor-memory
+// lanes that are never read.
 template <int D, int B>
 struct TcSmem {
     static constexpr int kPanels = D / 64;
@@ -242,8 +244,11 @@ __device__ __forceinline__ void shared_prefix_producer_tc(uint8_t *slots, uint64
 // tokens of one segment.  Thread 0 issues the MMAs.  A consumer thread owns
 // the tensor-memory lane its warp reaches (CTA warp w: lanes 32 (w % 4) ..,
 // so the halves' consumer warps cover the four quadrants in different
-// orders); lane t < 64 is query row t of the pass (member t / G, query head
-// kvh * G + t % G).  Per round:
+// orders); lane rbase + t holds query row t < 64 of the pass (member t / G,
+// query head kvh * G + t % G), rbase = 0 in the first half and 64 in the
+// second (its Q and P descriptors start 8 KiB early, so its rows sit in
+// quadrants 2 and 3 and the halves' softmax warps use different SM
+// partitions).  Per round:
 //   S[rows][64] = Q K^T   (D/16 MMAs of N = the round's tokens),
 //   rows: lazy running maximum, P = 2^(x - m) to shared memory as bf16,
 //   O[rows][D] += P V     (one MMA of N = D per 16 tokens).
@@ -304,10 +309,17 @@ __device__ __forceinline__ void shared_prefix_cta_tc(uint8_t *smem, const CUtens
     // -------------------------------------------------------- consumers
     const int row = (int)((threadIdx.x >> 5) & 3) * 32 + lane;  // this thread's tensor-memory lane
     const uint32_t t_lane = (uint32_t)(row & ~31) << 16;
+    // The second half keeps its query rows in lanes 64..127 (quadrants 2 and
+    // 3), so that the two halves' softmax warps run on different SM
+    // partitions: its Q and P descriptors start 8 KiB before the rows (rows
+    // 0..63 of its products read the preceding bytes and are never used).
+    const int rbase = half ? 64 : 0;
+    const int qi = row - rbase;  // query row of the pass this lane holds (0..63), if any
+    const uint32_t a_shift = half ? 8192u : 0u;
     const uint32_t tS = tmem, tO = tmem + 64;
     const uint32_t q_base = smem_u32(Qs), p_base = smem_u32(Ps), slot_base = smem_u32(slots);
     float m_run = -INFINITY, l_run = 0.f;
-    bool valid = false;      // this thread's row belongs to a member (row < 64)
+    bool valid = false;      // this thread's lane holds a query row of a member
     bool warp_rows = false;  // some row of this warp does
     bool seg_start = true, first_round = true, abort = false;
     uint32_t sph = 0, oph = 0;
@@ -337,7 +349,7 @@ __device__ __forceinline__ void shared_prefix_cta_tc(uint8_t *smem, const CUtens
                 *reinterpret_cast<uint4 *>(Qs + (ch >> 3) * L::kPanel + i * 128 + (((ch & 7) ^ (i & 7)) << 4)) = val[k];
             }
             fence_proxy_async_smem();
-            valid = row < 64 && sh.rowseq[(int64_t)v * 64 + row] >= 0;
+            valid = qi >= 0 && qi < 64 && sh.rowseq[(int64_t)v * 64 + qi] >= 0;
             warp_rows = __any_sync(0xffffffffu, valid);
             m_run = -INFINITY;
             l_run = 0.f;
@@ -355,7 +367,7 @@ __device__ __forceinline__ void shared_prefix_cta_tc(uint8_t *smem, const CUtens
 #pragma unroll
             for (int k = 0; k < KT; ++k) {
                 const uint32_t koff = (uint32_t)(k >> 2) * L::kPanel + (uint32_t)(k & 3) * 32;
-                const uint64_t a = smem_desc_sw128(q_base + koff, 16, 1024);  // Q panels have the same stride
+                const uint64_t a = smem_desc_sw128(q_base - a_shift + koff, 16, 1024);  // Q panels: the same stride
                 tc_mma_bf16(tS, a, smem_desc_sw128(kbase + koff, 16, 1024), idesc, k > 0 ? 1u : 0u);
             }
             tc_commit(smem_u32(sbar));
@@ -397,8 +409,8 @@ __device__ __forceinline__ void shared_prefix_cta_tc(uint8_t *smem, const CUtens
                 }
             }
             const float mref = valid ? m_run : 0.f;  // rows outside the pass: finite zeros
-            // P row (rows < 64: quadrants 0 and 1) as bf16, one 16-byte chunk
-            // of 8 tokens at a time, in the 128-byte-swizzled K-major layout.
+            // P row qi as bf16, one 16-byte chunk of 8 tokens at a time, in the
+            // 128-byte-swizzled K-major layout.
             float lsum = 0.f;
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
@@ -411,8 +423,8 @@ __device__ __forceinline__ void shared_prefix_cta_tc(uint8_t *smem, const CUtens
                     lsum += p0 + p1;
                     w[k] = pack_bf16x2(p0, p1);
                 }
-                if (row < 64)
-                    *reinterpret_cast<uint4 *>(Ps + row * 128 + ((ch ^ (row & 7)) << 4)) =
+                if (qi >= 0 && qi < 64)
+                    *reinterpret_cast<uint4 *>(Ps + qi * 128 + ((ch ^ (qi & 7)) << 4)) =
                         make_uint4(w[0], w[1], w[2], w[3]);
             }
             l_run += lsum;
@@ -423,7 +435,7 @@ __device__ __forceinline__ void shared_prefix_cta_tc(uint8_t *smem, const CUtens
         if (tid == 0) {
             tc_fence_after();
             for (int j = 0; j < ntok / 16; ++j) {
-                const uint64_t a = smem_desc_sw128(p_base + (uint32_t)j * 32, 16, 1024);
+                const uint64_t a = smem_desc_sw128(p_base - a_shift + (uint32_t)j * 32, 16, 1024);
                 const uint64_t bv = smem_desc_sw128(vbase + (uint32_t)j * 2048, L::kPanel, 1024);
                 tc_mma_bf16(tO, a, bv, IDESC_O, first_round && j == 0 ? 0u : 1u);
             }
@@ -440,7 +452,7 @@ __device__ __forceinline__ void shared_prefix_cta_tc(uint8_t *smem, const CUtens
             tc_fence_after();
             if (warp_rows) {
                 const int64_t slot_p = partial_slot(c, kvh * V + v);
-                const int64_t prow = slot_p * kPlanSlotRows + row;
+                const int64_t prow = slot_p * kPlanSlotRows + qi;
                 float *ab = sh.acc_s + prow * D;
 #pragma unroll 1
                 for (int d0 = 0; d0 < D; d0 += 32) {
