@@ -241,7 +241,8 @@ __device__ __forceinline__ void shared_prefix_producer_tc(uint8_t *slots, uint64
 // A shared-prefix CTA on tcgen05 (plans of 64 rows per pass: one KV head
 // per segment), one half of a two-half CTA.  Warp 4 of the half streams the
 // CTA's range of (KV head, virtual sequence, block) in rounds of up to 64
-// tokens of one segment.  Thread 0 issues the MMAs.  A consumer thread owns
+// tokens of one segment.  A consumer thread of a warp without query rows
+// issues the MMAs.  A consumer thread owns
 // the tensor-memory lane its warp reaches (CTA warp w: lanes 32 (w % 4) ..,
 // so the halves' consumer warps cover the four quadrants in different
 // orders); lane rbase + t holds query row t < 64 of the pass (member t / G,
@@ -316,6 +317,10 @@ __device__ __forceinline__ void shared_prefix_cta_tc(uint8_t *smem, const CUtens
     const int rbase = half ? 64 : 0;
     const int qi = row - rbase;  // query row of the pass this lane holds (0..63), if any
     const uint32_t a_shift = half ? 8192u : 0u;
+    // The MMAs are issued by lane 0 of a consumer warp that holds no query
+    // rows (quadrant 2 in the first half, quadrant 1 in the second), so that
+    // a softmax warp never waits on a full MMA queue.
+    const int issuer = half ? 0 : 64;
     const uint32_t tS = tmem, tO = tmem + 64;
     const uint32_t q_base = smem_u32(Qs), p_base = smem_u32(Ps), slot_base = smem_u32(slots);
     float m_run = -INFINITY, l_run = 0.f;
@@ -357,7 +362,7 @@ __device__ __forceinline__ void shared_prefix_cta_tc(uint8_t *smem, const CUtens
             named_bar_sync(cons_bar, 4 * 32);  // Q complete before the first S MMA
             seg_start = false;
         }
-        if (tid == 0) {
+        if (tid == issuer) {
             if (!abort && !mbar_wait_bounded(smem_u32(&full[slot]), (uint32_t)((r >> 1) & 1))) {
                 atomicOr(err, kErrTimeout);
                 abort = true;  // the MMAs still run (on stale tiles), so that every wait below ends
@@ -432,7 +437,7 @@ __device__ __forceinline__ void shared_prefix_cta_tc(uint8_t *smem, const CUtens
         }
         tc_fence_before();
         named_bar_sync(cons_bar, 4 * 32);  // P written, S and O reads done
-        if (tid == 0) {
+        if (tid == issuer) {
             tc_fence_after();
             for (int j = 0; j < ntok / 16; ++j) {
                 const uint64_t a = smem_desc_sw128(p_base - a_shift + (uint32_t)j * 32, 16, 1024);
