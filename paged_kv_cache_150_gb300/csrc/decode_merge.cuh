@@ -434,25 +434,41 @@ __global__ void __launch_bounds__(256) long_merge_kernel(
 // group, KV head).  The piece ranges depend only on the plan kernel's output,
 // so they are worked out before waiting for the attention launch (which lets
 // this grid start as its CTAs finish); only the pieces are read after it.
+// Every thread waits, also those with nothing to merge (a rejected plan, a
+// sequence computed without sharing): this grid must not end before the
+// attention launch, since work after it on the stream may rely on both.
 template <int D>
-__global__ void __launch_bounds__(256) shared_merge_kernel(
+__global__ void __launch_bounds__(256, 2) shared_merge_kernel(
     __nv_bfloat16 *__restrict__ out, const int32_t *__restrict__ cu, int32_t N, int32_t H, int32_t Hk, int32_t G,
     int32_t NH, int32_t C, const float2 *__restrict__ ml_ws, const float *__restrict__ acc_ws, const SharedArgs sh) {
     const int32_t Cs = sh.ctl[0];
-    if (Cs <= 0) return;  // plan rejected: every sequence was merged in the attention launch
-    const SharedView sv = shared_view(sh.plan, sh.skip, sh.ml_s, sh.acc_s, Hk, Cs);
     const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (wid >= (int64_t)sv.pv.M * Hk) return;
-    const int32_t seq = sv.pv.members[wid / Hk];
-    const int32_t kvh = (int32_t)(wid % Hk);
-    if (sh.skip[seq] <= 0) return;  // computed without sharing: merged in the attention launch
-    const int64_t W = (int64_t)(Hk / NH) * cu[N];
-    const int32_t Ce = (int32_t)(W < (int64_t)(C - Cs) ? W : (int64_t)(C - Cs));
-    const PieceRange rg[2] = {own_range(ml_ws, acc_ws, cu, N, seq, kvh / NH, kvh % NH, G, NH * G, W, Ce),
-                              shared_range(sv, seq, kvh, G)};
+    int32_t seq = -1, kvh = 0;
+    PieceRange own = no_range(), shr = no_range();
+    // Cs <= 0: plan rejected, every sequence was merged in the attention launch
+    if (Cs > 0) {
+        const SharedView sv = shared_view(sh.plan, sh.skip, sh.ml_s, sh.acc_s, Hk, Cs);
+        if (wid < (int64_t)sv.pv.M * Hk) {
+            seq = sv.pv.members[wid / Hk];
+            kvh = (int32_t)(wid % Hk);
+            if (sh.skip[seq] > 0) {
+                const int64_t W = (int64_t)(Hk / NH) * cu[N];
+                const int32_t Ce = (int32_t)(W < (int64_t)(C - Cs) ? W : (int64_t)(C - Cs));
+                own = own_range(ml_ws, acc_ws, cu, N, seq, kvh / NH, kvh % NH, G, NH * G, W, Ce);
+                shr = shared_range(sv, seq, kvh, G);
+            } else {
+                seq = -1;  // computed without sharing: merged in the attention launch
+            }
+        }
+    }
     grid_dependency_wait();  // the attention launch's pieces
-    merge_online<__nv_bfloat16, D, 2>(out + ((int64_t)seq * H + (int64_t)kvh * G) * D, rg, G, lane);
+    if (seq >= 0) {
+        // the ranges' arrays are these parameters: only their indexes were kept across the wait
+        const PieceRange rg[2] = {PieceRange{ml_ws, acc_ws, own.base, own.stride, own.col, own.c0, own.c1},
+                                  PieceRange{sh.ml_s, sh.acc_s, shr.base, shr.stride, shr.col, shr.c0, shr.c1}};
+        merge_online<__nv_bfloat16, D, 2>(out + ((int64_t)seq * H + (int64_t)kvh * G) * D, rg, G, lane);
+    }
 }
 
 }  // namespace pa
