@@ -224,6 +224,29 @@ def test_plan_that_does_not_match_is_reported_and_ignored(corrupt):
     assert max_abs_err(out, oracle_decode(wl, host, r)) <= TOL["bf16"]
 
 
+def test_back_to_back_calls_on_one_workspace_with_a_rejected_plan():
+    """Calls queued on one stream and one workspace with no synchronisation
+    between them, alternating a rejected plan (its merge grid has nothing to
+    merge, and the call's attention launch takes every sequence) and a good
+    one.  Each call's plan kernel re-zeroes the arrival counters the previous
+    call's attention launch counts on, so every output matching the oracle
+    shows that no call's work overlapped the one before it."""
+    wl, host, r, g, plan, lens = _plan_case()
+    bad = plan.clone()
+    bad[0] = 0  # not a plan: rejected on the device
+    plans = [bad.cuda(), plan.cuda()]
+    ref = oracle_decode(wl, host, r)
+    ws = torch.empty(pa.pa_decode_workspace_bytes(g["k_cache"], wl.num_seqs, wl.num_q_heads, shared=True),
+                     dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    outs = [pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale, workspace=ws,
+                         shared_plan=plans[i % 2]) for i in range(12)]
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error(raise_on_error=False) == pa._lib.PA_ERR_DEVICE_PLAN
+    for out in outs:
+        assert max_abs_err(out, ref) <= TOL["bf16"]
+
+
 def test_plan_with_one_cta_is_ignored_quietly():
     wl, host, r, g, plan, lens = _plan_case()
     out = pa.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["tables"], g["lens"], wl.scale, num_splits=1,
